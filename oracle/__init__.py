@@ -1,0 +1,200 @@
+"""Float64 CPU oracle for the chunked LM-head cross-entropy.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product path
+(``chunked_lm_head_gemm_gb300``) does not import it and shares no code with
+it. The arithmetic lives in ``lce_oracle.c`` (plain C, float64, pthreads);
+this module only compiles it with gcc and marshals arguments.
+
+What it follows: "Training Beyond 1M Tokens" (TRL guide), sections "The loss
+is the first thing to break" (logits = hidden x LM-head weights, then a
+cross entropy against the labels) and "The massive logits matrix: chunk it"
+(the loss is a sum over rows; the softmax runs along one row's vocabulary).
+The reduction the pages leave open is: mean over rows whose label is neither
+ignore_index nor outside [0, V); 0 when no row is valid.
+
+Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lce_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liblce_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+# Status codes returned by the C functions.
+OK = 0
+BAD_ARG = 1
+LABEL_RANGE = 4
+NO_MEMORY = 7
+
+DT_BF16, DT_F32, DT_F64 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile lce_oracle.c into liblce_oracle.so next to it (gcc, -O2)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared",
+                    "-pthread", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Open a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    p, i64, i32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                        ctypes.c_double)
+    lib.lce_oracle_forward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
+                                       i32, p, p, p, p]
+    lib.lce_oracle_forward.restype = i32
+    lib.lce_oracle_backward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
+                                        f64, i32, p, p]
+    lib.lce_oracle_backward.restype = i32
+    lib.lce_oracle_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64, f64, p,
+                                    i64, i32, p, p, p]
+    lib.lce_oracle_rows.restype = i32
+    lib.lce_oracle_count_valid.argtypes = [p, i64, i64, i64, p]
+    lib.lce_oracle_count_valid.restype = i64
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def _as_input(x):
+    """Return (contiguous numpy array, dtype code) for h or W.
+
+    Accepts numpy float32/float64 arrays and torch CPU tensors of dtype
+    bfloat16/float32/float64 (bf16 is passed as its raw 16-bit patterns)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), DT_BF16
+            x = x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, DT_F32
+    if x.dtype == np.float64:
+        return x, DT_F64
+    if x.dtype == np.uint16:
+        return x, DT_BF16
+    raise TypeError(f"oracle input dtype {x.dtype} not supported")
+
+
+def _labels(y):
+    try:
+        import torch
+        if isinstance(y, torch.Tensor):
+            y = y.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(y, dtype=np.int64)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None):
+    """Returns dict(loss, lse[L], zy[L], n_valid, status) in float64."""
+    hn, dt = _as_input(h)
+    Wn, dt2 = _as_input(W)
+    if dt != dt2:
+        raise TypeError("h and W must have the same dtype")
+    y = _labels(labels)
+    L, H = hn.shape
+    V = Wn.shape[0]
+    assert Wn.shape[1] == H and y.shape == (L,)
+    lse = np.empty(L, np.float64)
+    zy = np.empty(L, np.float64)
+    loss = np.zeros(1, np.float64)
+    nv = np.zeros(1, np.int64)
+    st = _load().lce_oracle_forward(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
+                                    ignore_index, nthreads or default_threads(),
+                                    _ptr(lse), _ptr(zy), _ptr(loss), _ptr(nv))
+    if st not in (OK, LABEL_RANGE):
+        raise RuntimeError(f"lce_oracle_forward status {st}")
+    return dict(loss=float(loss[0]), lse=lse, zy=zy, n_valid=int(nv[0]),
+                status=st)
+
+
+def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
+             want_dH: bool = True, want_dW: bool = True,
+             nthreads: int | None = None):
+    """Returns dict(dH[L,H] or None, dW[V,H] or None, status) in float64."""
+    hn, dt = _as_input(h)
+    Wn, dt2 = _as_input(W)
+    if dt != dt2:
+        raise TypeError("h and W must have the same dtype")
+    y = _labels(labels)
+    L, H = hn.shape
+    V = Wn.shape[0]
+    dH = np.empty((L, H), np.float64) if want_dH else None
+    dW = np.empty((V, H), np.float64) if want_dW else None
+    st = _load().lce_oracle_backward(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
+                                     ignore_index, float(dloss),
+                                     nthreads or default_threads(), _ptr(dH),
+                                     _ptr(dW))
+    if st not in (OK, LABEL_RANGE):
+        raise RuntimeError(f"lce_oracle_backward status {st}")
+    return dict(dH=dH, dW=dW, status=st)
+
+
+def rows(h, W, labels, rows, dloss: float = 1.0, ignore_index: int = -100,
+         want_dH: bool = True, nthreads: int | None = None):
+    """Selected rows of a problem of any size (N counted over all labels).
+
+    Returns dict(lse[n], zy[n], dH[n,H] or None, status) in float64."""
+    hn, dt = _as_input(h)
+    Wn, dt2 = _as_input(W)
+    if dt != dt2:
+        raise TypeError("h and W must have the same dtype")
+    y = _labels(labels)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    L, H = hn.shape
+    V = Wn.shape[0]
+    n = r.shape[0]
+    lse = np.empty(n, np.float64)
+    zy = np.empty(n, np.float64)
+    dH = np.empty((n, H), np.float64) if want_dH else None
+    st = _load().lce_oracle_rows(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
+                                 ignore_index, float(dloss), _ptr(r), n,
+                                 nthreads or default_threads(), _ptr(lse),
+                                 _ptr(zy), _ptr(dH))
+    if st not in (OK, LABEL_RANGE):
+        raise RuntimeError(f"lce_oracle_rows status {st}")
+    return dict(lse=lse, zy=zy, dH=dH, status=st)
+
+
+def count_valid(labels, V: int, ignore_index: int = -100):
+    """Returns (N, any_label_out_of_range)."""
+    y = _labels(labels)
+    bad = ctypes.c_int(0)
+    n = _load().lce_oracle_count_valid(_ptr(y), y.shape[0], V, ignore_index,
+                                       ctypes.byref(bad))
+    return int(n), bool(bad.value)

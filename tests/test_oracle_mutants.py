@@ -1,0 +1,79 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case copies lce_oracle.c, plants one plausible mistake (a dropped
+term, a wrong sign, a wrong index, a transposed operand, a wrong
+normaliser), compiles the copy into a temporary library and checks that
+the pins of tests/test_oracle_pins.py reject it. Runs on the CPU only.
+"""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTANTS = {
+    "drop_onehot": ("g[y] -= jb->gscale;", "(void)y;"),
+    "onehot_sign": ("g[y] -= jb->gscale;", "g[y] += jb->gscale;"),
+    "lse_drops_max": ("return m + log(s);", "return log(s);"),
+    "softmax_unshifted": ("g[j] = jb->gscale * exp(z[j] - lse);",
+                          "g[j] = jb->gscale * exp(z[j]);"),
+    "dot_wrong_index": ("acc += x[k] * (double)f;",
+                        "acc += x[(k + 1) % H] * (double)f;"),
+    "dot_wrong_index_f64": ("for (int64_t k = 0; k < H; ++k) acc += x[k] * w[k];",
+                            "for (int64_t k = 0; k < H; ++k) acc += x[k] * w[H - 1 - k];"),
+    "dW_transposed": ("const double *hr = jb->hd + i * jb->H;",
+                      "const double *hr = jb->hd + (j % jb->L) * jb->H;"),
+    "dH_uses_h": ("if (g[j] != 0.0) axpy_row(g[j], jb->W, jb->dtype, j, jb->H, out);",
+                  "if (g[j] != 0.0) axpy_row(g[j], jb->W, jb->dtype, (j + 1) % jb->V, jb->H, out);"),
+    "mean_over_all_rows": ("if (loss) *loss = n > 0 ? total / (double)n : 0.0;",
+                           "if (loss) *loss = n > 0 ? total / (double)L : 0.0;"),
+    "grad_scale_all_rows": ("proto.gscale = n > 0 ? dloss / (double)n : 0.0;\n        st = run_rows(proto, L, nthreads);",
+                            "proto.gscale = n > 0 ? dloss / (double)L : 0.0;\n        st = run_rows(proto, L, nthreads);"),
+    "ignored_rows_count": ("if (label_is_valid(labels[i], V, ignore_index))\n            ++n;",
+                           "if (labels[i] != ignore_index || 1)\n            ++n;"),
+}
+
+PIN_CHECKS = [
+    lambda o: pins.test_hand_worked_example(o),
+    lambda o: pins.test_against_torch_cross_entropy_f64(o, 37, 19, 53, 2),
+    lambda o: pins.test_low_precision_inputs_are_widened_exactly(
+        o, pins.torch.bfloat16),
+    lambda o: pins.test_finite_differences(o),
+    lambda o: pins.test_w_zero_closed_form(o, 4096),
+    lambda o: pins.test_v2_is_logistic_loss(o),
+    lambda o: pins.test_invariants(o),
+    lambda o: pins.test_all_ignored_and_bad_labels(o),
+]
+
+
+def _caught(mod) -> bool:
+    for check in PIN_CHECKS:
+        try:
+            check(mod)
+        except (AssertionError, RuntimeError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread",
+                    "-o", str(so), str(mutant), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(so)))
+    assert _caught(oracle), f"planted mistake {name} passed every pin"
+
+
+def test_unmutated_passes_all_pins(oracle_mod):
+    assert not _caught(oracle_mod)
