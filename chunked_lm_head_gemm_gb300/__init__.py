@@ -1,0 +1,22 @@
+"""Fused linear cross-entropy (the chunked LM-head loss) for NVIDIA GB300.
+
+loss = mean over valid rows of the cross entropy of logits = h W^T against
+integer labels, forward and backward, without ever holding the L x V logits
+("Training Beyond 1M Tokens", sections "The loss is the first thing to
+break" and "The massive logits matrix: chunk it"). The arithmetic runs in
+hand-written sm_103a kernels (tcgen05 tensor cores, TMA) behind the C ABI in
+include/lce.h; this package is the thin Python binding.
+
+    import chunked_lm_head_gemm_gb300 as lce
+    loss = lce.linear_cross_entropy(h, W, labels)       # autograd-aware
+    loss, lse = lce.forward(h, W, labels)
+    dH, dW = lce.backward(h, W, labels, lse, dloss)
+"""
+from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
+                       alloc_workspace, backward, default_chunk_rows, forward,
+                       get_error, library_path, linear_cross_entropy, load,
+                       workspace_size)
+
+__all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "alloc_workspace",
+           "backward", "default_chunk_rows", "forward", "get_error",
+           "library_path", "linear_cross_entropy", "load", "workspace_size"]

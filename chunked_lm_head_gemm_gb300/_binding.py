@@ -1,0 +1,238 @@
+"""ctypes binding of liblce.so (include/lce.h): argument marshalling only.
+
+Every step of the loss runs in the library's CUDA kernels; this module only
+checks tensors, passes their device pointers and the current CUDA stream,
+and raises on a non-OK status. There is no fallback: if the library is not
+built or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+LCE_OK = 0
+LCE_ERR_INVALID_ARG = 1
+LCE_ERR_UNSUPPORTED = 2
+LCE_ERR_WORKSPACE = 3
+LCE_ERR_LABEL_RANGE = 4
+LCE_ERR_TIMEOUT = 5
+LCE_ERR_CUDA = 6
+
+LCE_BF16 = 0
+LCE_F32 = 1
+
+IGNORE_INDEX = -100
+
+EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
+            "lce_backward", "lce_get_error", "lce_status_string",
+            "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout")
+
+
+class LCEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib
+        name = lib.lce_status_string(status).decode() if lib else str(status)
+        detail = lib.lce_last_cuda_error().decode() if lib else ""
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Open liblce.so and declare the C signatures. Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"CUDA library not built: {path} is missing "
+                    "(run __graft_entry__.build() or python -m "
+                    "chunked_lm_head_gemm_gb300.build)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        p, i64, i32, u64, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                ctypes.c_uint64, ctypes.c_size_t)
+        lib.lce_workspace_size.argtypes = [i64, i64, i64, i32, i64]
+        lib.lce_workspace_size.restype = sz
+        lib.lce_default_chunk_rows.argtypes = [i64, i64, i64]
+        lib.lce_default_chunk_rows.restype = i64
+        lib.lce_forward.argtypes = [p, p, i32, p, i64, i64, i64, i64, p, p, p,
+                                    sz, p]
+        lib.lce_forward.restype = i32
+        lib.lce_backward.argtypes = [p, p, i32, p, p, i64, i64, i64, i64, p,
+                                     i64, p, p, p, sz, p]
+        lib.lce_backward.restype = i32
+        lib.lce_get_error.argtypes = [p]
+        lib.lce_get_error.restype = i32
+        lib.lce_status_string.argtypes = [i32]
+        lib.lce_status_string.restype = ctypes.c_char_p
+        lib.lce_last_cuda_error.argtypes = []
+        lib.lce_last_cuda_error.restype = ctypes.c_char_p
+        lib.lce_test_gemm.argtypes = [p, p, p, i64, i64, i64, i32, i32, p]
+        lib.lce_test_gemm.restype = i32
+        lib.lce_test_wait_timeout.argtypes = [u64, p]
+        lib.lce_test_wait_timeout.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != LCE_OK:
+        raise LCEError(status, where)
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return LCE_BF16
+    if t.dtype == torch.float32:
+        return LCE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _check_inputs(h, W, labels):
+    if not (h.is_cuda and W.is_cuda and labels.is_cuda):
+        raise ValueError("h, W and labels must be CUDA tensors")
+    if h.dim() != 2 or W.dim() != 2 or labels.dim() != 1:
+        raise ValueError("expected h [L,H], W [V,H], labels [L]")
+    if h.shape[1] != W.shape[1] or labels.shape[0] != h.shape[0]:
+        raise ValueError(f"shape mismatch: h {tuple(h.shape)}, W "
+                         f"{tuple(W.shape)}, labels {tuple(labels.shape)}")
+    if h.dtype != W.dtype:
+        raise TypeError("h and W must have the same dtype")
+    if labels.dtype != torch.int64:
+        raise TypeError("labels must be int64")
+    if not (h.is_contiguous() and W.is_contiguous() and labels.is_contiguous()):
+        raise ValueError("h, W and labels must be contiguous")
+
+
+def workspace_size(L: int, H: int, V: int, dtype=torch.bfloat16,
+                   chunk_rows: int = 0) -> int:
+    code = LCE_BF16 if dtype == torch.bfloat16 else LCE_F32
+    n = load().lce_workspace_size(L, H, V, code, chunk_rows)
+    if n == 0:
+        raise ValueError(f"invalid sizes L={L} H={H} V={V} chunk={chunk_rows}")
+    return n
+
+
+def default_chunk_rows(L: int, H: int, V: int) -> int:
+    return load().lce_default_chunk_rows(L, H, V)
+
+
+def alloc_workspace(L, H, V, dtype, chunk_rows, device) -> torch.Tensor:
+    return torch.empty(workspace_size(L, H, V, dtype, chunk_rows),
+                       dtype=torch.uint8, device=device)
+
+
+def forward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
+            ignore_index: int = IGNORE_INDEX, workspace=None,
+            loss_out=None, lse_out=None):
+    """Returns (loss [scalar fp32], lse [L] fp32), both on h's device."""
+    lib = load()
+    _check_inputs(h, W, labels)
+    L, H = h.shape
+    V = W.shape[0]
+    dev = h.device
+    if workspace is None:
+        workspace = alloc_workspace(L, H, V, h.dtype, 0, dev)
+    loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float32, device=dev)
+    lse = lse_out if lse_out is not None else torch.empty(L, dtype=torch.float32, device=dev)
+    st = lib.lce_forward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                         labels.data_ptr(), L, H, V, ignore_index,
+                         loss.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), _stream_ptr(dev))
+    _check(st, "lce_forward")
+    return loss, lse
+
+
+def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
+             lse: torch.Tensor, dloss: torch.Tensor,
+             ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
+             workspace=None, dH_out=None, dW_out=None):
+    """Returns (dH [L,H] of h's dtype, dW [V,H] fp32)."""
+    lib = load()
+    _check_inputs(h, W, labels)
+    L, H = h.shape
+    V = W.shape[0]
+    dev = h.device
+    if lse.dtype != torch.float32 or lse.shape != (L,) or not lse.is_cuda:
+        raise ValueError("lse must be a CUDA float32 [L] tensor")
+    dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
+    if workspace is None:
+        workspace = alloc_workspace(L, H, V, h.dtype, chunk_rows, dev)
+    dH = dH_out if dH_out is not None else torch.empty_like(h)
+    dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
+    st = lib.lce_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                          labels.data_ptr(), lse.data_ptr(), L, H, V,
+                          ignore_index, dloss.data_ptr(), chunk_rows,
+                          dH.data_ptr(), dW.data_ptr(), workspace.data_ptr(),
+                          workspace.numel(), _stream_ptr(dev))
+    _check(st, "lce_backward")
+    return dH, dW
+
+
+def get_error(device=None) -> int:
+    """Synchronises the current stream and returns (and clears) the device
+    error status: LCE_OK, LCE_ERR_LABEL_RANGE or LCE_ERR_TIMEOUT."""
+    return load().lce_get_error(_stream_ptr(device))
+
+
+def tc_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int,
+              a_mn: bool, b_mn: bool) -> torch.Tensor:
+    """D = A B (fp32) through the tensor-core building block.
+    A: [M,K] if not a_mn else [K,M]; B: [N,K] if not b_mn else [K,N]."""
+    lib = load()
+    D = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    st = lib.lce_test_gemm(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                           int(a_mn), int(b_mn), _stream_ptr(A.device))
+    _check(st, "lce_test_gemm")
+    return D
+
+
+def wait_timeout_probe(timeout_ns: int, device=None):
+    st = load().lce_test_wait_timeout(timeout_ns, _stream_ptr(device))
+    _check(st, "lce_test_wait_timeout")
+
+
+class LinearCrossEntropy(torch.autograd.Function):
+    """loss = mean cross entropy of h W^T against labels, without the logits.
+
+    Forward saves only lse [L] (4 bytes per row); backward recomputes the
+    logits chunk by chunk in the library."""
+
+    @staticmethod
+    def forward(ctx, h, W, labels, ignore_index=IGNORE_INDEX, chunk_rows=0):
+        loss, lse = forward(h, W, labels, ignore_index)
+        ctx.save_for_backward(h, W, labels, lse)
+        ctx.ignore_index = ignore_index
+        ctx.chunk_rows = chunk_rows
+        return loss
+
+    @staticmethod
+    def backward(ctx, dloss):
+        h, W, labels, lse = ctx.saved_tensors
+        dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,
+                          ctx.chunk_rows)
+        return dH, dW.to(W.dtype), None, None, None
+
+
+def linear_cross_entropy(h, W, labels, ignore_index: int = IGNORE_INDEX,
+                         chunk_rows: int = 0):
+    return LinearCrossEntropy.apply(h, W, labels, ignore_index, chunk_rows)

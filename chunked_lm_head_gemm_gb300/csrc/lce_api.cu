@@ -1,0 +1,541 @@
+// Host layer of the fused linear cross-entropy library: argument checks,
+// workspace carving, TMA tensor maps, work decomposition and the launch
+// sequence behind the C ABI declared in include/lce.h.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/lce.h"
+#include "lce_internal.h"
+
+namespace lce {
+
+// The device error word: kernels OR error bits into it, lce_get_error reads
+// and clears it. One per device (module globals are per device).
+__device__ unsigned g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 16;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+thread_local char t_last_cuda_error[256] = "";
+
+lce_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error, "%s: %s", where,
+                cudaGetErrorString(e));
+  return LCE_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  unsigned* err = nullptr;  // device address of g_error_word
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+lce_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.num_sms,
+                                    cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    // The kernels are built for sm_103a only.
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress");
+      d.err = static_cast<unsigned*>(p);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return LCE_ERR_UNSUPPORTED;
+  *out = &d;
+  return LCE_OK;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("LCE_WAIT_TIMEOUT_MS");
+    if (s && *s) {
+      const double ms = std::atof(s);
+      if (ms > 0) return static_cast<uint64_t>(ms * 1e6);
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// rows `row_bytes` apart; boxes of box_inner x box_outer with 128-byte
+// swizzle (box_inner = 64 elements = one swizzle row). Out-of-range
+// elements of a box read as zero.
+lce_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner,
+                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                     uint32_t box_outer) {
+  auto enc = tmap_encoder();
+  if (!enc) {
+    std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error,
+                  "cuTensorMapEncodeTiled not available");
+    return LCE_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error,
+                  "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, "
+                  "stride %llu",
+                  static_cast<int>(r), static_cast<unsigned long long>(inner),
+                  static_cast<unsigned long long>(outer),
+                  static_cast<unsigned long long>(row_bytes));
+    return LCE_ERR_CUDA;
+  }
+  return LCE_OK;
+}
+
+// Tensor maps of the two operand layouts the contractions read.
+// K-major: rows of the operand's M (or N) index, K contiguous; one box per
+// stage covers the whole 64-wide K slice of `rows_per_box` rows.
+lce_status tmap_kmajor(CUtensorMap* tm, const void* base, int64_t k_extent,
+                       int64_t rows, int64_t row_elems, uint32_t rows_per_box) {
+  return make_tmap(tm, base, k_extent, rows, row_elems * 2, BK, rows_per_box);
+}
+// MN-major: rows of K, the operand's M (or N) index contiguous; boxes of
+// 64 MN x 64 K, several per stage.
+lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
+                        int64_t k_rows, int64_t row_elems) {
+  return make_tmap(tm, base, mn_extent, k_rows, row_elems * 2, 64, BK);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Column-tile runs per row block for the contractions that sweep the whole
+// vocabulary (forward logits and their backward recompute). Enough runs that
+// at most ~48 MB of A row panels are live at once (they stay in L2 while
+// every CTA sweeps W), then the smallest count whose static schedule is
+// within 5% of the best one.
+void choose_splits(int num_m, int num_n, int nsm, int64_t K, int* splits,
+                   int* tps) {
+  const double panel = static_cast<double>(BM) * K * 2.0;
+  int s_min = static_cast<int>(std::ceil(nsm * panel / 48e6));
+  const int s_max = std::max(1, std::min(kMaxSplits, num_n));
+  s_min = std::max(1, std::min(s_min, s_max));
+  const double work = static_cast<double>(num_m) * num_n;
+  double best = -1.0;
+  double effs[kMaxSplits + 1] = {0};
+  for (int s = s_min; s <= s_max; ++s) {
+    const int t = static_cast<int>(ceil_div(num_n, s));
+    const int se = static_cast<int>(ceil_div(num_n, t));
+    const double units = static_cast<double>(num_m) * se;
+    const double makespan = std::ceil(units / nsm) * t;
+    effs[s] = work / (makespan * nsm);
+    best = std::max(best, effs[s]);
+  }
+  for (int s = s_min; s <= s_max; ++s) {
+    if (effs[s] >= 0.95 * best) {
+      *tps = static_cast<int>(ceil_div(num_n, s));
+      *splits = static_cast<int>(ceil_div(num_n, *tps));
+      return;
+    }
+  }
+  *tps = num_n;
+  *splits = 1;
+}
+
+GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps) {
+  GemmGeom g{};
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.num_m = static_cast<int>(ceil_div(M, BM));
+  g.num_n = static_cast<int>(ceil_div(N, BN));
+  g.num_kb = static_cast<int>(ceil_div(K, BK));
+  g.splits = splits;
+  g.tiles_per_split = tps;
+  g.num_units = g.num_m * splits;
+  g.timeout_ns = wait_timeout_ns();
+  return g;
+}
+
+// One contraction per output tile (dH, dW, the test GEMM).
+GemmGeom tile_geom(int64_t M, int64_t N, int64_t K) {
+  const int num_n = static_cast<int>(ceil_div(N, BN));
+  return make_geom(M, N, K, num_n, 1);
+}
+
+int grid_for(const GemmGeom& g, int nsm) {
+  return std::max(1, std::min(g.num_units, nsm));
+}
+
+struct WsLayout {
+  size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, total;
+  int64_t chunk, ldg;
+};
+
+bool sizes_ok(int64_t L, int64_t H, int64_t V) {
+  return L >= 1 && H >= 8 && V >= 1 && H % 8 == 0 && L <= (1ll << 31) - BM &&
+         V <= (1ll << 31) - BN && H <= (1ll << 31) - BK;
+}
+
+int64_t default_chunk(int64_t L, int64_t V) {
+  const double budget = 4.0 * (1ull << 30);  // bf16 gradient-logit chunk
+  const int64_t ldg = round_up(V, 8);
+  int64_t cmax = static_cast<int64_t>(budget / (2.0 * ldg)) / BM * BM;
+  cmax = std::max<int64_t>(cmax, BM);
+  const int64_t nchunks = ceil_div(L, cmax);
+  const int64_t c = round_up(ceil_div(L, nchunks), BM);
+  return std::min(c, round_up(L, BM));
+}
+
+WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
+                   int64_t chunk_rows) {
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off + bytes), 256));
+    return o;
+  };
+  const int64_t nb = ceil_div(L, 256);
+  w.n_valid = take(8);
+  w.block_sums = take(nb * 8);
+  w.part_m = take(static_cast<size_t>(kMaxSplits) * L * 4);
+  w.part_s = take(static_cast<size_t>(kMaxSplits) * L * 4);
+  w.zy = take(L * 4);
+  if (dt == LCE_F32) {
+    w.h16 = take(static_cast<size_t>(L) * H * 2);
+    w.w16 = take(static_cast<size_t>(V) * H * 2);
+  } else {
+    w.h16 = w.w16 = 0;
+  }
+  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : default_chunk(L, V);
+  w.ldg = round_up(V, 8);
+  w.G = take(static_cast<size_t>(w.chunk) * w.ldg * 2);
+  w.total = off;
+  return w;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Bring fp32 inputs to bf16 in the workspace; return the operand pointers.
+lce_status operands(const void* h, const void* W, lce_dtype dt, int64_t L,
+                    int64_t H, int64_t V, const WsLayout& w, uint8_t* ws,
+                    cudaStream_t s, const void** hb, const void** Wb) {
+  if (dt == LCE_BF16) {
+    *hb = h;
+    *Wb = W;
+    return LCE_OK;
+  }
+  uint16_t* h16 = reinterpret_cast<uint16_t*>(ws + w.h16);
+  uint16_t* w16 = reinterpret_cast<uint16_t*>(ws + w.w16);
+  cudaError_t e;
+  if ((e = launch_f32_to_bf16(static_cast<const float*>(h), h16, L * H, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "f32_to_bf16(h)");
+  if ((e = launch_f32_to_bf16(static_cast<const float*>(W), w16, V * H, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "f32_to_bf16(W)");
+  *hb = h16;
+  *Wb = w16;
+  return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+using namespace lce;
+
+extern "C" {
+
+size_t lce_workspace_size(int64_t L, int64_t H, int64_t V, lce_dtype dt,
+                          int64_t chunk_rows) {
+  if (!sizes_ok(L, H, V) || chunk_rows < 0 || (dt != LCE_BF16 && dt != LCE_F32))
+    return 0;
+  return ws_layout(L, H, V, dt, chunk_rows).total;
+}
+
+int64_t lce_default_chunk_rows(int64_t L, int64_t H, int64_t V) {
+  if (!sizes_ok(L, H, V)) return 0;
+  return default_chunk(L, V);
+}
+
+lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
+                       const int64_t* labels, int64_t L, int64_t H, int64_t V,
+                       int64_t ignore_index, float* loss, float* lse, void* ws,
+                       size_t ws_bytes, void* stream) {
+  if (!h || !W || !labels || !loss || !lse || !ws) return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, V)) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, V, dt, 0);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, V, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  cudaError_t e = launch_count_valid(labels, L, V, ignore_index, n_valid,
+                                     dev->err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+
+  // logits = h W^T: M = L rows, N = V columns, K = H
+  const int num_m = static_cast<int>(ceil_div(L, BM));
+  const int num_n = static_cast<int>(ceil_div(V, BN));
+  int splits = 1, tps = num_n;
+  choose_splits(num_m, num_n, dev->num_sms, H, &splits, &tps);
+  const GemmGeom g = make_geom(L, V, H, splits, tps);
+  CUtensorMap ta, tb;
+  if ((st = tmap_kmajor(&ta, hb, H, L, H, BM)) != LCE_OK) return st;
+  if ((st = tmap_kmajor(&tb, Wb, H, V, H, BN)) != LCE_OK) return st;
+  LseParams p{};
+  p.labels = labels;
+  p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
+  p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  p.zy = reinterpret_cast<float*>(wsb + w.zy);
+  p.ignore_index = ignore_index;
+  if ((e = launch_gemm_lse(ta, tb, g, p, dev->err, grid_for(g, dev->num_sms),
+                           s)) != cudaSuccess)
+    return cuda_fail(e, "gemm_lse");
+
+  int nblocks = 0;
+  double* block_sums = reinterpret_cast<double*>(wsb + w.block_sums);
+  if ((e = launch_lse_combine(p.part_m, p.part_s, g.splits, p.zy, labels, L, V,
+                              ignore_index, lse, block_sums, &nblocks, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "lse_combine");
+  if ((e = launch_loss_finalize(block_sums, nblocks, n_valid, loss, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "loss_finalize");
+  return LCE_OK;
+}
+
+lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
+                        const int64_t* labels, const float* lse, int64_t L,
+                        int64_t H, int64_t V, int64_t ignore_index,
+                        const float* dloss, int64_t chunk_rows, void* dH,
+                        float* dW, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || !W || !labels || !lse || !dloss || !dH || !dW || !ws)
+    return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, V) || chunk_rows < 0) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(dH) ||
+      !aligned16(dW) || (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dloss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, V, dt, chunk_rows);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, V, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  cudaError_t e = launch_count_valid(labels, L, V, ignore_index, n_valid,
+                                     dev->err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+
+  uint16_t* G = reinterpret_cast<uint16_t*>(wsb + w.G);
+  const size_t dh_elem = dt == LCE_F32 ? 4 : 2;
+  CUtensorMap t_w_k, t_w_mn;
+  if ((st = tmap_kmajor(&t_w_k, Wb, H, V, H, BN)) != LCE_OK) return st;
+  if ((st = tmap_mnmajor(&t_w_mn, Wb, H, V, H)) != LCE_OK) return st;
+
+  for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
+    const int64_t cr = std::min(w.chunk, L - c0);
+    const uint16_t* hc = static_cast<const uint16_t*>(hb) + c0 * H;
+
+    // (1) recompute z_c = h_c W^T and write G_c = softmax - onehot (bf16)
+    {
+      const int num_m = static_cast<int>(ceil_div(cr, BM));
+      const int num_n = static_cast<int>(ceil_div(V, BN));
+      int splits = 1, tps = num_n;
+      choose_splits(num_m, num_n, dev->num_sms, H, &splits, &tps);
+      const GemmGeom g = make_geom(cr, V, H, splits, tps);
+      CUtensorMap ta;
+      if ((st = tmap_kmajor(&ta, hc, H, cr, H, BM)) != LCE_OK) return st;
+      GradParams p{};
+      p.labels = labels + c0;
+      p.lse = lse + c0;
+      p.G = G;
+      p.ldg = w.ldg;
+      p.ignore_index = ignore_index;
+      if ((e = launch_gemm_grad(ta, t_w_k, g, p, dev->err,
+                                grid_for(g, dev->num_sms), s)) != cudaSuccess)
+        return cuda_fail(e, "gemm_grad");
+    }
+    // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
+    {
+      const GemmGeom g = tile_geom(cr, H, V);
+      CUtensorMap ta;
+      if ((st = tmap_kmajor(&ta, G, V, cr, w.ldg, BM)) != LCE_OK) return st;
+      StoreParams p{};
+      p.out = static_cast<uint8_t*>(dH) + c0 * H * dh_elem;
+      p.ldo = H;
+      p.out_f32 = dt == LCE_F32;
+      p.accumulate = 0;
+      p.dloss = dloss;
+      p.n_valid = n_valid;
+      if ((e = launch_gemm_store(false, true, ta, t_w_mn, g, p, dev->err,
+                                 grid_for(g, dev->num_sms), s)) != cudaSuccess)
+        return cuda_fail(e, "gemm_dH");
+    }
+    // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
+    {
+      const GemmGeom g = tile_geom(V, H, cr);
+      CUtensorMap ta, tb;
+      if ((st = tmap_mnmajor(&ta, G, V, cr, w.ldg)) != LCE_OK) return st;
+      if ((st = tmap_mnmajor(&tb, hc, H, cr, H)) != LCE_OK) return st;
+      StoreParams p{};
+      p.out = dW;
+      p.ldo = H;
+      p.out_f32 = 1;
+      p.accumulate = c0 > 0;
+      p.dloss = dloss;
+      p.n_valid = n_valid;
+      if ((e = launch_gemm_store(true, true, ta, tb, g, p, dev->err,
+                                 grid_for(g, dev->num_sms), s)) != cudaSuccess)
+        return cuda_fail(e, "gemm_dW");
+    }
+  }
+  return LCE_OK;
+}
+
+lce_status lce_get_error(void* stream) {
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  if ((e = cudaMemcpy(&word, dev->err, sizeof word, cudaMemcpyDeviceToHost)) !=
+      cudaSuccess)
+    return cuda_fail(e, "read error word");
+  if (word) {
+    const unsigned zero = 0;
+    if ((e = cudaMemcpy(dev->err, &zero, sizeof zero,
+                        cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear error word");
+  }
+  if (word & ERRBIT_TIMEOUT) return LCE_ERR_TIMEOUT;
+  if (word & ERRBIT_LABEL_RANGE) return LCE_ERR_LABEL_RANGE;
+  return LCE_OK;
+}
+
+const char* lce_status_string(lce_status s) {
+  switch (s) {
+    case LCE_OK: return "LCE_OK";
+    case LCE_ERR_INVALID_ARG: return "LCE_ERR_INVALID_ARG";
+    case LCE_ERR_UNSUPPORTED: return "LCE_ERR_UNSUPPORTED";
+    case LCE_ERR_WORKSPACE: return "LCE_ERR_WORKSPACE";
+    case LCE_ERR_LABEL_RANGE: return "LCE_ERR_LABEL_RANGE";
+    case LCE_ERR_TIMEOUT: return "LCE_ERR_TIMEOUT";
+    case LCE_ERR_CUDA: return "LCE_ERR_CUDA";
+  }
+  return "LCE_ERR_UNKNOWN";
+}
+
+const char* lce_last_cuda_error(void) { return t_last_cuda_error; }
+
+lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
+                         int64_t N, int64_t K, int a_mn, int b_mn,
+                         void* stream) {
+  if (!A || !B || !D) return LCE_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || K < 1 || N % 8 || M > (1ll << 30) ||
+      N > (1ll << 30) || K > (1ll << 30))
+    return LCE_ERR_INVALID_ARG;
+  if ((a_mn ? M : K) % 8 || (b_mn ? N : K) % 8) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D))
+    return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  const GemmGeom g = tile_geom(M, N, K);
+  CUtensorMap ta, tb;
+  st = a_mn ? tmap_mnmajor(&ta, A, M, K, M) : tmap_kmajor(&ta, A, K, M, K, BM);
+  if (st != LCE_OK) return st;
+  st = b_mn ? tmap_mnmajor(&tb, B, N, K, N) : tmap_kmajor(&tb, B, K, N, K, BN);
+  if (st != LCE_OK) return st;
+  StoreParams p{};
+  p.out = D;
+  p.ldo = N;
+  p.out_f32 = 1;
+  p.accumulate = 0;
+  p.dloss = nullptr;
+  p.n_valid = nullptr;
+  cudaError_t e = launch_gemm_store(a_mn != 0, b_mn != 0, ta, tb, g, p,
+                                    dev->err, grid_for(g, dev->num_sms),
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "test_gemm");
+}
+
+lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaError_t e = launch_wait_probe(dev->err, timeout_ns,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "wait_probe");
+}
+
+}  // extern "C"

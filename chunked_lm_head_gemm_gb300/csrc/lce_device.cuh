@@ -1,0 +1,717 @@
+// Device layer of the fused linear cross-entropy library for sm_103a:
+// inline-PTX wrappers for mbarrier, TMA and the 5th-generation tensor cores
+// (tcgen05 + tensor memory), a persistent warp-specialised contraction
+// kernel, and the epilogues that fold the loss arithmetic into it.
+//
+// Contraction D[M,N] = A[M,K] * B[K,N], bf16 operands, fp32 accumulation in
+// tensor memory (TMEM). One CTA per SM; 6 warps:
+//   warp 0      TMA producer (one lane): streams A/B k-slices into a 4-stage
+//               shared-memory ring, 128-byte swizzled;
+//   warp 1      MMA issuer (one lane): tcgen05.mma 128x256x16 into one of two
+//               256-column TMEM accumulators (double buffered);
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter of the
+//               accumulator, then the fused loss arithmetic.
+// Every mbarrier wait is bounded in time: on expiry the kernel raises a
+// timeout bit in the error word, the other roles see a shared abort flag,
+// in-flight copies and MMAs are drained (again bounded) and TMEM is freed.
+#pragma once
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "lce_internal.h"
+
+namespace lce {
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// shared memory, mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
+                                                      uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Context of the bounded waits of one CTA.
+struct WaitCtx {
+  volatile uint32_t* abort;  // shared flag: some role gave up
+  unsigned* err;             // global error word
+  uint64_t timeout_ns;
+};
+
+// Wait until the phase of `bar` with parity `parity` has completed. Gives up
+// after ctx.timeout_ns (sets the abort flag and the timeout bit) or, when
+// honor_abort is set, as soon as another role has raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const WaitCtx& ctx,
+                                          bool honor_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *ctx.abort) return false;
+    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+      *ctx.abort = 1u;
+      atomicOr(ctx.err, ERRBIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm))
+               : "memory");
+}
+
+// 2-D tiled load of one box into shared memory; completes on `bar` with the
+// box's byte count. c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
+                                            int32_t c0, int32_t c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 / tensor memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(ncols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, tcgen05 version bits.
+//   K-major operand (rows of 64 K-elements = 128 B, 8-row atoms of 1 KB):
+//     SBO = 1024 (next 8 rows), LBO unused; a K step of 16 adds 32 B.
+//   MN-major operand (rows of 64 MN-elements, one row per k, 8-k atoms):
+//     SBO = 1024 (next 8 k), LBO = byte distance to the next 64 MN-elements;
+//     a K step of 16 adds 16 rows = 2048 B.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
+                                                uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16) |
+         (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) |
+         (1ull << 46) |  // descriptor version (tcgen05)
+         (2ull << 61);   // swizzle: 128 B
+}
+
+// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, M = 128, N = 256.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ constexpr uint32_t idesc_bf16_f32() {
+  return (1u << 4) |                                 // D format: f32
+         (1u << 7) |                                 // A format: bf16
+         (1u << 10) |                                // B format: bf16
+         (static_cast<uint32_t>(A_MN) << 15) |       // A major
+         (static_cast<uint32_t>(B_MN) << 16) |       // B major
+         (static_cast<uint32_t>(BN >> 3) << 17) |    // N / 8
+         (static_cast<uint32_t>(BM >> 4) << 24);     // M / 16
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc,
+                                       uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape),
+// waited on inside the same asm block so no use can move above the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+  __nv_bfloat16 v = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&v);
+}
+
+__device__ __forceinline__ bool label_valid(int64_t y, int64_t V,
+                                            int64_t ignore_index) {
+  return y != ignore_index && y >= 0 && y < V;
+}
+
+// ---------------------------------------------------------------------------
+// unit decode
+// ---------------------------------------------------------------------------
+struct Unit {
+  int m_blk, split, n_first, n_count;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u) {
+  Unit t;
+  t.m_blk = u / g.splits;
+  t.split = u - t.m_blk * g.splits;
+  t.n_first = t.split * g.tiles_per_split;
+  t.n_count = min(g.tiles_per_split, g.num_n - t.n_first);
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// epilogues: one thread per accumulator row, 32 columns per TMEM load
+// ---------------------------------------------------------------------------
+
+// Forward: per-row running (max, sum 2^(u-max)) in log2 units over the
+// unit's columns; the logit at the label is written by the one tile that
+// holds that column.
+struct EpiLse {
+  using Params = LseParams;
+  float m2, s;
+  int64_t row;
+  int yv;  // label if it takes part, else -1
+  bool row_ok;
+
+  __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row_ok = row < g.M;
+    yv = -1;
+    if (row_ok) {
+      const int64_t y = p.labels[row];
+      if (label_valid(y, g.N, p.ignore_index)) yv = static_cast<int>(y);
+    }
+    m2 = -INFINITY;
+    s = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;  // same for the whole warp
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      const int64_t rem = g.N - j0;
+      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int yo = yv - static_cast<int>(j0);
+      if (static_cast<unsigned>(yo) < 32u) {
+        float zyv = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i == yo) zyv = v[i];
+        p.zy[row] = zyv;
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = (i < nv) ? v[i] * LOG2E : -INFINITY;
+        mx[i & 3] = fmaxf(mx[i & 3], v[i]);
+      }
+      const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float mn = fmaxf(m2, cmax);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i & 3] += ex2(v[i] - mn);
+      s = s * ex2(m2 - mn) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      m2 = mn;
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(const Params& p, const GemmGeom& g,
+                                           const Unit& t, int) {
+    if (row_ok) {
+      p.part_m[static_cast<int64_t>(t.split) * g.M + row] = m2;
+      p.part_s[static_cast<int64_t>(t.split) * g.M + row] = s;
+    }
+  }
+};
+
+// Backward recompute: G = exp(z - lse) - [j == y] for rows that take part,
+// 0 for the others, rounded to bf16. The dloss/N scale is applied later, in
+// fp32, by the dH and dW epilogues.
+struct EpiGrad {
+  using Params = GradParams;
+  int64_t row;
+  bool row_ok;
+  int yv;
+  float lse2;
+
+  __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row_ok = row < g.M;
+    yv = -1;
+    lse2 = 0.f;
+    if (row_ok) {
+      const int64_t y = p.labels[row];
+      if (label_valid(y, g.N, p.ignore_index)) {
+        yv = static_cast<int>(y);
+        lse2 = p.lse[row] * LOG2E;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      if (!row_ok) continue;
+      const int yo = yv - static_cast<int>(j0);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float gi = (yv >= 0) ? ex2(fmaf(v[i], LOG2E, -lse2)) : 0.f;
+        if (i == yo) gi -= 1.f;
+        v[i] = gi;
+      }
+      uint16_t* dst = p.G + row * p.ldg + j0;
+      if (j0 + 32 <= g.N) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                             pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                             pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      } else {
+        const int nv = static_cast<int>(g.N - j0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) dst[i] = to_bf16_bits(v[i]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(const Params&, const GemmGeom&,
+                                           const Unit&, int) {}
+};
+
+// out[row][col] (+)= scale * acc, fp32 or bf16. scale = dloss / N when the
+// parameters carry them (N = 0 gives 0), else 1.
+struct EpiStore {
+  using Params = StoreParams;
+  int64_t row;
+  bool row_ok;
+  float scale;
+
+  __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row_ok = row < g.M;
+    scale = 1.f;
+    if (p.dloss != nullptr) {
+      const unsigned long long n = *p.n_valid;
+      scale = n ? static_cast<float>(static_cast<double>(*p.dloss) /
+                                     static_cast<double>(n))
+                : 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= scale;
+      const bool full = j0 + 32 <= g.N;
+      const int nv = full ? 32 : static_cast<int>(g.N - j0);
+      if (p.out_f32) {
+        float* dst = static_cast<float*>(p.out) + row * p.ldo + j0;
+        if (full) {
+          float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                   v[4 * q + 3]);
+            if (p.accumulate) {
+              const float4 a = d4[q];
+              o.x += a.x;
+              o.y += a.y;
+              o.z += a.z;
+              o.w += a.w;
+            }
+            d4[q] = o;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nv) dst[i] = p.accumulate ? dst[i] + v[i] : v[i];
+        }
+      } else {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.ldo + j0;
+        if (full) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                               pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                               pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nv) dst[i] = to_bf16_bits(v[i]);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(const Params&, const GemmGeom&,
+                                           const Unit&, int) {}
+};
+
+// ---------------------------------------------------------------------------
+// the persistent contraction kernel
+// ---------------------------------------------------------------------------
+struct SmemMap {
+  uint32_t a, b, bars;
+  __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const {
+    return bars + 8u * (STAGES + s);
+  }
+  __device__ __forceinline__ uint32_t tfull(int a_) const {
+    return bars + 8u * (2 * STAGES + a_);
+  }
+  __device__ __forceinline__ uint32_t tempty(int a_) const {
+    return bars + 8u * (2 * STAGES + 2 + a_);
+  }
+  __device__ __forceinline__ uint32_t drain() const {
+    return bars + 8u * (2 * STAGES + 4);
+  }
+};
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void role_producer(const CUtensorMap* ta,
+                                              const CUtensorMap* tb,
+                                              const GemmGeom& g,
+                                              const SmemMap& sm,
+                                              const WaitCtx& ctx) {
+  uint32_t stage = 0, phase = 0, issued = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+    const Unit t = decode_unit(g, u);
+    const int m0 = t.m_blk * BM;
+    for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      const int n0 = (t.n_first + tt) * BN;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = sm.full(stage);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        const uint32_t sa = sm.a + stage * A_STAGE_BYTES;
+        const uint32_t sb = sm.b + stage * B_STAGE_BYTES;
+        const int k0 = kb * BK;
+        if (A_MN) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_2d(sa + j * 64 * BK * 2, ta, m0 + 64 * j, k0, fb);
+        } else {
+          tma_load_2d(sa, ta, k0, m0, fb);
+        }
+        if (B_MN) {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(sb + j * 64 * BK * 2, tb, n0 + 64 * j, k0, fb);
+        } else {
+          tma_load_2d(sb, tb, k0, n0, fb);
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+  // Drain: every copy issued must have landed before the CTA may exit.
+  for (int s = 0; s < STAGES; ++s) {
+    const uint32_t cnt = issued / STAGES + (static_cast<uint32_t>(s) < issued % STAGES ? 1u : 0u);
+    if (cnt) mbar_wait(sm.full(s), (cnt - 1u) & 1u, ctx, false);
+  }
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void role_mma(const GemmGeom& g, const SmemMap& sm,
+                                         uint32_t tmem_base,
+                                         const WaitCtx& ctx) {
+  constexpr uint32_t IDESC = idesc_bf16_f32<A_MN, B_MN>();
+  // operand strides inside one stage (see sdesc_sw128)
+  constexpr uint32_t MN_LBO = 64 * BK * 2;  // one 64-wide MN box: 8 KB
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+    const Unit t = decode_unit(g, u);
+    for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      if (!mbar_wait(sm.tempty(acc), acc_phase ^ 1u, ctx, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * BN;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(sm.full(stage), phase, ctx, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = sm.a + stage * A_STAGE_BYTES;
+        const uint32_t sb = sm.b + stage * B_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_LBO, 1024)
+                                   : sdesc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_LBO, 1024)
+                                   : sdesc_sw128(sb + k * 32, 16, 1024);
+          tc_mma(d, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(sm.empty(stage));  // frees the stage once these MMAs finish
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(sm.tfull(acc));  // accumulator ready for the epilogue
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  // Drain: all MMAs issued by this thread complete before TMEM is freed.
+  tc_commit(sm.drain());
+  mbar_wait(sm.drain(), 0, ctx, false);
+}
+
+template <class Epi>
+__device__ __forceinline__ void role_epilogue(const GemmGeom& g,
+                                              const typename Epi::Params& p,
+                                              const SmemMap& sm,
+                                              uint32_t tmem_base,
+                                              const WaitCtx& ctx, int warp,
+                                              int lane) {
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int r = q * 32 + lane;
+  uint32_t acc = 0, acc_phase = 0;
+  Epi epi;
+  for (int u = blockIdx.x; u < g.num_units; u += gridDim.x) {
+    const Unit t = decode_unit(g, u);
+    epi.begin_unit(p, g, t, r);
+    bool ok = true;
+    for (int tt = 0; tt < t.n_count; ++tt) {
+      const bool got = mbar_wait(sm.tfull(acc), acc_phase, ctx, true);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      epi.tile(p, g, t, t.n_first + tt, taddr, r);
+      tc_fence_before();
+      mbar_arrive(sm.tempty(acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) return;
+    epi.end_unit(p, g, t, r);
+  }
+}
+
+template <class Epi, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap ta,
+           const __grid_constant__ CUtensorMap tb, const GemmGeom g,
+           const typename Epi::Params p, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms: 1 KB aligned
+  SmemMap sm;
+  sm.a = base;
+  sm.b = base + STAGES * A_STAGE_BYTES;
+  sm.bars = base + STAGES * STAGE_BYTES;
+  uint8_t* misc = smem_raw + (sm.bars - raw) + 8 * (2 * STAGES + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(sm.full(s), 1);
+      mbar_init(sm.empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(sm.tfull(a), 1);
+      mbar_init(sm.tempty(a), 128);  // every epilogue thread arrives
+    }
+    mbar_init(sm.drain(), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&ta);
+    tma_prefetch_desc(&tb);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx ctx{abort_flag, err, g.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) role_producer<A_MN, B_MN>(&ta, &tb, g, sm, ctx);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) role_mma<A_MN, B_MN>(g, sm, tmem_base, ctx);
+    __syncwarp();
+  } else {
+    role_epilogue<Epi>(g, p, sm, tmem_base, ctx, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Host helper for the kernel translation units: launch one instantiation.
+template <class Epi, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb,
+                          const GemmGeom& g, const typename Epi::Params& p,
+                          unsigned* err, int grid, cudaStream_t s) {
+  auto kern = k_gemm<Epi, A_MN, B_MN>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, g, p, err);
+  return cudaGetLastError();
+}
+
+}  // namespace lce

@@ -1,0 +1,23 @@
+// Tensor-core contractions whose epilogues carry the loss arithmetic:
+//  - forward logits h W^T -> per-row online log-sum-exp partials and the
+//    logit at the label ("Training Beyond 1M Tokens", section "The loss is
+//    the first thing to break": logits L x V, cross entropy against labels);
+//  - backward recompute of the same logits for one row chunk -> bf16
+//    softmax - onehot (the gradient of that cross entropy w.r.t. the logits).
+#include "lce_device.cuh"
+
+namespace lce {
+
+cudaError_t launch_gemm_lse(const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmGeom& g, const LseParams& p,
+                            unsigned* err, int grid, cudaStream_t s) {
+  return launch_gemm_t<EpiLse, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                             const GemmGeom& g, const GradParams& p,
+                             unsigned* err, int grid, cudaStream_t s) {
+  return launch_gemm_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+}  // namespace lce

@@ -1,0 +1,104 @@
+// Internal declarations shared by the host layer and the kernel translation
+// units of the fused linear cross-entropy library. Not part of the C-ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lce {
+
+// Tile shape of every tensor-core contraction: one CTA owns a 128 x 256 fp32
+// accumulator in tensor memory and walks K in steps of 64 bf16 elements
+// (one 128-byte swizzle row).
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int GEMM_THREADS = 192;           // 6 warps: TMA, MMA, 4 x epilogue
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int TMEM_COLS = 512;              // two 256-column accumulators
+
+// Device error bits, OR-ed into the library's error word.
+constexpr unsigned ERRBIT_LABEL_RANGE = 1u << 4;
+constexpr unsigned ERRBIT_TIMEOUT = 1u << 5;
+
+// Work decomposition of one contraction D[M,N] = A[M,K] B[K,N].
+// A unit is (row block m_blk, a run of n_count consecutive column tiles
+// starting at n_first). Units are numbered u = m_blk * splits + split.
+struct GemmGeom {
+  int64_t M, N, K;
+  int num_m, num_n, num_kb;
+  int splits;           // column-tile runs per row block
+  int tiles_per_split;  // column tiles per run (the last run may be shorter)
+  int num_units;        // num_m * splits
+  uint64_t timeout_ns;  // limit of every wait inside the kernel
+};
+
+// ---- epilogue parameter blocks ----------------------------------------------
+
+// Forward logits tile -> per-row online (max, sum of exp) over the unit's
+// columns, plus the logit at the label.
+struct LseParams {
+  const int64_t* labels;  // [M]
+  float* part_m;          // [splits][M], running max in log2 units
+  float* part_s;          // [splits][M], sum of 2^(u - max)
+  float* zy;              // [M], logit at the label (valid rows only)
+  int64_t ignore_index;
+};
+
+// Backward recompute tile -> G = softmax - onehot (unscaled), bf16.
+struct GradParams {
+  const int64_t* labels;  // [M], rows of this chunk
+  const float* lse;       // [M], rows of this chunk
+  uint16_t* G;            // [M][ldg] bf16 bits
+  int64_t ldg;
+  int64_t ignore_index;
+};
+
+// Plain store of scale * acc (dH chunk, or the building-block test GEMM).
+struct StoreParams {
+  void* out;              // [M][ldo]
+  int64_t ldo;
+  int out_f32;            // 1: fp32 output, 0: bf16 output
+  int accumulate;         // 1: out += scale*acc (fp32 only), 0: out = scale*acc
+  const float* dloss;     // scale = dloss[0] / n_valid[0] (n_valid 0 -> 0);
+  const unsigned long long* n_valid;  // both NULL -> scale = 1
+};
+
+// ---- launch wrappers (defined in the kernel translation units) --------------
+// Each launches one persistent tensor-core contraction on `stream`.
+// a_mn / b_mn: operand stored MN-major (true) or K-major (false).
+cudaError_t launch_gemm_lse(const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmGeom& g, const LseParams& p,
+                            unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                             const GemmGeom& g, const GradParams& p,
+                             unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
+                              const CUtensorMap& tb, const GemmGeom& g,
+                              const StoreParams& p, unsigned* err, int grid,
+                              cudaStream_t s);
+
+// Small kernels.
+cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
+                               int64_t ignore_index,
+                               unsigned long long* n_valid, unsigned* err,
+                               cudaStream_t s);
+cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
+                               int splits, const float* zy,
+                               const int64_t* labels, int64_t L, int64_t V,
+                               int64_t ignore_index, float* lse,
+                               double* block_sums, int* nblocks_out,
+                               cudaStream_t s);
+cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
+                                 const unsigned long long* n_valid,
+                                 float* loss, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
+                               cudaStream_t s);
+cudaError_t launch_wait_probe(unsigned* err, uint64_t timeout_ns,
+                              cudaStream_t s);
+
+}  // namespace lce

@@ -1,0 +1,166 @@
+// The small kernels of the path: label count, log-sum-exp combine, loss
+// reduction, fp32 -> bf16 input conversion, and the bounded-wait probe.
+#include "lce_device.cuh"
+
+namespace lce {
+
+// N = #{i : label i takes part}. Labels that are neither ignore_index nor in
+// [0, V) raise the label-range bit and count as ignored, as everywhere else.
+__global__ void k_count_valid(const int64_t* __restrict__ labels, int64_t L,
+                              int64_t V, int64_t ignore_index,
+                              unsigned long long* n_valid, unsigned* err) {
+  unsigned long long c = 0;
+  bool bad = false;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i < L; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t y = labels[i];
+    if (y != ignore_index) {
+      if (y >= 0 && y < V)
+        ++c;
+      else
+        bad = true;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  const bool any_bad = __any_sync(0xffffffffu, bad);
+  if ((threadIdx.x & 31) == 0) {
+    if (c) atomicAdd(n_valid, c);  // integer sum: order does not matter
+    if (any_bad) atomicOr(err, ERRBIT_LABEL_RANGE);
+  }
+}
+
+cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
+                               int64_t ignore_index,
+                               unsigned long long* n_valid, unsigned* err,
+                               cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(n_valid, 0, sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return e;
+  const int64_t want = (L + 255) / 256;
+  const int grid = static_cast<int>(want < 1024 ? (want < 1 ? 1 : want) : 1024);
+  k_count_valid<<<grid, 256, 0, s>>>(labels, L, V, ignore_index, n_valid, err);
+  return cudaGetLastError();
+}
+
+// lse_i = ln 2 * (M + log2 sum_k s_k 2^(m_k - M)), M = max_k m_k, merging the
+// per-split partials in a fixed order; then a fixed-order block sum of
+// (lse_i - z_i,y_i) over rows that take part, in float64.
+constexpr int COMBINE_THREADS = 256;
+
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    k_lse_combine(const float* __restrict__ part_m,
+                  const float* __restrict__ part_s, int splits,
+                  const float* __restrict__ zy,
+                  const int64_t* __restrict__ labels, int64_t L, int64_t V,
+                  int64_t ignore_index, float* __restrict__ lse,
+                  double* __restrict__ block_sums) {
+  __shared__ double warp_sums[COMBINE_THREADS / 32];
+  const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
+                    threadIdx.x;
+  double term = 0.0;
+  if (i < L) {
+    float M = -INFINITY;
+    for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[k * L + i]);
+    float t = 0.f;
+    for (int k = 0; k < splits; ++k)
+      t += part_s[k * L + i] * exp2f(part_m[k * L + i] - M);
+    const float l = (M + log2f(t)) * LN2;
+    lse[i] = l;
+    if (label_valid(labels[i], V, ignore_index))
+      term = static_cast<double>(l) - static_cast<double>(zy[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = term;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double b = 0.0;
+    for (int w = 0; w < COMBINE_THREADS / 32; ++w) b += warp_sums[w];
+    block_sums[blockIdx.x] = b;
+  }
+}
+
+cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
+                               int splits, const float* zy,
+                               const int64_t* labels, int64_t L, int64_t V,
+                               int64_t ignore_index, float* lse,
+                               double* block_sums, int* nblocks_out,
+                               cudaStream_t s) {
+  const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
+  *nblocks_out = nb;
+  k_lse_combine<<<nb, COMBINE_THREADS, 0, s>>>(part_m, part_s, splits, zy,
+                                               labels, L, V, ignore_index, lse,
+                                               block_sums);
+  return cudaGetLastError();
+}
+
+// loss = (sum of block sums, fixed order) / N, and 0 when N = 0.
+__global__ void __launch_bounds__(256)
+    k_loss_finalize(const double* __restrict__ block_sums, int nblocks,
+                    const unsigned long long* __restrict__ n_valid,
+                    float* __restrict__ loss) {
+  __shared__ double part[256];
+  double acc = 0.0;
+  for (int b = threadIdx.x; b < nblocks; b += 256) acc += block_sums[b];
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const unsigned long long n = *n_valid;
+    *loss = n ? static_cast<float>(part[0] / static_cast<double>(n)) : 0.f;
+  }
+}
+
+cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
+                                 const unsigned long long* n_valid,
+                                 float* loss, cudaStream_t s) {
+  k_loss_finalize<<<1, 256, 0, s>>>(block_sums, nblocks, n_valid, loss);
+  return cudaGetLastError();
+}
+
+// fp32 -> bf16 (round to nearest even), 8 elements per thread when aligned.
+__global__ void k_f32_to_bf16(const float* __restrict__ in,
+                              uint16_t* __restrict__ out, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i < n; i += stride)
+    out[i] = to_bf16_bits(in[i]);
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
+                               cudaStream_t s) {
+  const int64_t want = (n + 255) / 256;
+  const int grid = static_cast<int>(want < 4096 ? (want < 1 ? 1 : want) : 4096);
+  k_f32_to_bf16<<<grid, 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+// One thread waits on an mbarrier that nothing arrives at, with the same
+// bounded wait the contraction kernels use; it must give up after
+// timeout_ns and raise the timeout bit. Used to test failure detection
+// without hanging the GPU.
+__global__ void k_wait_probe(unsigned* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx ctx{&abort_flag, err, timeout_ns};
+    mbar_wait(smem_u32(&bar), 0, ctx, true);
+  }
+}
+
+cudaError_t launch_wait_probe(unsigned* err, uint64_t timeout_ns,
+                              cudaStream_t s) {
+  k_wait_probe<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace lce

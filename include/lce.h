@@ -1,0 +1,166 @@
+/*
+ * lce.h -- C ABI of the fused linear cross-entropy library (liblce.so) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the loss at the end of a language model, as defined in
+ * "Training Beyond 1M Tokens" (TRL guide), section "The loss is the first
+ * thing to break": the last hidden states h (L x H) are multiplied by the
+ * LM-head weights W (V x H, nn.Linear layout) into logits z = h W^T (L x V),
+ * and the loss is the cross entropy of those logits against the integer
+ * labels. Section "The massive logits matrix: chunk it" of the same guide
+ * gives the reason the logits are never materialised: the loss is a sum over
+ * rows and each softmax runs along one row's vocabulary, so rows can be
+ * processed piecewise. This library goes further than row pieces: the
+ * forward keeps only running per-row (max, sum of exp) statistics in the
+ * tensor-core epilogue; the backward recomputes the logits one bounded row
+ * chunk at a time. Extra device memory is O(chunk_rows * V), never O(L * V).
+ *
+ * Definition (the reduction is this library's reading; the pages only say
+ * the per-row pieces are summed):
+ *   valid(i)  = labels[i] != ignore_index and 0 <= labels[i] < V
+ *   N         = #{i : valid(i)}
+ *   lse[i]    = log sum_j exp(z[i][j])                     (every row)
+ *   loss      = (1/N) sum_{valid i} (lse[i] - z[i][labels[i]]),  0 if N = 0
+ *   G[i][j]   = dloss/N (exp(z[i][j] - lse[i]) - [j == labels[i]]), valid i
+ *             = 0                                               otherwise
+ *   dH        = G W,   dW = G^T h
+ *
+ * Conventions shared by every call below:
+ *   - All pointers named "device" are CUDA device pointers owned by the
+ *     caller; the library allocates nothing and keeps no pointer after the
+ *     call returns (work is queued on `stream`).
+ *   - Matrices are row-major and contiguous. h, W, dH and the workspace must
+ *     be 16-byte aligned, and H must be a multiple of 8 (the tensor-memory
+ *     copy engine needs 16-byte row strides).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Calls are asynchronous on that stream; none synchronises the host,
+ *     except lce_get_error.
+ *   - Argument errors are returned synchronously, before anything is
+ *     queued. Errors found on the device (a label out of range, a bounded
+ *     wait that expired) set the library's device error word, read by
+ *     lce_get_error; the kernels never trap.
+ *   - Inputs of dtype LCE_F32 are rounded to bf16 on the device (into the
+ *     workspace) before the tensor-core contractions; accumulation is fp32.
+ *   - Results are deterministic: no floating-point atomics; fixed reduction
+ *     orders for a fixed shape, dtype and chunk_rows.
+ *   - The functions are thread-safe for distinct workspaces; calls that
+ *     share a workspace must be ordered on one stream.
+ */
+#ifndef LCE_H_
+#define LCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LCE_OK = 0,
+  LCE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment */
+  LCE_ERR_UNSUPPORTED = 2, /* device is not sm_103 / sm_100 family, or dtype */
+  LCE_ERR_WORKSPACE = 3,   /* ws_bytes below lce_workspace_size() */
+  LCE_ERR_LABEL_RANGE = 4, /* a label outside [0, V) that is not ignore_index
+                              (that row was treated as ignored) */
+  LCE_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel expired */
+  LCE_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} lce_status;
+
+typedef enum {
+  LCE_BF16 = 0, /* h, W (and dH) are bfloat16 */
+  LCE_F32 = 1   /* h, W (and dH) are float32; computed from bf16 roundings */
+} lce_dtype;
+
+/*
+ * Bytes of device workspace that lce_forward and lce_backward need for this
+ * shape (the same buffer serves both). chunk_rows is the backward's row
+ * chunk (0 = the library's default). Returns 0 for invalid sizes.
+ * The dominant term is chunk_rows * round_up(V, 8) * 2 bytes (the bf16
+ * gradient-logit chunk); with LCE_F32 add bf16 copies of h and W.
+ */
+size_t lce_workspace_size(int64_t L, int64_t H, int64_t V, lce_dtype dt,
+                          int64_t chunk_rows);
+
+/* The row chunk the backward uses when chunk_rows = 0. */
+int64_t lce_default_chunk_rows(int64_t L, int64_t H, int64_t V);
+
+/*
+ * Forward. Source: "Training Beyond 1M Tokens", sections "The loss is the
+ * first thing to break" and "The massive logits matrix: chunk it".
+ *   h       device, [L][H] of dt
+ *   W       device, [V][H] of dt
+ *   labels  device, [L] int64
+ *   loss    device, [1] float32 out: mean loss over valid rows (0 if none)
+ *   lse     device, [L] float32 out: per-row log-sum-exp (every row); keep
+ *           it for lce_backward
+ *   ws      device workspace of ws_bytes >= lce_workspace_size(...)
+ * Queues: label count, one persistent tensor-core kernel over all logit
+ * tiles (online log-sum-exp + label-logit gather in its epilogue), a
+ * per-row combine, a one-block loss reduction.
+ */
+lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
+                       const int64_t* labels, int64_t L, int64_t H, int64_t V,
+                       int64_t ignore_index, float* loss, float* lse, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * Backward. The pages do not describe it; it is the gradient of the forward
+ * above: G = dloss/N (softmax - onehot) on valid rows.
+ *   lse        device, [L] float32 from lce_forward on the same inputs
+ *   dloss      device, [1] float32: gradient of the scalar loss
+ *   chunk_rows rows per chunk (multiple of 128, or 0 for the default)
+ *   dH         device, [L][H] of dt, overwritten
+ *   dW         device, [V][H] float32, overwritten
+ * For each chunk of rows: one tensor-core kernel recomputes the chunk's
+ * logits and writes bf16 (softmax - onehot) into the workspace, one computes
+ * the chunk's dH rows, one adds the chunk's contribution into dW (fp32
+ * read-add-write, chunks in order, no atomics).
+ */
+lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
+                        const int64_t* labels, const float* lse, int64_t L,
+                        int64_t H, int64_t V, int64_t ignore_index,
+                        const float* dloss, int64_t chunk_rows, void* dH,
+                        float* dW, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device. Returns LCE_ERR_TIMEOUT or LCE_ERR_LABEL_RANGE if a kernel
+ * raised one since the last call (timeout first), LCE_ERR_CUDA if the
+ * synchronisation failed, else LCE_OK. The word is shared by all streams of
+ * the device.
+ */
+lce_status lce_get_error(void* stream);
+
+/* Human-readable name of a status. Static storage; never NULL. */
+const char* lce_status_string(lce_status s);
+
+/* Text of the last CUDA error the library saw on this thread ("" if none). */
+const char* lce_last_cuda_error(void);
+
+/*
+ * Test hook for the tensor-core building block: D = A B in fp32.
+ * No counterpart on the pages; it exposes the contraction kernel alone so
+ * that every operand layout can be checked against a plain matmul.
+ *   A device bf16: a_mn = 0 -> [M][K] (K-major), a_mn = 1 -> [K][M]
+ *   B device bf16: b_mn = 0 -> [N][K] (K-major), b_mn = 1 -> [K][N]
+ *   D device fp32 [M][N]; N % 8 == 0; the contiguous dimension of A and B
+ *   must be a multiple of 8.
+ */
+lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
+                         int64_t N, int64_t K, int a_mn, int b_mn,
+                         void* stream);
+
+/*
+ * Test hook for failure detection: one kernel waits on a barrier that
+ * nothing signals, gives up after timeout_ns and raises the timeout bit, so
+ * the next lce_get_error returns LCE_ERR_TIMEOUT. No counterpart on the
+ * pages. The GPU context stays usable.
+ */
+lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H_ */

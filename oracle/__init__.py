@@ -60,7 +60,7 @@ def load_library(path: str):
                                        i32, p, p, p, p]
     lib.lce_oracle_forward.restype = i32
     lib.lce_oracle_backward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
-                                        f64, i32, p, p]
+                                        f64, i32, p, p, p, i64]
     lib.lce_oracle_backward.restype = i32
     lib.lce_oracle_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64, f64, p,
                                     i64, i32, p, p, p]
@@ -144,9 +144,12 @@ def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None)
 
 
 def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
-             want_dH: bool = True, want_dW: bool = True,
+             want_dH: bool = True, want_dW: bool = True, vrows=None,
              nthreads: int | None = None):
-    """Returns dict(dH[L,H] or None, dW[V,H] or None, status) in float64."""
+    """Returns dict(dH[L,H] or None, dW or None, status) in float64.
+
+    dW is [V,H], or [len(vrows), H] holding rows dW[vrows] when vrows is
+    given."""
     hn, dt = _as_input(h)
     Wn, dt2 = _as_input(W)
     if dt != dt2:
@@ -154,12 +157,15 @@ def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
     y = _labels(labels)
     L, H = hn.shape
     V = Wn.shape[0]
+    vr = None if vrows is None else np.ascontiguousarray(vrows, dtype=np.int64)
     dH = np.empty((L, H), np.float64) if want_dH else None
-    dW = np.empty((V, H), np.float64) if want_dW else None
+    nvr = V if vr is None else vr.shape[0]
+    dW = np.empty((nvr, H), np.float64) if want_dW else None
     st = _load().lce_oracle_backward(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
                                      ignore_index, float(dloss),
                                      nthreads or default_threads(), _ptr(dH),
-                                     _ptr(dW))
+                                     _ptr(dW), _ptr(vr),
+                                     0 if vr is None else nvr)
     if st not in (OK, LABEL_RANGE):
         raise RuntimeError(f"lce_oracle_backward status {st}")
     return dict(dH=dH, dW=dW, status=st)

@@ -309,6 +309,7 @@ typedef struct {
     int64_t L, H, V;
     int64_t a0, a1;   /* row range (dH) or vocab range (dW) */
     double *dH, *dW;
+    const int64_t *vrows; /* dW rows to compute: vrows[a] (NULL: a itself) */
 } mm_job;
 
 /* dH[i][:] = sum_j G[i][j] * W[j][:] for i in [a0, a1) */
@@ -324,11 +325,13 @@ static void *dH_worker(void *arg) {
     return NULL;
 }
 
-/* dW[j][:] = sum_i G[i][j] * h[i][:] for j in [a0, a1) */
+/* dW[j][:] = sum_i G[i][j] * h[i][:] for the vocabulary ids j of [a0, a1)
+ * (or of vrows[a0..a1) when a subset was asked for; out row a then). */
 static void *dW_worker(void *arg) {
     mm_job *jb = (mm_job *)arg;
-    for (int64_t j = jb->a0; j < jb->a1; ++j) {
-        double *out = jb->dW + j * jb->H;
+    for (int64_t a = jb->a0; a < jb->a1; ++a) {
+        const int64_t j = jb->vrows ? jb->vrows[a] : a;
+        double *out = jb->dW + a * jb->H;
         for (int64_t k = 0; k < jb->H; ++k) out[k] = 0.0;
         for (int64_t i = 0; i < jb->L; ++i) {
             double g = jb->G[i * jb->V + j];
@@ -358,16 +361,23 @@ static void run_mm(mm_job proto, int64_t n, int nthreads, void *(*fn)(void *)) {
 
 /*
  * Backward for the whole problem: given the upstream gradient dloss of the
- * scalar loss, writes dH (L x H) and/or dW (V x H) in float64 (either may be
- * NULL). Holds G (L x V float64) in host memory, so it is for shapes whose
- * L x V fits.
+ * scalar loss, writes dH (L x H) and/or dW in float64 (either may be NULL).
+ * dW is V x H, or, when vrows is not NULL, the nvrows x H rows dW[vrows[a]].
+ * Holds G (L x V float64) in host memory, so it is for shapes whose L x V
+ * fits.
  */
 int lce_oracle_backward(const void *h, const void *W, int dtype,
                         const int64_t *labels, int64_t L, int64_t H, int64_t V,
                         int64_t ignore_index, double dloss, int nthreads,
-                        double *dH, double *dW) {
+                        double *dH, double *dW, const int64_t *vrows,
+                        int64_t nvrows) {
     int st = check_args(h, W, dtype, labels, L, H, V);
     if (st) return st;
+    if (vrows) {
+        if (nvrows < 1) return ORACLE_BAD_ARG;
+        for (int64_t a = 0; a < nvrows; ++a)
+            if (vrows[a] < 0 || vrows[a] >= V) return ORACLE_BAD_ARG;
+    }
     int bad = 0;
     int64_t n = count_valid(labels, L, V, ignore_index, &bad);
     double *hd = widen_all(h, dtype, L, H);
@@ -392,9 +402,9 @@ int lce_oracle_backward(const void *h, const void *W, int dtype,
         if (st) goto out;
     }
     {
-        mm_job mp = {G, W, dtype, hd, L, H, V, 0, 0, dH, dW};
+        mm_job mp = {G, W, dtype, hd, L, H, V, 0, 0, dH, dW, vrows};
         if (dH) run_mm(mp, L, nthreads, dH_worker);
-        if (dW) run_mm(mp, V, nthreads, dW_worker);
+        if (dW) run_mm(mp, vrows ? nvrows : V, nthreads, dW_worker);
     }
     st = bad ? ORACLE_LABEL_RANGE : ORACLE_OK;
 out:
@@ -446,7 +456,7 @@ int lce_oracle_rows(const void *h, const void *W, int dtype,
         if (st) goto out;
     }
     if (dH_rows) {
-        mm_job mp = {G, W, dtype, NULL, nrows, H, V, 0, 0, dH_rows, NULL};
+        mm_job mp = {G, W, dtype, NULL, nrows, H, V, 0, 0, dH_rows, NULL, NULL};
         run_mm(mp, nrows, nthreads, dH_worker);
     }
     st = bad ? ORACLE_LABEL_RANGE : ORACLE_OK;

@@ -1,0 +1,60 @@
+"""Helpers shared by the GPU tests: tolerances and comparisons.
+
+Tolerances of the comparison with the float64 oracle, fixed for this
+library (bf16 operands, fp32 accumulation):
+  loss        relative error <= 1e-3
+  dH, dW      relative Frobenius error <= 1e-2
+  lse         max abs error <= 2e-3 (bf16 inputs: the oracle sees the same
+              bf16 values; fp32 inputs: the GPU rounds them to bf16 first)
+"""
+import numpy as np
+import pytest
+import torch
+
+LOSS_RTOL = 1e-3
+GRAD_RFRO = 1e-2
+LSE_ATOL = 2e-3
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import chunked_lm_head_gemm_gb300 as lce
+    lce.load(build_if_missing=True)
+    return torch.device("cuda:0")
+
+
+def rel_fro(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    num = np.linalg.norm(got - ref)
+    return float(num / den) if den > 0 else float(num)
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+def run_gpu(h, W, y, dloss=1.0, chunk_rows=0, ignore_index=-100):
+    """Forward + backward through the library; returns host float64 arrays."""
+    import chunked_lm_head_gemm_gb300 as lce
+    loss, lse = lce.forward(h, W, y, ignore_index)
+    d = torch.full((), float(dloss), device=h.device)
+    dH, dW = lce.backward(h, W, y, lse, d, ignore_index, chunk_rows)
+    status = lce.get_error()
+    return dict(loss=float(loss.item()), lse=to64(lse), dH=to64(dH),
+                dW=to64(dW), status=status)
+
+
+def assert_parity(gpu, f, b, lse_atol=LSE_ATOL, check_dW=True, dW_rows=None):
+    assert abs(gpu["loss"] - f["loss"]) <= LOSS_RTOL * max(abs(f["loss"]), 1e-30), \
+        f"loss {gpu['loss']} vs oracle {f['loss']}"
+    err = np.max(np.abs(gpu["lse"] - f["lse"]))
+    assert err <= lse_atol, f"lse max abs err {err}"
+    e = rel_fro(gpu["dH"], b["dH"])
+    assert e <= GRAD_RFRO, f"dH rel Frobenius err {e}"
+    if check_dW:
+        got = gpu["dW"] if dW_rows is None else gpu["dW"][dW_rows]
+        e = rel_fro(got, b["dW"])
+        assert e <= GRAD_RFRO, f"dW rel Frobenius err {e}"

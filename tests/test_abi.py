@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/lce.h declares, sizes its workspace, and rejects bad arguments
+before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import chunked_lm_head_gemm_gb300 as lce
+    return lce.load(build_if_missing=True)
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "lce.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lce_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared()
+    assert "lce_forward" in names and "lce_backward" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in lce.h but not exported"
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    assert sorted(B.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["LCE_OK", "LCE_ERR_INVALID_ARG",
+                                 "LCE_ERR_UNSUPPORTED", "LCE_ERR_WORKSPACE",
+                                 "LCE_ERR_LABEL_RANGE", "LCE_ERR_TIMEOUT",
+                                 "LCE_ERR_CUDA"]):
+        assert lib.lce_status_string(code).decode() == name
+    assert lib.lce_status_string(99).decode() == "LCE_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    f = lib.lce_workspace_size
+    assert f(0, 256, 4096, 0, 0) == 0          # L < 1
+    assert f(512, 12, 4096, 0, 0) == 0         # H % 8 != 0
+    assert f(512, 256, 4096, 7, 0) == 0        # bad dtype
+    assert f(512, 256, 4096, 0, -1) == 0       # bad chunk
+    small = f(512, 256, 4096, 0, 128)
+    big = f(512, 256, 4096, 0, 512)
+    assert 0 < small < big
+    # fp32 inputs add bf16 copies of h and W
+    assert f(512, 256, 4096, 1, 512) - big >= 2 * (512 * 256 + 4096 * 256)
+    # the gradient-logit chunk dominates: chunk * round_up(V, 8) * 2 bytes
+    L, H, V = 131072, 4096, 151936
+    c = lib.lce_default_chunk_rows(L, H, V)
+    assert c % 128 == 0 and 0 < c <= L
+    assert f(L, H, V, 0, 0) >= c * V * 2
+    # plus the forward statistics: 16 splits x (max, sum) + the label logit
+    assert f(L, H, V, 0, 0) < c * V * 2 + (16 * 8 + 4 + 1) * L + (1 << 20)
+    # peak extra memory is O(chunk * V), far below the L x V fp32 logits
+    assert f(L, H, V, 0, 0) < L * V * 4 / 8
+
+
+def test_bad_arguments_return_before_any_device_call(lib):
+    """Every call here fails validation first, so no pointer is used."""
+    p = ctypes.c_void_p(0x1000)  # aligned but never dereferenced
+    null = ctypes.c_void_p(0)
+    i = ctypes.c_int64
+    # null h
+    assert lib.lce_forward(null, p, 0, p, 8, 8, 8, -100, p, p, p, 1 << 30,
+                           null) == 1
+    # H not a multiple of 8
+    assert lib.lce_forward(p, p, 0, p, 8, 12, 8, -100, p, p, p, 1 << 30,
+                           null) == 1
+    # unsupported dtype
+    assert lib.lce_forward(p, p, 5, p, 8, 8, 8, -100, p, p, p, 1 << 30,
+                           null) == 2
+    # misaligned W
+    assert lib.lce_forward(p, ctypes.c_void_p(0x1002), 0, p, 8, 8, 8, -100,
+                           p, p, p, 1 << 30, null) == 1
+    # workspace too small
+    assert lib.lce_forward(p, p, 0, p, 8, 8, 8, -100, p, p, p, 16,
+                           null) == 3
+    assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, 0, p, p, p, 16,
+                            null) == 3
+    # negative chunk
+    assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, -5, p, p, p,
+                            1 << 30, null) == 1
+    # test hooks
+    assert lib.lce_test_gemm(null, p, p, 8, 8, 8, 0, 0, null) == 1
+    assert lib.lce_test_gemm(p, p, p, 8, 12, 8, 0, 0, null) == 1
+    assert lib.lce_test_wait_timeout(0, null) == 1
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    from chunked_lm_head_gemm_gb300 import build as Bld
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(Bld, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        B.load()

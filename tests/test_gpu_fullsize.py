@@ -1,0 +1,74 @@
+"""The head shapes at full size, in the launch configuration the benchmark
+times: sampled rows against the float64 oracle, then properties that hold
+at any size (gradient columns sum to zero, determinism, chunk-size
+invariance, loss consistent with lse)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_lm_head_gemm_gb300.inputs import WORKLOADS, make_inputs
+from tests.gpu_util import GRAD_RFRO, LSE_ATOL, rel_fro, require_gpu, to64
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["qwen3-0.6b", "qwen3-4b", "qwen3-8b", "qwen3-32b"]
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_full_size(name):
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = WORKLOADS[name]
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    L, H, V = wl.L, wl.H, wl.V
+    ws = lce.alloc_workspace(L, H, V, h.dtype, 0, dev)
+    loss, lse = lce.forward(h, W, y, workspace=ws)
+    dloss = torch.ones((), device=dev)
+    dH, dW = lce.backward(h, W, y, lse, dloss, workspace=ws)
+    assert lce.get_error() == 0
+
+    # sampled rows against the oracle: first, last, ignored, stressed, random
+    yc = y.cpu()
+    rs = np.random.default_rng(11)
+    rows = set([0, L - 1] + list(rs.integers(0, L, 10)))
+    ign = torch.nonzero(yc == -100).flatten()[:2].tolist()
+    rows.update(ign)
+    if wl.stress_frac:
+        hn = h.float().norm(dim=1)
+        rows.update(torch.topk(hn, 3).indices.cpu().tolist())
+    rows = np.array(sorted(rows), dtype=np.int64)
+    hc, Wc = h.cpu(), W.cpu()
+    r = oracle.rows(hc, Wc, yc, rows, dloss=1.0)
+    lse_g = to64(lse)[rows]
+    assert np.max(np.abs(lse_g - r["lse"])) <= LSE_ATOL
+    e = rel_fro(to64(dH[torch.from_numpy(rows).to(dev)]), r["dH"])
+    assert e <= GRAD_RFRO, f"sampled dH rows rel Frobenius err {e}"
+
+    # loss = mean over valid rows of (lse - z_y), z_y by an fp64 dot product
+    valid = (y >= 0) & (y < V)
+    idx = torch.nonzero(valid).flatten()
+    zy = torch.zeros(L, dtype=torch.float64, device=dev)
+    for s in range(0, idx.numel(), 8192):
+        ii = idx[s:s + 8192]
+        zy[ii] = (h[ii].double() * W[y[ii]].double()).sum(1)
+    ref_loss = ((lse.double() - zy)[valid]).mean().item()
+    assert abs(loss.item() - ref_loss) <= 1e-4 * abs(ref_loss)
+
+    # columns of dW sum to ~0 (rows of softmax - onehot sum to zero)
+    colsum = dW.double().sum(0)
+    scale = dW.double().abs().sum(0)
+    assert torch.max(colsum.abs() / scale).item() < 1e-2
+
+    # determinism: same inputs, same launch -> identical bits
+    loss2, lse2 = lce.forward(h, W, y, workspace=ws)
+    assert torch.equal(loss, loss2) and torch.equal(lse, lse2)
+    dH2, dW2 = lce.backward(h, W, y, lse, dloss, workspace=ws)
+    assert torch.equal(dH, dH2) and torch.equal(dW, dW2)
+    del dH2, dW2
+
+    # chunk-size invariance: dH rows do not depend on the chunking; dW only
+    # through its summation order
+    dH3, dW3 = lce.backward(h, W, y, lse, dloss, chunk_rows=4096)
+    assert torch.equal(dH, dH3)
+    assert rel_fro(to64(dW3), to64(dW)) < 1e-5

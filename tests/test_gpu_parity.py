@@ -1,0 +1,150 @@
+"""CUDA path against the float64 oracle, element by element, on seeded
+inputs small enough for the oracle: the small workload, edge cases, and row
+slices (full H and V) of every Qwen3 head shape."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_lm_head_gemm_gb300.inputs import (WORKLOADS, Workload,
+                                               make_inputs)
+from tests.gpu_util import assert_parity, rel_fro, require_gpu, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(h, W, y, dloss=1.0, vrows=None):
+    hc, Wc, yc = h.cpu(), W.cpu(), y.cpu()
+    f = oracle.forward(hc, Wc, yc)
+    b = oracle.backward(hc, Wc, yc, dloss=dloss, vrows=vrows)
+    return f, b
+
+
+def test_tiny_workload():
+    """512 x 256 x 4096, fp32 inputs, 10% ignored."""
+    dev = require_gpu()
+    h, W, y = make_inputs("tiny", seed=0, device=dev)
+    gpu = run_gpu(h, W, y)
+    assert gpu["status"] == 0
+    f, b = _oracle(h, W, y)
+    assert_parity(gpu, f, b)
+
+
+EDGE = [
+    # name, L, H, V, dtype, chunk_rows, ignore_frac, w_std
+    ("ragged_small", 3, 16, 5, "bf16", 0, 0.0, 0.5),
+    ("k_below_tile_v_odd", 130, 8, 300, "bf16", 0, 0.1, 0.3),
+    ("ragged_k", 257, 72, 1000, "bf16", 0, 0.1, 0.1),
+    ("chunk_64", 300, 64, 520, "bf16", 64, 0.1, 0.1),
+    ("chunk_100", 300, 64, 520, "bf16", 100, 0.1, 0.1),
+    ("multi_tile", 640, 256, 4100, "bf16", 256, 0.05, 0.05),
+    ("f32_ragged", 200, 40, 777, "f32", 96, 0.1, 0.1),
+    ("one_row", 1, 8, 700, "bf16", 0, 0.0, 0.5),
+]
+
+
+@pytest.mark.parametrize("name,L,H,V,dt,chunk,ign,wstd", EDGE,
+                         ids=[e[0] for e in EDGE])
+def test_edge_shapes(name, L, H, V, dt, chunk, ign, wstd):
+    dev = require_gpu()
+    wl = Workload(name, L, H, V, dt, 1.0, wstd, "uniform", ignore_frac=ign)
+    h, W, y = make_inputs(wl, seed=1, device=dev)
+    gpu = run_gpu(h, W, y, dloss=1.0, chunk_rows=chunk)
+    assert gpu["status"] == 0
+    f, b = _oracle(h, W, y)
+    assert_parity(gpu, f, b)
+
+
+def test_single_class_gives_zero():
+    """V = 1: every lse equals the one logit; loss and gradients vanish."""
+    dev = require_gpu()
+    wl = Workload("v1", 70, 16, 1, "bf16", 1.0, 0.5, "uniform")
+    h, W, y = make_inputs(wl, seed=2, device=dev)
+    gpu = run_gpu(h, W, y)
+    z = (h.double() @ W.double().T)[:, 0].cpu().numpy()
+    assert np.max(np.abs(gpu["lse"] - z)) < 1e-4 * max(1.0, np.max(np.abs(z)))
+    assert abs(gpu["loss"]) < 1e-5
+    assert np.max(np.abs(gpu["dH"])) < 1e-6 and np.max(np.abs(gpu["dW"])) < 1e-6
+
+
+def test_all_rows_ignored():
+    dev = require_gpu()
+    wl = Workload("allign", 150, 32, 400, "bf16", 1.0, 0.1, "uniform")
+    h, W, y = make_inputs(wl, seed=3, device=dev)
+    y[:] = -100
+    gpu = run_gpu(h, W, y)
+    assert gpu["status"] == 0
+    assert gpu["loss"] == 0.0
+    assert np.all(gpu["dH"] == 0.0) and np.all(gpu["dW"] == 0.0)
+    f = oracle.forward(h.cpu(), W.cpu(), y.cpu())
+    assert np.max(np.abs(gpu["lse"] - f["lse"])) < 2e-3
+
+
+def test_labels_out_of_range_are_reported_and_ignored():
+    dev = require_gpu()
+    wl = Workload("bad", 260, 32, 500, "bf16", 1.0, 0.1, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=4, device=dev)
+    y[3] = 500
+    y[77] = -7
+    y[200] = 10 ** 12
+    gpu = run_gpu(h, W, y)
+    import chunked_lm_head_gemm_gb300._binding as B
+    assert gpu["status"] == B.LCE_ERR_LABEL_RANGE
+    f, b = _oracle(h, W, y)
+    assert f["status"] == oracle.LABEL_RANGE
+    assert_parity(gpu, f, b)
+    assert B.get_error() == 0  # cleared by the read
+
+
+@pytest.mark.parametrize("dloss", [0.0, 2.5, -0.75])
+def test_dloss_scaling(dloss):
+    dev = require_gpu()
+    wl = Workload("dl", 200, 64, 700, "bf16", 1.0, 0.1, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=5, device=dev)
+    gpu = run_gpu(h, W, y, dloss=dloss)
+    if dloss == 0.0:
+        assert np.all(gpu["dH"] == 0.0) and np.all(gpu["dW"] == 0.0)
+        return
+    f, b = _oracle(h, W, y, dloss=dloss)
+    assert_parity(gpu, f, b)
+
+
+def test_autograd_function_matches_explicit_calls():
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = Workload("ag", 300, 64, 900, "bf16", 1.0, 0.1, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=6, device=dev)
+    hh = h.clone().requires_grad_(True)
+    WW = W.clone().requires_grad_(True)
+    loss = lce.linear_cross_entropy(hh, WW, y)
+    (3.0 * loss).backward()
+    gpu = run_gpu(h, W, y, dloss=3.0)
+    assert loss.item() == gpu["loss"]
+    assert torch.equal(hh.grad.float().cpu(),
+                       torch.from_numpy(gpu["dH"]).float())
+    assert rel_fro(WW.grad.double().cpu().numpy(), gpu["dW"]) < 4e-3
+
+
+SLICES = [("qwen3-0.6b", 256), ("qwen3-4b", 300), ("qwen3-8b", 256),
+          ("qwen3-32b", 256)]
+
+
+@pytest.mark.parametrize("name,rows", SLICES, ids=[s[0] for s in SLICES])
+def test_row_slice_of_head_shape(name, rows):
+    """The first rows of each head shape (full H and V = 151936); dW is
+    compared on the vocabulary rows the slice's labels touch, plus 256
+    seeded others and the last id."""
+    dev = require_gpu()
+    wl = WORKLOADS[name].with_rows(rows)
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    gpu = run_gpu(h, W, y, dloss=1.0)
+    assert gpu["status"] == 0
+    yc = y.cpu().numpy()
+    rs = np.random.default_rng(7)
+    vrows = np.unique(np.concatenate([yc[yc >= 0], rs.integers(0, wl.V, 256),
+                                      [0, wl.V - 1]]))
+    f, b = _oracle(h, W, y, vrows=vrows)
+    assert_parity(gpu, f, b, dW_rows=vrows)

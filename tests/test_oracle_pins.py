@@ -264,3 +264,13 @@ def test_threads_do_not_change_results(oracle_mod):
     b = oracle_mod.backward(h, W, y, nthreads=5)
     assert np.array_equal(a["dH"], b["dH"]) and np.array_equal(a["dW"],
                                                               b["dW"])
+
+
+def test_dW_vocab_subset_matches_whole(oracle_mod):
+    L, H, V = 20, 6, 31
+    h, W, y = _rand_problem(L, H, V, 41)
+    full = oracle_mod.backward(h, W, y, dloss=1.1)["dW"]
+    v = np.array([30, 0, 5, 5, 17])
+    sub = oracle_mod.backward(h, W, y, dloss=1.1, want_dH=False,
+                              vrows=v)["dW"]
+    np.testing.assert_array_equal(sub, full[v])
