@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark: fused linear cross-entropy forward + backward on GB300.
+
+One step = lce_forward + lce_backward over one synthetic batch of the chosen
+head shape (default: the Qwen3-8B head at one 1M-token sequence's per-GPU
+shard, L=131072, H=4096, V=151936), inputs resident in HBM. Prints one JSON
+line (rank 0):
+
+  value        whole-job tokens/s (rows of h per second), device-timed with
+               CUDA events around exactly --steps steps
+  roofline     the dominant kernel: algorithmic flops per launch / its
+               event-measured launch duration, against the bf16 tensor peak
+  cpu_baseline the float64 oracle timed on this host's cores on a bounded
+               row sample of the same workload (N=1, rank 0)
+  e2e          the same metric with pinned-host inputs copied in and the
+               results (loss, dH, dW) copied out inside the timed region
+  clocks       nvidia-smi samples taken during the timed region
+
+--impl reference times the float64 oracle instead (host cores, bounded row
+sample per step) and prints the same line with "impl": "reference".
+--gpus N under torchrun: N independent replicas, one per GPU (the library
+has no multi-GPU path), weak scaling, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("fused linear-CE fwd+bwd tokens/s and TFLOPS "
+          "(fraction of GB300 BF16 peak)")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "hbm_gbs": 6800.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _flatten(d, out=None):
+    out = {} if out is None else out
+    if isinstance(d, dict):
+        for k, v in d.items():
+            if isinstance(v, (int, float)) and not isinstance(v, bool):
+                out.setdefault(k, float(v))
+            else:
+                _flatten(v, out)
+    return out
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            flat = _flatten(json.load(open(path)))
+            peaks = dict(FALLBACK_PEAKS)
+            found = False
+            for k in FALLBACK_PEAKS:
+                if k in flat:
+                    peaks[k] = flat[k]
+                    found = True
+            if found:
+                return peaks, "measured"
+        except Exception:  # noqa: BLE001 - fall back on any parse problem
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    csrc = os.path.join(ROOT, "chunked_lm_head_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+    except Exception:  # noqa: BLE001
+        return None
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+               "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        import torch
+        self.proc = None
+        self.err = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.target = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception as e:  # noqa: BLE001
+            self.target = str(device_index)
+            self.err = repr(e)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target,
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # noqa: BLE001
+            self.err = repr(e)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"error": self.err or "nvidia-smi not started"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_median": statistics.median(power),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm and CPU baseline: the float64 oracle on host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_rate_macs(h, W, y) -> float:
+    """Multiply-adds per second of the oracle forward on a few rows."""
+    import oracle
+    n = min(4, h.shape[0])
+    t0 = time.perf_counter()
+    oracle.forward(h[:n], W, y[:n])
+    dt = time.perf_counter() - t0
+    return n * W.shape[0] * W.shape[1] / max(dt, 1e-6)
+
+
+def time_oracle_sample(h, W, y, rows: int):
+    """Float64 forward + backward (lse, loss, dH, full dW) on the first
+    `rows` rows; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward(h[:rows], W, y[:rows])
+    oracle.backward(h[:rows], W, y[:rows], dloss=1.0)
+    return time.perf_counter() - t0
+
+
+def sample_rows_for(seconds: float, rate: float, wl) -> int:
+    per_row = 4.0 * wl.H * wl.V  # fwd + recompute + dH + dW multiply-adds
+    return int(max(1, min(wl.L, round(seconds * rate / per_row))))
+
+
+def cpu_inputs(wl, rows: int):
+    """The workload's distributions on the CPU: W whole, h/labels `rows`."""
+    from chunked_lm_head_gemm_gb300.inputs import (make_hidden, make_labels,
+                                                   make_weight)
+    sub = wl.with_rows(rows)
+    return make_hidden(sub, 0, "cpu"), make_weight(wl, 0, "cpu"), \
+        make_labels(sub, 0)
+
+
+def cpu_baseline(wl, h_cpu, W_cpu, y_cpu, target_s: float = 20.0) -> dict:
+    import oracle
+    oracle.build()
+    rate = _oracle_rate_macs(h_cpu, W_cpu, y_cpu)
+    rows = min(h_cpu.shape[0], sample_rows_for(target_s, rate, wl))
+    t = time_oracle_sample(h_cpu, W_cpu, y_cpu, rows)
+    return {"value": rows / t, "unit": "tokens/s",
+            "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": (f"first {rows} of {wl.L} rows of {wl.name} (full "
+                       f"H={wl.H}, V={wl.V}); float64 forward + backward "
+                       f"(lse, loss, dH, full dW) in {t:.1f} s; tokens/s = "
+                       f"sample rows / time")}
+
+
+def run_reference(args, wl) -> dict:
+    import oracle
+    oracle.build()
+    probe_rows = 4
+    h, W, y = cpu_inputs(wl, probe_rows)
+    rate = _oracle_rate_macs(h, W, y)
+    # bounded sample per step: the whole --warmup + --steps run ~2 minutes
+    per_step_s = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    rows = sample_rows_for(per_step_s, rate, wl)
+    h, W, y = cpu_inputs(wl, rows)
+    for _ in range(args.warmup):
+        time_oracle_sample(h, W, y, rows)
+    times = [time_oracle_sample(h, W, y, rows) for _ in range(args.steps)]
+    t = statistics.median(times)
+    value = rows / t
+    cores = oracle.default_threads()
+    sample = (f"first {rows} of {wl.L} rows of {wl.name} (full H={wl.H}, "
+              f"V={wl.V}) per step; float64 forward + backward (lse, loss, "
+              f"dH, full dW); tokens/s = rows / median step time")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "L": wl.L, "H": wl.H, "V": wl.V,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="lce", choices=["lce", "reference"])
+    ap.add_argument("--config", default="qwen3-8b")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override L (a row slice of the workload)")
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    from chunked_lm_head_gemm_gb300.inputs import WORKLOADS
+    wl = WORKLOADS[args.config]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+
+    import torch
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    from chunked_lm_head_gemm_gb300.inputs import make_inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lce.load()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    L, H, V = wl.L, wl.H, wl.V
+    chunk = args.chunk_rows or lce.default_chunk_rows(L, H, V)
+    ws = lce.alloc_workspace(L, H, V, h.dtype, chunk, dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(L, dtype=torch.float32, device=dev)
+    dH = torch.empty_like(h)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    dloss = torch.ones(1, dtype=torch.float32, device=dev)
+
+    def step():
+        lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
+        lce.backward(h, W, y, lse, dloss, chunk_rows=chunk, workspace=ws,
+                     dH_out=dH, dW_out=dW)
+
+    in_bytes = h.numel() * h.element_size() + W.numel() * W.element_size()
+    flush = None
+    if in_bytes < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = lce.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error status {st} during warm-up")
+
+    # ---- timed region (device) ----
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    B.profile_start()
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        elapsed_ms = e0.elapsed_time(e1)
+    else:
+        elapsed_ms = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1.0)  # evict h and W from L2 between steps
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step()
+            e1.record()
+            torch.cuda.synchronize()
+            elapsed_ms += e0.elapsed_time(e1)
+    stats = B.profile_stop()
+    barrier()
+    clk = clocks.stop()
+    st = lce.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error status {st} in the timed region")
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max_s = t.item() / 1e3
+    tokens = float(L) * args.steps * world
+    value = tokens / t_max_s
+    ms_per_step = t.item() / args.steps
+    peaks, peak_src = load_peaks()
+    per_gpu_s = t_max_s / args.steps
+    tf_model = 6.0 * L * H * V / per_gpu_s / 1e12
+    tf_exec = 8.0 * L * H * V / per_gpu_s / 1e12
+
+    # dominant kernel: largest total event time in the timed region
+    kernels = {}
+    total_k_ms = sum(v[1] for v in stats.values()) or 1.0
+    for name, (n, ms, fl) in stats.items():
+        kernels[name] = {"launches": n, "ms_per_launch": ms / n,
+                         "share": ms / total_k_ms,
+                         "tflops": (fl / (ms / 1e3) / 1e12) if fl else None}
+    dom = max(stats.items(), key=lambda kv: kv[1][1])
+    dname, (dn, dms, dfl) = dom
+    peak_t = peaks["bf16_tflops_sustained"]
+    achieved = dfl / (dms / 1e3) / 1e12
+    traffic = load_traffic(dname, wl.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t,
+                "unit": "TFLOP/s", "frac": achieved / peak_t,
+                "traffic": traffic, "kernel": dname,
+                "flops_per_launch": dfl / dn,
+                "peak_source": f"bf16 sustained, {peak_src}"}
+    gpu_launches = int(sum(v[0] for v in stats.values()))
+
+    # ---- end to end: pinned host in, results out, inside the timed region --
+    e2e = None
+    if not args.no_e2e:
+        h_host = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+        W_host = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        h_host.copy_(h)
+        W_host.copy_(W)
+        y_host.copy_(y)
+        loss_host = torch.empty((), dtype=torch.float32, pin_memory=True)
+        dH_host = torch.empty(dH.shape, dtype=dH.dtype, pin_memory=True)
+        dW_host = torch.empty(dW.shape, dtype=dW.dtype, pin_memory=True)
+
+        def e2e_step():
+            h.copy_(h_host, non_blocking=True)
+            W.copy_(W_host, non_blocking=True)
+            y.copy_(y_host, non_blocking=True)
+            step()
+            loss_host.copy_(loss, non_blocking=True)
+            dH_host.copy_(dH, non_blocking=True)
+            dW_host.copy_(dW, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64,
+                          device=dev)
+        if dist is not None:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        assert torch.isfinite(loss_host).item()
+        e2e = {"value": tokens / (te.item() / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h_host.nbytes + W_host.nbytes +
+                                         y_host.nbytes),
+               "d2h_bytes_per_step": int(loss_host.nbytes + dH_host.nbytes +
+                                         dW_host.nbytes),
+               "wall_s": wall}
+        del h_host, W_host, dH_host, dW_host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = min(L, 512)
+        hc = h[:rows].cpu()
+        yc = y[:rows].cpu()
+        Wc = W.cpu()
+        cpu = cpu_baseline(wl, hc, Wc, yc)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "L": L, "H": H, "V": V,
+                       "inputs": wl.dtype, "chunk_rows": chunk,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": ("inputs larger than L2, no flush" if flush is None
+                              else "L2 flushed between steps (not timed)")},
+            "tflops_model": tf_model, "tflops_executed": tf_exec,
+            "frac_of_bf16_peak": tf_model / peak_t,
+            "peak_note": (f"6LHV model flops per GPU vs {peak_t} TFLOP/s bf16 "
+                          f"sustained ({peak_src}); executed basis 8LHV "
+                          "includes the backward's logit recompute"),
+            "roofline": roofline, "kernels": kernels,
+            "gpu_launches": gpu_launches, "clocks": clk, "e2e": e2e,
+            "cpu_baseline": cpu,
+            "peak_extra_bytes": int(ws.numel()),
+        }
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -33,7 +33,15 @@ IGNORE_INDEX = -100
 
 EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_backward", "lce_get_error", "lce_status_string",
-            "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout")
+            "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout",
+            "lce_profile_start", "lce_profile_stop")
+
+KERNEL_KINDS = 10
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double), ("flops", ctypes.c_double)]
 
 
 class LCEError(RuntimeError):
@@ -86,6 +94,10 @@ def load(build_if_missing: bool = False):
         lib.lce_test_gemm.restype = i32
         lib.lce_test_wait_timeout.argtypes = [u64, p]
         lib.lce_test_wait_timeout.restype = i32
+        lib.lce_profile_start.argtypes = []
+        lib.lce_profile_start.restype = i32
+        lib.lce_profile_stop.argtypes = [ctypes.POINTER(KernelStat)]
+        lib.lce_profile_stop.restype = i32
         _lib = lib
         return lib
 
@@ -209,6 +221,20 @@ def tc_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int,
 def wait_timeout_probe(timeout_ns: int, device=None):
     st = load().lce_test_wait_timeout(timeout_ns, _stream_ptr(device))
     _check(st, "lce_test_wait_timeout")
+
+
+def profile_start():
+    """Time every kernel this thread launches through the library."""
+    _check(load().lce_profile_start(), "lce_profile_start")
+
+
+def profile_stop() -> dict:
+    """Waits for the recorded launches; returns {kind: (launches, total_ms,
+    flops)} for the kinds that ran."""
+    arr = (KernelStat * KERNEL_KINDS)()
+    _check(load().lce_profile_stop(arr), "lce_profile_stop")
+    return {a.name.decode(): (a.launches, a.total_ms, a.flops) for a in arr
+            if a.launches}
 
 
 class LinearCrossEntropy(torch.autograd.Function):

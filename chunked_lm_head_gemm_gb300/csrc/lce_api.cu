@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/lce.h"
 #include "lce_internal.h"
@@ -32,6 +33,52 @@ lce_status cuda_fail(cudaError_t e, const char* where) {
                 cudaGetErrorString(e));
   return LCE_ERR_CUDA;
 }
+
+// ---- optional per-kernel timing (lce_profile_start / lce_profile_stop) ----
+// When on, every kernel this thread launches is bracketed by two CUDA events
+// on its stream; stop() waits for them and sums durations per kernel kind.
+const char* const kKindNames[LCE_KERNEL_KINDS] = {
+    "count_valid", "gemm_lse", "lse_combine", "loss_finalize", "f32_to_bf16",
+    "gemm_grad", "gemm_dH", "gemm_dW", "test_gemm", "wait_probe"};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t e0, e1;
+  double flops;
+};
+
+struct Profiler {
+  bool on = false;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  cudaEvent_t take() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+};
+thread_local Profiler t_prof;
+
+// Brackets one launch: construct before, call done(flops) after.
+struct ProfScope {
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t e0 = nullptr;
+  ProfScope(int k, cudaStream_t st) : kind(k), s(st) {
+    if (t_prof.on && (e0 = t_prof.take()) != nullptr) cudaEventRecord(e0, s);
+  }
+  void done(double flops) {
+    if (!e0) return;
+    cudaEvent_t e1 = t_prof.take();
+    if (!e1) return;
+    cudaEventRecord(e1, s);
+    t_prof.recs.push_back({kind, e0, e1, flops});
+  }
+};
 
 struct DeviceInfo {
   bool ready = false;
@@ -275,12 +322,18 @@ lce_status operands(const void* h, const void* W, lce_dtype dt, int64_t L,
   uint16_t* h16 = reinterpret_cast<uint16_t*>(ws + w.h16);
   uint16_t* w16 = reinterpret_cast<uint16_t*>(ws + w.w16);
   cudaError_t e;
-  if ((e = launch_f32_to_bf16(static_cast<const float*>(h), h16, L * H, s)) !=
-      cudaSuccess)
-    return cuda_fail(e, "f32_to_bf16(h)");
-  if ((e = launch_f32_to_bf16(static_cast<const float*>(W), w16, V * H, s)) !=
-      cudaSuccess)
-    return cuda_fail(e, "f32_to_bf16(W)");
+  {
+    ProfScope ps(LCE_K_F32_TO_BF16, s);
+    e = launch_f32_to_bf16(static_cast<const float*>(h), h16, L * H, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "f32_to_bf16(h)");
+  {
+    ProfScope ps(LCE_K_F32_TO_BF16, s);
+    e = launch_f32_to_bf16(static_cast<const float*>(W), w16, V * H, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "f32_to_bf16(W)");
   *hb = h16;
   *Wb = w16;
   return LCE_OK;
@@ -329,8 +382,12 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
     return st;
 
   auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
-  cudaError_t e = launch_count_valid(labels, L, V, ignore_index, n_valid,
-                                     dev->err, s);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V, ignore_index, n_valid, dev->err, s);
+    ps.done(0);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
 
   // logits = h W^T: M = L rows, N = V columns, K = H
@@ -348,19 +405,28 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
   p.zy = reinterpret_cast<float*>(wsb + w.zy);
   p.ignore_index = ignore_index;
-  if ((e = launch_gemm_lse(ta, tb, g, p, dev->err, grid_for(g, dev->num_sms),
-                           s)) != cudaSuccess)
-    return cuda_fail(e, "gemm_lse");
+  {
+    ProfScope ps(LCE_K_GEMM_LSE, s);
+    e = launch_gemm_lse(ta, tb, g, p, dev->err, grid_for(g, dev->num_sms), s);
+    ps.done(2.0 * L * V * H);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_lse");
 
   int nblocks = 0;
   double* block_sums = reinterpret_cast<double*>(wsb + w.block_sums);
-  if ((e = launch_lse_combine(p.part_m, p.part_s, g.splits, p.zy, labels, L, V,
-                              ignore_index, lse, block_sums, &nblocks, s)) !=
-      cudaSuccess)
-    return cuda_fail(e, "lse_combine");
-  if ((e = launch_loss_finalize(block_sums, nblocks, n_valid, loss, s)) !=
-      cudaSuccess)
-    return cuda_fail(e, "loss_finalize");
+  {
+    ProfScope ps(LCE_K_LSE_COMBINE, s);
+    e = launch_lse_combine(p.part_m, p.part_s, g.splits, p.zy, labels, L, V,
+                           ignore_index, lse, block_sums, &nblocks, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "lse_combine");
+  {
+    ProfScope ps(LCE_K_LOSS_FINALIZE, s);
+    e = launch_loss_finalize(block_sums, nblocks, n_valid, loss, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "loss_finalize");
   return LCE_OK;
 }
 
@@ -390,8 +456,12 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
     return st;
 
   auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
-  cudaError_t e = launch_count_valid(labels, L, V, ignore_index, n_valid,
-                                     dev->err, s);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V, ignore_index, n_valid, dev->err, s);
+    ps.done(0);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
 
   uint16_t* G = reinterpret_cast<uint16_t*>(wsb + w.G);
@@ -419,9 +489,11 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.G = G;
       p.ldg = w.ldg;
       p.ignore_index = ignore_index;
-      if ((e = launch_gemm_grad(ta, t_w_k, g, p, dev->err,
-                                grid_for(g, dev->num_sms), s)) != cudaSuccess)
-        return cuda_fail(e, "gemm_grad");
+      ProfScope ps(LCE_K_GEMM_GRAD, s);
+      e = launch_gemm_grad(ta, t_w_k, g, p, dev->err,
+                           grid_for(g, dev->num_sms), s);
+      ps.done(2.0 * cr * V * H);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_grad");
     }
     // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
     {
@@ -435,9 +507,11 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.accumulate = 0;
       p.dloss = dloss;
       p.n_valid = n_valid;
-      if ((e = launch_gemm_store(false, true, ta, t_w_mn, g, p, dev->err,
-                                 grid_for(g, dev->num_sms), s)) != cudaSuccess)
-        return cuda_fail(e, "gemm_dH");
+      ProfScope ps(LCE_K_GEMM_DH, s);
+      e = launch_gemm_store(false, true, ta, t_w_mn, g, p, dev->err,
+                            grid_for(g, dev->num_sms), s);
+      ps.done(2.0 * cr * H * V);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
     }
     // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
     {
@@ -452,9 +526,11 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.accumulate = c0 > 0;
       p.dloss = dloss;
       p.n_valid = n_valid;
-      if ((e = launch_gemm_store(true, true, ta, tb, g, p, dev->err,
-                                 grid_for(g, dev->num_sms), s)) != cudaSuccess)
-        return cuda_fail(e, "gemm_dW");
+      ProfScope ps(LCE_K_GEMM_DW, s);
+      e = launch_gemm_store(true, true, ta, tb, g, p, dev->err,
+                            grid_for(g, dev->num_sms), s);
+      ps.done(2.0 * V * H * cr);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_dW");
     }
   }
   return LCE_OK;
@@ -522,9 +598,11 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
   p.accumulate = 0;
   p.dloss = nullptr;
   p.n_valid = nullptr;
+  ProfScope ps(LCE_K_TEST_GEMM, static_cast<cudaStream_t>(stream));
   cudaError_t e = launch_gemm_store(a_mn != 0, b_mn != 0, ta, tb, g, p,
                                     dev->err, grid_for(g, dev->num_sms),
                                     static_cast<cudaStream_t>(stream));
+  ps.done(2.0 * M * N * K);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "test_gemm");
 }
 
@@ -533,9 +611,46 @@ lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream) {
   DeviceInfo* dev = nullptr;
   lce_status st = device_info(&dev);
   if (st != LCE_OK) return st;
+  ProfScope ps(LCE_K_WAIT_PROBE, static_cast<cudaStream_t>(stream));
   cudaError_t e = launch_wait_probe(dev->err, timeout_ns,
                                     static_cast<cudaStream_t>(stream));
+  ps.done(0);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "wait_probe");
+}
+
+lce_status lce_profile_start(void) {
+  if (t_prof.on) return LCE_ERR_INVALID_ARG;
+  t_prof.recs.clear();
+  t_prof.used = 0;
+  t_prof.on = true;
+  return LCE_OK;
+}
+
+lce_status lce_profile_stop(lce_kernel_stat* stats) {
+  if (!t_prof.on || !stats) return LCE_ERR_INVALID_ARG;
+  t_prof.on = false;
+  for (int k = 0; k < LCE_KERNEL_KINDS; ++k) {
+    stats[k].name = kKindNames[k];
+    stats[k].launches = 0;
+    stats[k].total_ms = 0.0;
+    stats[k].flops = 0.0;
+  }
+  lce_status st = LCE_OK;
+  for (const ProfRec& r : t_prof.recs) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.e0, r.e1);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "profile events");
+      continue;
+    }
+    stats[r.kind].launches += 1;
+    stats[r.kind].total_ms += ms;
+    stats[r.kind].flops += r.flops;
+  }
+  t_prof.recs.clear();
+  t_prof.used = 0;
+  return st;
 }
 
 }  // extern "C"

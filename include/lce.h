@@ -30,8 +30,8 @@
  *     caller; the library allocates nothing and keeps no pointer after the
  *     call returns (work is queued on `stream`).
  *   - Matrices are row-major and contiguous. h, W, dH and the workspace must
- *     be 16-byte aligned, and H must be a multiple of 8 (the tensor-memory
- *     copy engine needs 16-byte row strides).
+ *     be 16-byte aligned, and H must be a multiple of 8 (the TMA copy
+ *     engine needs 16-byte row strides).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *     Calls are asynchronous on that stream; none synchronises the host,
  *     except lce_get_error.
@@ -59,7 +59,7 @@ extern "C" {
 typedef enum {
   LCE_OK = 0,
   LCE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment */
-  LCE_ERR_UNSUPPORTED = 2, /* device is not sm_103 / sm_100 family, or dtype */
+  LCE_ERR_UNSUPPORTED = 2, /* device is not sm_103, or unknown dtype */
   LCE_ERR_WORKSPACE = 3,   /* ws_bytes below lce_workspace_size() */
   LCE_ERR_LABEL_RANGE = 4, /* a label outside [0, V) that is not ignore_index
                               (that row was treated as ignored) */
@@ -158,6 +158,41 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
  * pages. The GPU context stays usable.
  */
 lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * Per-kernel timing of this library's own launches, for benchmarks. No
+ * counterpart on the pages. Between lce_profile_start() and
+ * lce_profile_stop(), every kernel the calling thread launches through this
+ * library is bracketed by two CUDA events on its stream (a few microseconds
+ * per launch). lce_profile_stop waits for those events and fills
+ * stats[LCE_KERNEL_KINDS]: per kernel kind, the number of launches, the sum
+ * of their event-measured durations, and their algorithmic flops (2 M N K
+ * per tensor-core contraction, 0 for the other kernels). Host-side state
+ * only; events are created on first use and reused.
+ */
+#define LCE_KERNEL_KINDS 10
+enum {
+  LCE_K_COUNT_VALID = 0,
+  LCE_K_GEMM_LSE = 1,
+  LCE_K_LSE_COMBINE = 2,
+  LCE_K_LOSS_FINALIZE = 3,
+  LCE_K_F32_TO_BF16 = 4,
+  LCE_K_GEMM_GRAD = 5,
+  LCE_K_GEMM_DH = 6,
+  LCE_K_GEMM_DW = 7,
+  LCE_K_TEST_GEMM = 8,
+  LCE_K_WAIT_PROBE = 9
+};
+
+typedef struct {
+  const char* name; /* static string */
+  int64_t launches;
+  double total_ms;
+  double flops;
+} lce_kernel_stat;
+
+lce_status lce_profile_start(void);
+lce_status lce_profile_stop(lce_kernel_stat* stats);
 
 #ifdef __cplusplus
 }
