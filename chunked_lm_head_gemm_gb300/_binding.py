@@ -34,7 +34,7 @@ IGNORE_INDEX = -100
 EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_backward", "lce_get_error", "lce_status_string",
             "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout",
-            "lce_profile_start", "lce_profile_stop")
+            "lce_profile_start", "lce_profile_stop", "lce_forward_static")
 
 KERNEL_KINDS = 10
 
@@ -94,6 +94,9 @@ def load(build_if_missing: bool = False):
         lib.lce_test_gemm.restype = i32
         lib.lce_test_wait_timeout.argtypes = [u64, p]
         lib.lce_test_wait_timeout.restype = i32
+        lib.lce_forward_static.argtypes = [p, p, p, i64, i64, i64, i64, p, p,
+                                           p]
+        lib.lce_forward_static.restype = i32
         lib.lce_profile_start.argtypes = []
         lib.lce_profile_start.restype = i32
         lib.lce_profile_stop.argtypes = [ctypes.POINTER(KernelStat)]

@@ -340,6 +340,42 @@ lce_status operands(const void* h, const void* W, lce_dtype dt, int64_t L,
 }
 
 }  // namespace
+
+// ---- scratch of lce_forward_static -----------------------------------------
+// Callers that cannot allocate device memory (see lce_forward_static) get the
+// forward's scratch from this fixed array instead of a caller workspace.
+// Every GPU that loads the library holds these bytes until the process
+// exits. Layout: the valid-row count, the per-block loss sums, the label
+// logits, then the per-split (max, sum) partials.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int64_t kStaticMaxRows = 131072;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device. The host-side
+// name of the array is only a stand-in; the address is looked up once per
+// device, with that device current, on the first lce_forward_static call.
+lce_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return LCE_OK;
+}
+
+}  // namespace
 }  // namespace lce
 
 using namespace lce;
@@ -651,6 +687,83 @@ lce_status lce_profile_stop(lce_kernel_stat* stats) {
   t_prof.recs.clear();
   t_prof.used = 0;
   return st;
+}
+
+lce_status lce_forward_static(const void* h, const void* W,
+                              const int64_t* labels, int64_t L, int64_t H,
+                              int64_t V, int64_t ignore_index, float* loss,
+                              float* lse, void* stream) {
+  if (!h || !W || !labels || !loss || !lse) return LCE_ERR_INVALID_ARG;
+  if (!sizes_ok(L, H, V)) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  if (L > kStaticMaxRows) {
+    std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error,
+                  "lce_forward_static: L = %lld exceeds the static scratch "
+                  "limit of %lld rows",
+                  static_cast<long long>(L),
+                  static_cast<long long>(kStaticMaxRows));
+    return LCE_ERR_WORKSPACE;
+  }
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  void* scratch = nullptr;
+  if ((st = static_scratch(&scratch)) != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // carve the scratch
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  const int64_t nb = ceil_div(L, 256);
+  const size_t off_sums = 256;
+  const size_t off_zy = static_cast<size_t>(round_up(off_sums + nb * 8, 256));
+  const size_t off_part = static_cast<size_t>(round_up(off_zy + L * 4, 256));
+  const size_t part_bytes = static_cast<size_t>(round_up(L * 4, 256));
+  const int max_splits = static_cast<int>(
+      std::min<size_t>(kMaxSplits,
+                       (kStaticScratchBytes - off_part) / (2 * part_bytes)));
+  auto* n_valid = reinterpret_cast<unsigned long long*>(base);
+  double* block_sums = reinterpret_cast<double*>(base + off_sums);
+
+  // the valid-row count starts at zero on every call (a memset, not an
+  // allocation); every other region is written before it is read
+  cudaError_t e =
+      launch_count_valid(labels, L, V, ignore_index, n_valid, dev->err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+
+  const int num_m = static_cast<int>(ceil_div(L, BM));
+  const int num_n = static_cast<int>(ceil_div(V, BN));
+  int splits = 1, tps = num_n;
+  choose_splits(num_m, num_n, dev->num_sms, H, &splits, &tps);
+  if (splits > max_splits) {
+    tps = static_cast<int>(ceil_div(num_n, max_splits));
+    splits = static_cast<int>(ceil_div(num_n, tps));
+  }
+  const GemmGeom g = make_geom(L, V, H, splits, tps);
+  CUtensorMap ta, tb;
+  if ((st = tmap_kmajor(&ta, h, H, L, H, BM)) != LCE_OK) return st;
+  if ((st = tmap_kmajor(&tb, W, H, V, H, BN)) != LCE_OK) return st;
+  LseParams p{};
+  p.labels = labels;
+  p.zy = reinterpret_cast<float*>(base + off_zy);
+  p.part_m = reinterpret_cast<float*>(base + off_part);
+  p.part_s = reinterpret_cast<float*>(base + off_part + splits * part_bytes);
+  p.ignore_index = ignore_index;
+  if ((e = launch_gemm_lse(ta, tb, g, p, dev->err, grid_for(g, dev->num_sms),
+                           s)) != cudaSuccess)
+    return cuda_fail(e, "gemm_lse");
+  int nblocks = 0;
+  if ((e = launch_lse_combine(p.part_m, p.part_s, g.splits, p.zy, labels, L, V,
+                              ignore_index, lse, block_sums, &nblocks, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "lse_combine");
+  if ((e = launch_loss_finalize(block_sums, nblocks, n_valid, loss, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "loss_finalize");
+  return LCE_OK;
 }
 
 }  // extern "C"

@@ -160,6 +160,32 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
 lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /*
+ * Forward for callers that cannot allocate device memory. No counterpart on
+ * the pages: it exists for callers that have no way to provide
+ * lce_forward's workspace, such as an embedding runtime that owns all device
+ * memory and hands out only the tensors themselves, code that must not
+ * allocate after start-up (a frozen memory arena, or a latency-critical loop
+ * where cudaMalloc's implicit device synchronisation is not allowed), or a
+ * plain C host with no device allocator of its own. It computes exactly what lce_forward
+ * computes (bf16 inputs only), taking its scratch from a fixed 16 MiB
+ * array inside the library instead of a caller workspace; every GPU that
+ * loads the library holds that array until the process exits.
+ *   h, W, labels, loss, lse, stream: as for lce_forward (dt = LCE_BF16)
+ *   L must be <= 131072 rows; larger L returns LCE_ERR_WORKSPACE (see
+ *   lce_last_cuda_error) without queuing anything.
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents, so
+ * calls whose work overlaps on the GPU (two streams, or concurrent graph
+ * replays) race and give wrong results; order them on one stream.
+ */
+lce_status lce_forward_static(const void* h, const void* W,
+                              const int64_t* labels, int64_t L, int64_t H,
+                              int64_t V, int64_t ignore_index, float* loss,
+                              float* lse, void* stream);
+
+/*
  * Per-kernel timing of this library's own launches, for benchmarks. No
  * counterpart on the pages. Between lce_profile_start() and
  * lce_profile_stop(), every kernel the calling thread launches through this
