@@ -1,10 +1,16 @@
 #!/usr/bin/env python3
 """Benchmark: fused linear cross-entropy forward + backward on GB300.
 
-One step = lce_forward + lce_backward over one synthetic batch of the chosen
-head shape (default: the Qwen3-8B head at one 1M-token sequence's per-GPU
-shard, L=131072, H=4096, V=151936), inputs resident in HBM. Prints one JSON
-line (rank 0):
+One step = the loss and its gradients (dloss = 1) over one synthetic batch
+of the chosen head shape (default: the Qwen3-8B head at one 1M-token
+sequence's per-GPU shard, L=131072, H=4096, V=151936), inputs resident in
+HBM, by one of the library's two paths:
+  --mode separate  lce_forward + lce_backward (the backward recomputes the
+                   logits chunk by chunk)
+  --mode fused     lce_forward_backward + lce_scale_gradients (logits
+                   computed once; default)
+Both paths are timed; the line reports the --mode one and lists both under
+"modes". Prints one JSON line (rank 0):
 
   value        whole-job tokens/s (rows of h per second), device-timed with
                CUDA events around exactly --steps steps
@@ -261,6 +267,12 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="override L (a row slice of the workload)")
     ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--mode", default="fused", choices=["separate", "fused"])
+    ap.add_argument("--only-mode", action="store_true",
+                    help="time only --mode (profiling runs)")
+    ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
+                    help="contractions on CTA pairs (1) or single CTAs (0); "
+                         "-1 keeps the library default")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -290,6 +302,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     lce.load()
+    if args.cta_pair >= 0:
+        B.set_cta_pair(bool(args.cta_pair))
 
     def barrier():
         if dist is not None:
@@ -305,59 +319,81 @@ def main():
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     dloss = torch.ones(1, dtype=torch.float32, device=dev)
 
-    def step():
+    def step_separate():
         lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
         lce.backward(h, W, y, lse, dloss, chunk_rows=chunk, workspace=ws,
                      dH_out=dH, dW_out=dW)
+
+    def step_fused():
+        lce.forward_backward(h, W, y, chunk_rows=chunk, workspace=ws,
+                             loss_out=loss, lse_out=lse, dH_out=dH,
+                             dW_out=dW)
+        lce.scale_gradients(dH, dW, dloss)
+
+    steps = {"separate": step_separate, "fused": step_fused}
+    step = steps[args.mode]
 
     in_bytes = h.numel() * h.element_size() + W.numel() * W.element_size()
     flush = None
     if in_bytes < 4 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st = lce.get_error()
-    if st != 0:
-        raise RuntimeError(f"device error status {st} during warm-up")
-
-    # ---- timed region (device) ----
-    clocks = ClockSampler(local)
-    clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    B.profile_start()
-    if flush is None:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            step()
-        e1.record()
+    def timed(step_fn, with_clocks):
+        """W warm-up steps, then exactly K steps between CUDA events, the
+        library's per-kernel events on; returns (max-over-ranks ms, kernel
+        stats, clocks)."""
+        for _ in range(args.warmup):
+            step_fn()
         torch.cuda.synchronize()
-        elapsed_ms = e0.elapsed_time(e1)
-    else:
-        elapsed_ms = 0.0
-        for _ in range(args.steps):
-            flush.fill_(1.0)  # evict h and W from L2 between steps
+        st = lce.get_error()
+        if st != 0:
+            raise RuntimeError(f"device error status {st} during warm-up")
+        clocks = ClockSampler(local) if with_clocks else None
+        if clocks:
+            clocks.start()
+        barrier()
+        torch.cuda.synchronize()
+        B.profile_start()
+        if flush is None:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            step()
+            for _ in range(args.steps):
+                step_fn()
             e1.record()
             torch.cuda.synchronize()
-            elapsed_ms += e0.elapsed_time(e1)
-    stats = B.profile_stop()
-    barrier()
-    clk = clocks.stop()
-    st = lce.get_error()
-    if st != 0:
-        raise RuntimeError(f"device error status {st} in the timed region")
+            elapsed_ms = e0.elapsed_time(e1)
+        else:
+            elapsed_ms = 0.0
+            for _ in range(args.steps):
+                flush.fill_(1.0)  # evict h and W from L2 between steps
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                step_fn()
+                e1.record()
+                torch.cuda.synchronize()
+                elapsed_ms += e0.elapsed_time(e1)
+        stats = B.profile_stop()
+        barrier()
+        clk = clocks.stop() if clocks else None
+        st = lce.get_error()
+        if st != 0:
+            raise RuntimeError(f"device error status {st} in the timed region")
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        if dist is not None:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return tt.item(), stats, clk
 
+    modes = {}
+    if not args.only_mode:
+        for m in steps:
+            if m != args.mode:
+                ms, _, _ = timed(steps[m], False)
+                modes[m] = ms
+    elapsed_ms, stats, clk = timed(step, True)
+    modes[args.mode] = elapsed_ms
     t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
     t_max_s = t.item() / 1e3
     tokens = float(L) * args.steps * world
     value = tokens / t_max_s
@@ -365,7 +401,13 @@ def main():
     peaks, peak_src = load_peaks()
     per_gpu_s = t_max_s / args.steps
     tf_model = 6.0 * L * H * V / per_gpu_s / 1e12
-    tf_exec = 8.0 * L * H * V / per_gpu_s / 1e12
+    exec_flops = (8.0 if args.mode == "separate" else 6.0) * L * H * V
+    tf_exec = exec_flops / per_gpu_s / 1e12
+    modes_out = {m: {"ms_per_step": ms / args.steps,
+                     "tokens_per_s": float(L) * world * args.steps / (ms / 1e3),
+                     "tflops_model": 6.0 * L * H * V / (ms / args.steps / 1e3)
+                     / 1e12}
+                 for m, ms in modes.items()}
 
     # dominant kernel: largest total event time in the timed region
     kernels = {}
@@ -451,14 +493,18 @@ def main():
             "data": "synthetic",
             "config": {"workload": wl.name, "L": L, "H": H, "V": V,
                        "inputs": wl.dtype, "chunk_rows": chunk,
+                       "mode": args.mode,
+                       "cta_pair": B.get_cta_pair(),
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": ("inputs larger than L2, no flush" if flush is None
                               else "L2 flushed between steps (not timed)")},
             "tflops_model": tf_model, "tflops_executed": tf_exec,
             "frac_of_bf16_peak": tf_model / peak_t,
             "peak_note": (f"6LHV model flops per GPU vs {peak_t} TFLOP/s bf16 "
-                          f"sustained ({peak_src}); executed basis 8LHV "
-                          "includes the backward's logit recompute"),
+                          f"sustained ({peak_src}); the executed basis is "
+                          "8LHV for the separate path (the backward "
+                          "recomputes the logits), 6LHV for the fused path"),
+            "modes": modes_out,
             "roofline": roofline, "kernels": kernels,
             "gpu_launches": gpu_launches, "clocks": clk, "e2e": e2e,
             "cpu_baseline": cpu,

@@ -11,12 +11,16 @@ include/lce.h; this package is the thin Python binding.
     loss = lce.linear_cross_entropy(h, W, labels)       # autograd-aware
     loss, lse = lce.forward(h, W, labels)
     dH, dW = lce.backward(h, W, labels, lse, dloss)
+    loss, lse, dH, dW = lce.forward_backward(h, W, labels)  # no recompute
 """
 from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
                        alloc_workspace, backward, default_chunk_rows, forward,
-                       get_error, library_path, linear_cross_entropy, load,
-                       workspace_size)
+                       forward_backward, get_error, library_path,
+                       linear_cross_entropy, load, profile_start, profile_stop,
+                       scale_gradients, workspace_size)
 
 __all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "alloc_workspace",
-           "backward", "default_chunk_rows", "forward", "get_error",
-           "library_path", "linear_cross_entropy", "load", "workspace_size"]
+           "backward", "default_chunk_rows", "forward", "forward_backward",
+           "get_error", "library_path", "linear_cross_entropy", "load",
+           "profile_start", "profile_stop", "scale_gradients",
+           "workspace_size"]

@@ -34,9 +34,11 @@ IGNORE_INDEX = -100
 EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_backward", "lce_get_error", "lce_status_string",
             "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout",
-            "lce_profile_start", "lce_profile_stop", "lce_forward_static")
+            "lce_profile_start", "lce_profile_stop", "lce_forward_static",
+            "lce_forward_backward", "lce_scale_gradients",
+            "lce_set_cta_pair", "lce_get_cta_pair")
 
-KERNEL_KINDS = 10
+KERNEL_KINDS = 13
 
 
 class KernelStat(ctypes.Structure):
@@ -94,6 +96,15 @@ def load(build_if_missing: bool = False):
         lib.lce_test_gemm.restype = i32
         lib.lce_test_wait_timeout.argtypes = [u64, p]
         lib.lce_test_wait_timeout.restype = i32
+        lib.lce_forward_backward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
+                                             i64, p, p, p, p, p, sz, p]
+        lib.lce_forward_backward.restype = i32
+        lib.lce_scale_gradients.argtypes = [p, i32, i64, i64, p, i64, p, p]
+        lib.lce_scale_gradients.restype = i32
+        lib.lce_set_cta_pair.argtypes = [i32]
+        lib.lce_set_cta_pair.restype = i32
+        lib.lce_get_cta_pair.argtypes = []
+        lib.lce_get_cta_pair.restype = i32
         lib.lce_forward_static.argtypes = [p, p, p, i64, i64, i64, i64, p, p,
                                            p]
         lib.lce_forward_static.restype = i32
@@ -203,6 +214,45 @@ def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
     return dH, dW
 
 
+def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
+                     ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
+                     workspace=None, loss_out=None, lse_out=None, dH_out=None,
+                     dW_out=None):
+    """Loss, lse and the gradients of the loss itself (dloss = 1) in one
+    call, without recomputing the logits. Returns (loss, lse, dH, dW)."""
+    lib = load()
+    _check_inputs(h, W, labels)
+    L, H = h.shape
+    V = W.shape[0]
+    dev = h.device
+    if workspace is None:
+        workspace = alloc_workspace(L, H, V, h.dtype, chunk_rows, dev)
+    loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float32, device=dev)
+    lse = lse_out if lse_out is not None else torch.empty(L, dtype=torch.float32, device=dev)
+    dH = dH_out if dH_out is not None else torch.empty_like(h)
+    dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
+    st = lib.lce_forward_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                                  labels.data_ptr(), L, H, V, ignore_index,
+                                  chunk_rows, loss.data_ptr(), lse.data_ptr(),
+                                  dH.data_ptr(), dW.data_ptr(),
+                                  workspace.data_ptr(), workspace.numel(),
+                                  _stream_ptr(dev))
+    _check(st, "lce_forward_backward")
+    return loss, lse, dH, dW
+
+
+def scale_gradients(dH: torch.Tensor, dW: torch.Tensor, dloss: torch.Tensor):
+    """dH *= dloss and dW *= dloss in place (dloss a device scalar)."""
+    L, H = dH.shape
+    V = dW.shape[0]
+    dloss = dloss.reshape(1).to(device=dH.device, dtype=torch.float32).contiguous()
+    st = load().lce_scale_gradients(dH.data_ptr(), _dtype_code(dH), L, H,
+                                    dW.data_ptr(), V, dloss.data_ptr(),
+                                    _stream_ptr(dH.device))
+    _check(st, "lce_scale_gradients")
+    return dH, dW
+
+
 def get_error(device=None) -> int:
     """Synchronises the current stream and returns (and clears) the device
     error status: LCE_OK, LCE_ERR_LABEL_RANGE or LCE_ERR_TIMEOUT."""
@@ -226,6 +276,15 @@ def wait_timeout_probe(timeout_ns: int, device=None):
     _check(st, "lce_test_wait_timeout")
 
 
+def set_cta_pair(enable: bool):
+    """Run the contractions on CTA pairs (cta_group::2) or single CTAs."""
+    _check(load().lce_set_cta_pair(1 if enable else 0), "lce_set_cta_pair")
+
+
+def get_cta_pair() -> bool:
+    return bool(load().lce_get_cta_pair())
+
+
 def profile_start():
     """Time every kernel this thread launches through the library."""
     _check(load().lce_profile_start(), "lce_profile_start")
@@ -243,25 +302,40 @@ def profile_stop() -> dict:
 class LinearCrossEntropy(torch.autograd.Function):
     """loss = mean cross entropy of h W^T against labels, without the logits.
 
-    Forward saves only lse [L] (4 bytes per row); backward recomputes the
-    logits chunk by chunk in the library."""
+    fused=False: forward saves only lse [L] (4 bytes per row); backward
+    recomputes the logits chunk by chunk in the library.
+    fused=True: forward computes the loss and the gradients in one call
+    (no recompute) and keeps dH, dW until backward scales them by dloss."""
 
     @staticmethod
-    def forward(ctx, h, W, labels, ignore_index=IGNORE_INDEX, chunk_rows=0):
-        loss, lse = forward(h, W, labels, ignore_index)
-        ctx.save_for_backward(h, W, labels, lse)
+    def forward(ctx, h, W, labels, ignore_index=IGNORE_INDEX, chunk_rows=0,
+                fused=False):
         ctx.ignore_index = ignore_index
         ctx.chunk_rows = chunk_rows
+        ctx.fused = fused
+        ctx.w_dtype = W.dtype
+        if fused:
+            loss, _, dH, dW = forward_backward(h, W, labels, ignore_index,
+                                               chunk_rows)
+            ctx.save_for_backward(dH, dW)
+        else:
+            loss, lse = forward(h, W, labels, ignore_index)
+            ctx.save_for_backward(h, W, labels, lse)
         return loss
 
     @staticmethod
     def backward(ctx, dloss):
-        h, W, labels, lse = ctx.saved_tensors
-        dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,
-                          ctx.chunk_rows)
-        return dH, dW.to(W.dtype), None, None, None
+        if ctx.fused:
+            dH, dW = ctx.saved_tensors
+            scale_gradients(dH, dW, dloss)
+        else:
+            h, W, labels, lse = ctx.saved_tensors
+            dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,
+                              ctx.chunk_rows)
+        return dH, dW.to(ctx.w_dtype), None, None, None, None
 
 
 def linear_cross_entropy(h, W, labels, ignore_index: int = IGNORE_INDEX,
-                         chunk_rows: int = 0):
-    return LinearCrossEntropy.apply(h, W, labels, ignore_index, chunk_rows)
+                         chunk_rows: int = 0, fused: bool = False):
+    return LinearCrossEntropy.apply(h, W, labels, ignore_index, chunk_rows,
+                                    fused)

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -38,8 +39,10 @@ lce_status cuda_fail(cudaError_t e, const char* where) {
 // When on, every kernel this thread launches is bracketed by two CUDA events
 // on its stream; stop() waits for them and sums durations per kernel kind.
 const char* const kKindNames[LCE_KERNEL_KINDS] = {
-    "count_valid", "gemm_lse", "lse_combine", "loss_finalize", "f32_to_bf16",
-    "gemm_grad", "gemm_dH", "gemm_dW", "test_gemm", "wait_probe"};
+    "count_valid", "gemm_lse",   "lse_combine",   "loss_finalize",
+    "f32_to_bf16", "gemm_grad",  "gemm_dH",       "gemm_dW",
+    "test_gemm",   "wait_probe", "gemm_fused",    "grad_from_exp",
+    "scale_grads"};
 
 struct ProfRec {
   int kind;
@@ -84,6 +87,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
+  int pair_slots = 0;       // co-resident CTA pairs of the pair kernels
   unsigned* err = nullptr;  // device address of g_error_word
 };
 
@@ -114,12 +118,30 @@ lce_status device_info(DeviceInfo** out) {
       if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess)
         return cuda_fail(e, "cudaGetSymbolAddress");
       d.err = static_cast<unsigned*>(p);
+      if ((e = pair_max_active_clusters(&d.pair_slots)) != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
     }
     d.ready = true;
   }
   if (!d.supported) return LCE_ERR_UNSUPPORTED;
   *out = &d;
   return LCE_OK;
+}
+
+// Contractions on single CTAs (128 x 256 tiles) or on CTA pairs
+// (256 x 256 tiles, tcgen05 cta_group::2). LCE_CTA_PAIR=0/1 in the
+// environment or lce_set_cta_pair() choose; the default is kDefaultPair.
+constexpr int kDefaultPair = 0;
+std::atomic<int> g_pair_mode{-1};
+
+bool use_pair() {
+  int v = g_pair_mode.load();
+  if (v < 0) {
+    const char* s = std::getenv("LCE_CTA_PAIR");
+    v = (s && *s) ? (std::atoi(s) != 0) : kDefaultPair;
+    g_pair_mode.store(v);
+  }
+  return v != 0;
 }
 
 uint64_t wait_timeout_ns() {
@@ -206,8 +228,8 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // every CTA sweeps W), then the smallest count whose static schedule is
 // within 5% of the best one.
 void choose_splits(int num_m, int num_n, int nsm, int64_t K, int* splits,
-                   int* tps) {
-  const double panel = static_cast<double>(BM) * K * 2.0;
+                   int* tps, int rows_per_unit = BM) {
+  const double panel = static_cast<double>(rows_per_unit) * K * 2.0;
   int s_min = static_cast<int>(std::ceil(nsm * panel / 48e6));
   const int s_max = std::max(1, std::min(kMaxSplits, num_n));
   s_min = std::max(1, std::min(s_min, s_max));
@@ -233,12 +255,13 @@ void choose_splits(int num_m, int num_n, int nsm, int64_t K, int* splits,
   *splits = 1;
 }
 
-GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps) {
+GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps,
+                   int rows_per_unit = BM) {
   GemmGeom g{};
   g.M = M;
   g.N = N;
   g.K = K;
-  g.num_m = static_cast<int>(ceil_div(M, BM));
+  g.num_m = static_cast<int>(ceil_div(M, rows_per_unit));
   g.num_n = static_cast<int>(ceil_div(N, BN));
   g.num_kb = static_cast<int>(ceil_div(K, BK));
   g.splits = splits;
@@ -248,18 +271,78 @@ GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps) {
   return g;
 }
 
-// One contraction per output tile (dH, dW, the test GEMM).
-GemmGeom tile_geom(int64_t M, int64_t N, int64_t K) {
-  const int num_n = static_cast<int>(ceil_div(N, BN));
-  return make_geom(M, N, K, num_n, 1);
-}
-
 int grid_for(const GemmGeom& g, int nsm) {
   return std::max(1, std::min(g.num_units, nsm));
 }
 
+// One contraction D[M,N] = A[M,K] B[K,N] as the kernels see it: each operand
+// by its base pointer, row stride (elements) and major-ness.
+struct GemmOperands {
+  int64_t M, N, K;
+  bool a_mn, b_mn;     // A stored [K][M] / B stored [K][N] (else [M][K], [N][K])
+  const void* a;
+  int64_t a_ld;
+  const void* b;
+  int64_t b_ld;
+  bool sweep;          // sweep all column tiles per row block (choose splits)
+};
+
+struct GemmPlan {
+  bool pair;
+  GemmGeom g;
+  CUtensorMap ta, tb;
+  int grid;
+};
+
+lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
+                     GemmPlan* pl) {
+  pl->pair = use_pair() && dev.pair_slots > 0;
+  const int rows_unit = pl->pair ? 2 * BM : BM;
+  const int slots = pl->pair ? dev.pair_slots : dev.num_sms;
+  const int num_m = static_cast<int>(ceil_div(o.M, rows_unit));
+  const int num_n = static_cast<int>(ceil_div(o.N, BN));
+  int splits = num_n, tps = 1;
+  if (o.sweep) choose_splits(num_m, num_n, slots, o.K, &splits, &tps, rows_unit);
+  pl->g = make_geom(o.M, o.N, o.K, splits, tps, rows_unit);
+  lce_status st = o.a_mn ? tmap_mnmajor(&pl->ta, o.a, o.M, o.K, o.a_ld)
+                         : tmap_kmajor(&pl->ta, o.a, o.K, o.M, o.a_ld, BM);
+  if (st != LCE_OK) return st;
+  st = o.b_mn ? tmap_mnmajor(&pl->tb, o.b, o.N, o.K, o.b_ld)
+              : tmap_kmajor(&pl->tb, o.b, o.K, o.N, o.b_ld,
+                            pl->pair ? BM : BN);
+  if (st != LCE_OK) return st;
+  const int units = std::max(1, std::min(pl->g.num_units, slots));
+  pl->grid = pl->pair ? 2 * units : units;
+  return LCE_OK;
+}
+
+cudaError_t run_lse(const GemmPlan& pl, const LseParams& p, unsigned* err,
+                    cudaStream_t s) {
+  return pl.pair ? launch_gemm_pair_lse(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
+                 : launch_gemm_lse(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
+}
+cudaError_t run_grad(const GemmPlan& pl, const GradParams& p, unsigned* err,
+                     cudaStream_t s) {
+  return pl.pair ? launch_gemm_pair_grad(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
+                 : launch_gemm_grad(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
+}
+cudaError_t run_fused(const GemmPlan& pl, const FusedParams& p, unsigned* err,
+                      cudaStream_t s) {
+  return pl.pair
+             ? launch_gemm_pair_fused(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
+             : launch_gemm_fused(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
+}
+cudaError_t run_store(const GemmPlan& pl, bool a_mn, bool b_mn,
+                      const StoreParams& p, unsigned* err, cudaStream_t s) {
+  return pl.pair ? launch_gemm_pair_store(a_mn, b_mn, pl.ta, pl.tb, pl.g, p,
+                                          err, pl.grid, s)
+                 : launch_gemm_store(a_mn, b_mn, pl.ta, pl.tb, pl.g, p, err,
+                                     pl.grid, s);
+}
+
 struct WsLayout {
-  size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, total;
+  size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, tile_max,
+      total;
   int64_t chunk, ldg;
 };
 
@@ -287,7 +370,14 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
     off = static_cast<size_t>(round_up(static_cast<int64_t>(off + bytes), 256));
     return o;
   };
-  const int64_t nb = ceil_div(L, 256);
+  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : default_chunk(L, V);
+  w.ldg = round_up(V, 8);
+  // per-256-row loss sums: one set over all rows (forward), or one set per
+  // row chunk (fused forward+backward), whichever is longer
+  const int64_t nchunks = ceil_div(L, w.chunk);
+  const int64_t nb_fused = (nchunks - 1) * ceil_div(w.chunk, 256) +
+                           ceil_div(L - (nchunks - 1) * w.chunk, 256);
+  const int64_t nb = std::max(ceil_div(L, 256), nb_fused);
   w.n_valid = take(8);
   w.block_sums = take(nb * 8);
   w.part_m = take(static_cast<size_t>(kMaxSplits) * L * 4);
@@ -299,9 +389,8 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
   } else {
     w.h16 = w.w16 = 0;
   }
-  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : default_chunk(L, V);
-  w.ldg = round_up(V, 8);
   w.G = take(static_cast<size_t>(w.chunk) * w.ldg * 2);
+  w.tile_max = take(static_cast<size_t>(w.chunk) * ceil_div(V, BN) * 4);
   w.total = off;
   return w;
 }
@@ -427,14 +516,11 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
 
   // logits = h W^T: M = L rows, N = V columns, K = H
-  const int num_m = static_cast<int>(ceil_div(L, BM));
-  const int num_n = static_cast<int>(ceil_div(V, BN));
-  int splits = 1, tps = num_n;
-  choose_splits(num_m, num_n, dev->num_sms, H, &splits, &tps);
-  const GemmGeom g = make_geom(L, V, H, splits, tps);
-  CUtensorMap ta, tb;
-  if ((st = tmap_kmajor(&ta, hb, H, L, H, BM)) != LCE_OK) return st;
-  if ((st = tmap_kmajor(&tb, Wb, H, V, H, BN)) != LCE_OK) return st;
+  GemmPlan pl;
+  if ((st = plan_gemm({L, V, H, false, false, hb, H, Wb, H, true}, *dev,
+                      &pl)) != LCE_OK)
+    return st;
+  const GemmGeom& g = pl.g;
   LseParams p{};
   p.labels = labels;
   p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
@@ -443,7 +529,7 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   p.ignore_index = ignore_index;
   {
     ProfScope ps(LCE_K_GEMM_LSE, s);
-    e = launch_gemm_lse(ta, tb, g, p, dev->err, grid_for(g, dev->num_sms), s);
+    e = run_lse(pl, p, dev->err, s);
     ps.done(2.0 * L * V * H);
   }
   if (e != cudaSuccess) return cuda_fail(e, "gemm_lse");
@@ -502,9 +588,6 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
 
   uint16_t* G = reinterpret_cast<uint16_t*>(wsb + w.G);
   const size_t dh_elem = dt == LCE_F32 ? 4 : 2;
-  CUtensorMap t_w_k, t_w_mn;
-  if ((st = tmap_kmajor(&t_w_k, Wb, H, V, H, BN)) != LCE_OK) return st;
-  if ((st = tmap_mnmajor(&t_w_mn, Wb, H, V, H)) != LCE_OK) return st;
 
   for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
     const int64_t cr = std::min(w.chunk, L - c0);
@@ -512,13 +595,10 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
 
     // (1) recompute z_c = h_c W^T and write G_c = softmax - onehot (bf16)
     {
-      const int num_m = static_cast<int>(ceil_div(cr, BM));
-      const int num_n = static_cast<int>(ceil_div(V, BN));
-      int splits = 1, tps = num_n;
-      choose_splits(num_m, num_n, dev->num_sms, H, &splits, &tps);
-      const GemmGeom g = make_geom(cr, V, H, splits, tps);
-      CUtensorMap ta;
-      if ((st = tmap_kmajor(&ta, hc, H, cr, H, BM)) != LCE_OK) return st;
+      GemmPlan pl;
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true}, *dev,
+                          &pl)) != LCE_OK)
+        return st;
       GradParams p{};
       p.labels = labels + c0;
       p.lse = lse + c0;
@@ -526,16 +606,16 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.ldg = w.ldg;
       p.ignore_index = ignore_index;
       ProfScope ps(LCE_K_GEMM_GRAD, s);
-      e = launch_gemm_grad(ta, t_w_k, g, p, dev->err,
-                           grid_for(g, dev->num_sms), s);
+      e = run_grad(pl, p, dev->err, s);
       ps.done(2.0 * cr * V * H);
       if (e != cudaSuccess) return cuda_fail(e, "gemm_grad");
     }
     // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
     {
-      const GemmGeom g = tile_geom(cr, H, V);
-      CUtensorMap ta;
-      if ((st = tmap_kmajor(&ta, G, V, cr, w.ldg, BM)) != LCE_OK) return st;
+      GemmPlan pl;
+      if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false},
+                          *dev, &pl)) != LCE_OK)
+        return st;
       StoreParams p{};
       p.out = static_cast<uint8_t*>(dH) + c0 * H * dh_elem;
       p.ldo = H;
@@ -544,17 +624,16 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.dloss = dloss;
       p.n_valid = n_valid;
       ProfScope ps(LCE_K_GEMM_DH, s);
-      e = launch_gemm_store(false, true, ta, t_w_mn, g, p, dev->err,
-                            grid_for(g, dev->num_sms), s);
+      e = run_store(pl, false, true, p, dev->err, s);
       ps.done(2.0 * cr * H * V);
       if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
     }
     // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
     {
-      const GemmGeom g = tile_geom(V, H, cr);
-      CUtensorMap ta, tb;
-      if ((st = tmap_mnmajor(&ta, G, V, cr, w.ldg)) != LCE_OK) return st;
-      if ((st = tmap_mnmajor(&tb, hc, H, cr, H)) != LCE_OK) return st;
+      GemmPlan pl;
+      if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false},
+                          *dev, &pl)) != LCE_OK)
+        return st;
       StoreParams p{};
       p.out = dW;
       p.ldo = H;
@@ -563,13 +642,167 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.dloss = dloss;
       p.n_valid = n_valid;
       ProfScope ps(LCE_K_GEMM_DW, s);
-      e = launch_gemm_store(true, true, ta, tb, g, p, dev->err,
-                            grid_for(g, dev->num_sms), s);
+      e = run_store(pl, true, true, p, dev->err, s);
       ps.done(2.0 * V * H * cr);
       if (e != cudaSuccess) return cuda_fail(e, "gemm_dW");
     }
   }
   return LCE_OK;
+}
+
+lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
+                                const int64_t* labels, int64_t L, int64_t H,
+                                int64_t V, int64_t ignore_index,
+                                int64_t chunk_rows, float* loss, float* lse,
+                                void* dH, float* dW, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (!h || !W || !labels || !loss || !lse || !dH || !dW || !ws)
+    return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, V) || chunk_rows < 0) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(dH) ||
+      !aligned16(dW) || (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, V, dt, chunk_rows);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, V, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V, ignore_index, n_valid, dev->err, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+
+  uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
+  float* tile_max = reinterpret_cast<float*>(wsb + w.tile_max);
+  float* part_m = reinterpret_cast<float*>(wsb + w.part_m);
+  float* part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  float* zy = reinterpret_cast<float*>(wsb + w.zy);
+  double* block_sums = reinterpret_cast<double*>(wsb + w.block_sums);
+  const size_t dh_elem = dt == LCE_F32 ? 4 : 2;
+  const int num_n = static_cast<int>(ceil_div(V, BN));
+
+  int block_off = 0;
+  for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
+    const int64_t cr = std::min(w.chunk, L - c0);
+    const uint16_t* hc = static_cast<const uint16_t*>(hb) + c0 * H;
+    // (1) logits of the chunk -> forward statistics + tile exponentials
+    int splits = 1;
+    {
+      GemmPlan pl;
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true}, *dev,
+                          &pl)) != LCE_OK)
+        return st;
+      splits = pl.g.splits;
+      FusedParams p{};
+      p.labels = labels + c0;
+      p.part_m = part_m;
+      p.part_s = part_s;
+      p.zy = zy;
+      p.E = E;
+      p.ldg = w.ldg;
+      p.tile_max = tile_max;
+      p.ignore_index = ignore_index;
+      ProfScope ps(LCE_K_GEMM_FUSED, s);
+      e = run_fused(pl, p, dev->err, s);
+      ps.done(2.0 * cr * V * H);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_fused");
+    }
+    // (2) the chunk's lse and loss terms
+    {
+      int nb = 0;
+      ProfScope ps(LCE_K_LSE_COMBINE, s);
+      e = launch_lse_combine(part_m, part_s, splits, zy, labels + c0, cr, V,
+                             ignore_index, lse + c0, block_sums + block_off,
+                             &nb, s);
+      ps.done(0);
+      if (e != cudaSuccess) return cuda_fail(e, "lse_combine");
+      block_off += nb;
+    }
+    // (3) exponentials -> softmax - onehot, in place
+    {
+      ProfScope ps(LCE_K_GRAD_FROM_EXP, s);
+      e = launch_grad_from_exp(E, w.ldg, tile_max, num_n, lse + c0,
+                               labels + c0, cr, V, ignore_index, s);
+      ps.done(0);
+      if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
+    }
+    // (4) dH_c = G_c W / N
+    {
+      GemmPlan pl;
+      if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false},
+                          *dev, &pl)) != LCE_OK)
+        return st;
+      StoreParams p{};
+      p.out = static_cast<uint8_t*>(dH) + c0 * H * dh_elem;
+      p.ldo = H;
+      p.out_f32 = dt == LCE_F32;
+      p.accumulate = 0;
+      p.dloss = nullptr;
+      p.n_valid = n_valid;
+      ProfScope ps(LCE_K_GEMM_DH, s);
+      e = run_store(pl, false, true, p, dev->err, s);
+      ps.done(2.0 * cr * H * V);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
+    }
+    // (5) dW (+)= G_c^T h_c / N
+    {
+      GemmPlan pl;
+      if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false},
+                          *dev, &pl)) != LCE_OK)
+        return st;
+      StoreParams p{};
+      p.out = dW;
+      p.ldo = H;
+      p.out_f32 = 1;
+      p.accumulate = c0 > 0;
+      p.dloss = nullptr;
+      p.n_valid = n_valid;
+      ProfScope ps(LCE_K_GEMM_DW, s);
+      e = run_store(pl, true, true, p, dev->err, s);
+      ps.done(2.0 * V * H * cr);
+      if (e != cudaSuccess) return cuda_fail(e, "gemm_dW");
+    }
+  }
+  {
+    ProfScope ps(LCE_K_LOSS_FINALIZE, s);
+    e = launch_loss_finalize(block_sums, block_off, n_valid, loss, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "loss_finalize");
+  return LCE_OK;
+}
+
+lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
+                               float* dW, int64_t V, const float* dloss,
+                               void* stream) {
+  if (!dH || !dW || !dloss) return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, V)) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(dH) || !aligned16(dW) ||
+      (reinterpret_cast<uintptr_t>(dloss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(LCE_K_SCALE_GRADS, s);
+  cudaError_t e = launch_scale_grads(dH, dt == LCE_F32, L * H, dW, V * H,
+                                     dloss, s);
+  ps.done(0);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "scale_grads");
 }
 
 lce_status lce_get_error(void* stream) {
@@ -621,12 +854,11 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
   DeviceInfo* dev = nullptr;
   lce_status st = device_info(&dev);
   if (st != LCE_OK) return st;
-  const GemmGeom g = tile_geom(M, N, K);
-  CUtensorMap ta, tb;
-  st = a_mn ? tmap_mnmajor(&ta, A, M, K, M) : tmap_kmajor(&ta, A, K, M, K, BM);
-  if (st != LCE_OK) return st;
-  st = b_mn ? tmap_mnmajor(&tb, B, N, K, N) : tmap_kmajor(&tb, B, K, N, K, BN);
-  if (st != LCE_OK) return st;
+  GemmPlan pl;
+  if ((st = plan_gemm({M, N, K, a_mn != 0, b_mn != 0, A, a_mn ? M : K, B,
+                       b_mn ? N : K, false},
+                      *dev, &pl)) != LCE_OK)
+    return st;
   StoreParams p{};
   p.out = D;
   p.ldo = N;
@@ -635,9 +867,8 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
   p.dloss = nullptr;
   p.n_valid = nullptr;
   ProfScope ps(LCE_K_TEST_GEMM, static_cast<cudaStream_t>(stream));
-  cudaError_t e = launch_gemm_store(a_mn != 0, b_mn != 0, ta, tb, g, p,
-                                    dev->err, grid_for(g, dev->num_sms),
-                                    static_cast<cudaStream_t>(stream));
+  cudaError_t e = run_store(pl, a_mn != 0, b_mn != 0, p, dev->err,
+                            static_cast<cudaStream_t>(stream));
   ps.done(2.0 * M * N * K);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "test_gemm");
 }
@@ -653,6 +884,14 @@ lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream) {
   ps.done(0);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "wait_probe");
 }
+
+lce_status lce_set_cta_pair(int enable) {
+  if (enable != 0 && enable != 1) return LCE_ERR_INVALID_ARG;
+  g_pair_mode.store(enable);
+  return LCE_OK;
+}
+
+int lce_get_cta_pair(void) { return use_pair() ? 1 : 0; }
 
 lce_status lce_profile_start(void) {
   if (t_prof.on) return LCE_ERR_INVALID_ARG;

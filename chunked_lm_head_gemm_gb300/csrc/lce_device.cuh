@@ -250,14 +250,21 @@ __device__ __forceinline__ bool label_valid(int64_t y, int64_t V,
 // ---------------------------------------------------------------------------
 struct Unit {
   int m_blk, split, n_first, n_count;
+  int64_t row0;  // first output row held in this CTA's accumulator
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u) {
+// rows_per_unit = BM for single-CTA tiles, 2 * BM for CTA-pair tiles (the
+// pair's second CTA holds rows row0 + BM ...).
+__device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u,
+                                            int rows_per_unit = BM,
+                                            int rank = 0) {
   Unit t;
   t.m_blk = u / g.splits;
   t.split = u - t.m_blk * g.splits;
   t.n_first = t.split * g.tiles_per_split;
   t.n_count = min(g.tiles_per_split, g.num_n - t.n_first);
+  t.row0 = static_cast<int64_t>(t.m_blk) * rows_per_unit +
+           static_cast<int64_t>(rank) * BM;
   return t;
 }
 
@@ -277,7 +284,7 @@ struct EpiLse {
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
-    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row = t.row0 + r;
     row_ok = row < g.M;
     yv = -1;
     if (row_ok) {
@@ -345,7 +352,7 @@ struct EpiGrad {
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
-    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row = t.row0 + r;
     row_ok = row < g.M;
     yv = -1;
     lse2 = 0.f;
@@ -398,8 +405,108 @@ struct EpiGrad {
                                            const Unit&, int) {}
 };
 
+// Fused forward+backward over one row chunk. Two passes over each tile's
+// TMEM columns: the first finds the tile's row maximum m_t (log2 units) and
+// gathers the label logit; the second writes e = 2^(u - m_t) in bf16 and
+// sums the fp32 values. (m_t, sum) then merge into the row's running
+// (max, sum) exactly as in EpiLse, and m_t is stored so that a later pass
+// can turn e into softmax - onehot once the row's lse is known.
+struct EpiFused {
+  using Params = FusedParams;
+  float m2, s;
+  int64_t row;
+  int yv;
+  bool row_ok;
+
+  __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = t.row0 + r;
+    row_ok = row < g.M;
+    yv = -1;
+    if (row_ok) {
+      const int64_t y = p.labels[row];
+      if (label_valid(y, g.N, p.ignore_index)) yv = static_cast<int>(y);
+    }
+    m2 = -INFINITY;
+    s = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+    // pass 1: tile maximum, label logit
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      const int64_t rem = g.N - j0;
+      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int yo = yv - static_cast<int>(j0);
+      if (static_cast<unsigned>(yo) < 32u) {
+        float zyv = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i == yo) zyv = v[i];
+        if (row_ok) p.zy[row] = zyv;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nv) mx[i & 3] = fmaxf(mx[i & 3], v[i] * LOG2E);
+    }
+    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    // pass 2: exponentials relative to the tile maximum
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      const int64_t rem = g.N - j0;
+      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
+        acc[i & 3] += v[i];
+      }
+      if (!row_ok) continue;
+      uint16_t* dst = p.E + row * p.ldg + j0;
+      if (nv == 32) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                             pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                             pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) dst[i] = to_bf16_bits(v[i]);
+      }
+    }
+    const float st = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float mn = fmaxf(m2, mt);
+    s = s * ex2(m2 - mn) + st * ex2(mt - mn);
+    m2 = mn;
+    if (row_ok) p.tile_max[row * g.num_n + n_blk] = mt;
+  }
+
+  __device__ __forceinline__ void end_unit(const Params& p, const GemmGeom& g,
+                                           const Unit& t, int) {
+    if (row_ok) {
+      p.part_m[static_cast<int64_t>(t.split) * g.M + row] = m2;
+      p.part_s[static_cast<int64_t>(t.split) * g.M + row] = s;
+    }
+  }
+};
+
 // out[row][col] (+)= scale * acc, fp32 or bf16. scale = dloss / N when the
-// parameters carry them (N = 0 gives 0), else 1.
+// parameters carry them (N = 0 gives 0; a missing dloss counts as 1), else 1.
 struct EpiStore {
   using Params = StoreParams;
   int64_t row;
@@ -408,14 +515,15 @@ struct EpiStore {
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
-    row = static_cast<int64_t>(t.m_blk) * BM + r;
+    row = t.row0 + r;
     row_ok = row < g.M;
     scale = 1.f;
-    if (p.dloss != nullptr) {
+    if (p.n_valid != nullptr) {
       const unsigned long long n = *p.n_valid;
-      scale = n ? static_cast<float>(static_cast<double>(*p.dloss) /
-                                     static_cast<double>(n))
-                : 0.f;
+      const double d = p.dloss != nullptr ? *p.dloss : 1.0;
+      scale = n ? static_cast<float>(d / static_cast<double>(n)) : 0.f;
+    } else if (p.dloss != nullptr) {
+      scale = *p.dloss;
     }
   }
 
@@ -711,6 +819,391 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb,
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, g, p, err);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// CTA-pair contraction (tcgen05 cta_group::2): a cluster of two CTAs on two
+// SMs computes one 256 x 256 output tile. Each CTA loads 128 rows of A and
+// 128 rows (columns of the output) of B per k-slice into its own shared
+// memory; the pair's first CTA (the leader) issues 256x256x16 MMAs that read
+// both CTAs' operands and write rows 0..127 into its own TMEM and rows
+// 128..255 into its peer's. Per CTA a stage is 32 KB instead of 48 KB, so the
+// ring is 6 deep, and the B operand is read from shared memory once per pair.
+//   - full[s]    (leader's): the leader's producer posts the stage's bytes of
+//                both CTAs; both CTAs' TMA copies complete on it;
+//   - empty[s]   (each CTA's): the leader's commit arrives on both;
+//   - tfull[a]   (each CTA's): the leader's commit arrives on both;
+//   - tempty[a]  (leader's): one arrival per epilogue warp of both CTAs.
+// ===========================================================================
+constexpr int STAGES2 = 6;
+constexpr int A2_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B2_STAGE_BYTES = BM * BK * 2;  // 16 KB: half of the 256 columns
+constexpr int STAGE2_BYTES = A2_STAGE_BYTES + B2_STAGE_BYTES;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (either CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile(
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+          cluster_addr)
+      : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (given as a cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
+                                                 const CUtensorMap* tm,
+                                                 int32_t c0, int32_t c1,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1),
+      "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
+                                                uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(ncols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr,
+                                                  uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at this shared offset in both CTAs of the pair once
+// this thread's tcgen05 operations have completed.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ constexpr uint32_t idesc_pair_bf16_f32() {
+  return (1u << 4) | (1u << 7) | (1u << 10) |
+         (static_cast<uint32_t>(A_MN) << 15) |
+         (static_cast<uint32_t>(B_MN) << 16) |
+         (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>((2 * BM) >> 4) << 24);  // M = 256
+}
+
+struct SmemMap2 {
+  uint32_t a, b, bars;
+  __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const {
+    return bars + 8u * (STAGES2 + s);
+  }
+  __device__ __forceinline__ uint32_t tfull(int a_) const {
+    return bars + 8u * (2 * STAGES2 + a_);
+  }
+  __device__ __forceinline__ uint32_t tempty(int a_) const {
+    return bars + 8u * (2 * STAGES2 + 2 + a_);
+  }
+  __device__ __forceinline__ uint32_t drain() const {
+    return bars + 8u * (2 * STAGES2 + 4);
+  }
+};
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
+                                                   const CUtensorMap* tb,
+                                                   const GemmGeom& g,
+                                                   const SmemMap2& sm,
+                                                   uint32_t rank,
+                                                   const WaitCtx& ctx) {
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  uint32_t stage = 0, phase = 0, issued = 0;
+  bool ok = true;
+  for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+    const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
+    const int a0 = static_cast<int>(t.row0);  // this CTA's 128 rows of A
+    for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      // this CTA's 128 of the tile's 256 output columns
+      const int b0 = (t.n_first + tt) * BN + static_cast<int>(rank) * BM;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = mapa_shared(sm.full(stage), 0);
+        if (leader) mbar_arrive_expect_tx(sm.full(stage), 2 * STAGE2_BYTES);
+        const uint32_t sa = sm.a + stage * A2_STAGE_BYTES;
+        const uint32_t sb = sm.b + stage * B2_STAGE_BYTES;
+        const int k0 = kb * BK;
+        if (A_MN) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_2d_pair(sa + j * 64 * BK * 2, ta, a0 + 64 * j, k0, fb);
+        } else {
+          tma_load_2d_pair(sa, ta, k0, a0, fb);
+        }
+        if (B_MN) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_2d_pair(sb + j * 64 * BK * 2, tb, b0 + 64 * j, k0, fb);
+        } else {
+          tma_load_2d_pair(sb, tb, k0, b0, fb);
+        }
+        ++issued;
+        if (++stage == STAGES2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+  // Drain: the leader's full barriers count both CTAs' copies; once they
+  // have all completed no copy of either CTA is still in flight.
+  if (leader) {
+    for (int s = 0; s < STAGES2; ++s) {
+      const uint32_t cnt = issued / STAGES2 +
+                           (static_cast<uint32_t>(s) < issued % STAGES2 ? 1u : 0u);
+      if (cnt) mbar_wait(sm.full(s), (cnt - 1u) & 1u, ctx, false);
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void role_mma_pair(const GemmGeom& g,
+                                              const SmemMap2& sm,
+                                              uint32_t tmem_base,
+                                              const WaitCtx& ctx) {
+  constexpr uint32_t IDESC = idesc_pair_bf16_f32<A_MN, B_MN>();
+  constexpr uint32_t MN_LBO = 64 * BK * 2;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+    const Unit t = decode_unit(g, u, 2 * BM, 0);
+    for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      if (!mbar_wait(sm.tempty(acc), acc_phase ^ 1u, ctx, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * BN;
+      for (int kb = 0; kb < g.num_kb; ++kb) {
+        if (!mbar_wait(sm.full(stage), phase, ctx, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = sm.a + stage * A2_STAGE_BYTES;
+        const uint32_t sb = sm.b + stage * B2_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_LBO, 1024)
+                                   : sdesc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_LBO, 1024)
+                                   : sdesc_sw128(sb + k * 32, 16, 1024);
+          tc_mma_pair(d, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit_pair_both(sm.empty(stage));
+        if (++stage == STAGES2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit_pair_both(sm.tfull(acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_commit_pair_local(sm.drain());
+  mbar_wait(sm.drain(), 0, ctx, false);
+}
+
+template <class Epi>
+__device__ __forceinline__ void role_epilogue_pair(
+    const GemmGeom& g, const typename Epi::Params& p, const SmemMap2& sm,
+    uint32_t tmem_base, uint32_t rank, const WaitCtx& ctx, int warp,
+    int lane) {
+  const int q = warp & 3;
+  const int r = q * 32 + lane;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  uint32_t acc = 0, acc_phase = 0;
+  Epi epi;
+  for (int u = cluster; u < g.num_units; u += nclusters) {
+    const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
+    epi.begin_unit(p, g, t, r);
+    bool ok = true;
+    for (int tt = 0; tt < t.n_count; ++tt) {
+      const bool got = mbar_wait(sm.tfull(acc), acc_phase, ctx, true);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      epi.tile(p, g, t, t.n_first + tt, taddr, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(sm.tempty(acc), 0));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) return;
+    epi.end_unit(p, g, t, r);
+  }
+}
+
+template <class Epi, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap ta,
+                const __grid_constant__ CUtensorMap tb, const GemmGeom g,
+                const typename Epi::Params p, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  SmemMap2 sm;
+  sm.a = base;
+  sm.b = base + STAGES2 * A2_STAGE_BYTES;
+  sm.bars = base + STAGES2 * STAGE2_BYTES;
+  uint8_t* misc = smem_raw + (sm.bars - raw) + 8 * (2 * STAGES2 + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(sm.full(s), 1);
+      mbar_init(sm.empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(sm.tfull(a), 1);
+      mbar_init(sm.tempty(a), 8);  // 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(sm.drain(), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&ta);
+    tma_prefetch_desc(&tb);
+  }
+  // Both CTAs' barriers exist before either CTA signals the other's.
+  cluster_sync_all();
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx ctx{abort_flag, err, g.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) role_producer_pair<A_MN, B_MN>(&ta, &tb, g, sm, rank, ctx);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) role_mma_pair<A_MN, B_MN>(g, sm, tmem_base, ctx);
+    __syncwarp();
+  } else {
+    role_epilogue_pair<Epi>(g, p, sm, tmem_base, rank, ctx, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // Neither CTA frees its shared memory or tensor memory while the pair's
+  // MMAs or the peer's barrier traffic may still touch it.
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+constexpr int GEMM2_SMEM_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 256;
+
+template <class Epi, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb,
+                               const GemmGeom& g,
+                               const typename Epi::Params& p, unsigned* err,
+                               int grid, cudaStream_t s) {
+  auto kern = k_gemm_pair<Epi, A_MN, B_MN>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM2_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM2_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, g, p, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -3,7 +3,9 @@
 //    logit at the label ("Training Beyond 1M Tokens", section "The loss is
 //    the first thing to break": logits L x V, cross entropy against labels);
 //  - backward recompute of the same logits for one row chunk -> bf16
-//    softmax - onehot (the gradient of that cross entropy w.r.t. the logits).
+//    softmax - onehot (the gradient of that cross entropy w.r.t. the logits);
+//  - the fused forward+backward's logits of one row chunk -> the forward's
+//    statistics plus bf16 exponentials relative to each tile's maximum.
 #include "lce_device.cuh"
 
 namespace lce {
@@ -18,6 +20,32 @@ cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
                              const GemmGeom& g, const GradParams& p,
                              unsigned* err, int grid, cudaStream_t s) {
   return launch_gemm_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+cudaError_t launch_gemm_fused(const CUtensorMap& ta, const CUtensorMap& tb,
+                              const GemmGeom& g, const FusedParams& p,
+                              unsigned* err, int grid, cudaStream_t s) {
+  return launch_gemm_t<EpiFused, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+cudaError_t launch_gemm_pair_lse(const CUtensorMap& ta, const CUtensorMap& tb,
+                                 const GemmGeom& g, const LseParams& p,
+                                 unsigned* err, int grid, cudaStream_t s) {
+  return launch_gemm_pair_t<EpiLse, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+cudaError_t launch_gemm_pair_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                                  const GemmGeom& g, const GradParams& p,
+                                  unsigned* err, int grid, cudaStream_t s) {
+  return launch_gemm_pair_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s);
+}
+
+cudaError_t launch_gemm_pair_fused(const CUtensorMap& ta,
+                                   const CUtensorMap& tb, const GemmGeom& g,
+                                   const FusedParams& p, unsigned* err,
+                                   int grid, cudaStream_t s) {
+  return launch_gemm_pair_t<EpiFused, false, false>(ta, tb, g, p, err, grid,
+                                                    s);
 }
 
 }  // namespace lce

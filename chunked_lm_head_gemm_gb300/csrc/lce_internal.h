@@ -58,6 +58,21 @@ struct GradParams {
   int64_t ignore_index;
 };
 
+// Fused forward+backward, logits of one row chunk -> per-split online
+// (max, sum) partials and the label logit (as LseParams), plus each tile's
+// row maximum and the tile's exponentials e = 2^(u - tile max) in bf16,
+// which a later pass rescales into the gradient logits in place.
+struct FusedParams {
+  const int64_t* labels;  // [M], rows of this chunk
+  float* part_m;          // [splits][M]
+  float* part_s;          // [splits][M]
+  float* zy;              // [M]
+  uint16_t* E;            // [M][ldg] bf16 bits
+  int64_t ldg;
+  float* tile_max;        // [M][num_n], log2 units
+  int64_t ignore_index;
+};
+
 // Plain store of scale * acc (dH chunk, or the building-block test GEMM).
 struct StoreParams {
   void* out;              // [M][ldo]
@@ -65,7 +80,8 @@ struct StoreParams {
   int out_f32;            // 1: fp32 output, 0: bf16 output
   int accumulate;         // 1: out += scale*acc (fp32 only), 0: out = scale*acc
   const float* dloss;     // scale = dloss[0] / n_valid[0] (n_valid 0 -> 0);
-  const unsigned long long* n_valid;  // both NULL -> scale = 1
+  const unsigned long long* n_valid;  // dloss NULL counts as 1, n_valid
+                                      // NULL as 1: both NULL -> scale = 1
 };
 
 // ---- launch wrappers (defined in the kernel translation units) --------------
@@ -77,10 +93,35 @@ cudaError_t launch_gemm_lse(const CUtensorMap& ta, const CUtensorMap& tb,
 cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
                              const GemmGeom& g, const GradParams& p,
                              unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_fused(const CUtensorMap& ta, const CUtensorMap& tb,
+                              const GemmGeom& g, const FusedParams& p,
+                              unsigned* err, int grid, cudaStream_t s);
 cudaError_t launch_gemm_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const GemmGeom& g,
                               const StoreParams& p, unsigned* err, int grid,
                               cudaStream_t s);
+
+// The same four contractions on CTA pairs (cluster of 2, tcgen05
+// cta_group::2, 256 x 256 tiles): geometry in units of 256 rows, grid even,
+// K-major B boxes of 128 rows.
+cudaError_t launch_gemm_pair_lse(const CUtensorMap& ta, const CUtensorMap& tb,
+                                 const GemmGeom& g, const LseParams& p,
+                                 unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_pair_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                                  const GemmGeom& g, const GradParams& p,
+                                  unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_pair_fused(const CUtensorMap& ta,
+                                   const CUtensorMap& tb, const GemmGeom& g,
+                                   const FusedParams& p, unsigned* err,
+                                   int grid, cudaStream_t s);
+cudaError_t launch_gemm_pair_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
+                                   const CUtensorMap& tb, const GemmGeom& g,
+                                   const StoreParams& p, unsigned* err,
+                                   int grid, cudaStream_t s);
+
+// How many CTA pairs of the contraction kernels can be resident at once
+// (clusters are placed within a GPC, so this can be below SMs / 2).
+cudaError_t pair_max_active_clusters(int* n);
 
 // Small kernels.
 cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
@@ -97,6 +138,17 @@ cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
                                  const unsigned long long* n_valid,
                                  float* loss, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
+                               cudaStream_t s);
+// In place over one row chunk: E[i][j] = 2^(u - tile max) becomes
+// G = 2^(tile max - lse_i log2 e) E - [j == y_i] (bf16), 0 on ignored rows.
+cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
+                                 const float* tile_max, int64_t num_n,
+                                 const float* lse, const int64_t* labels,
+                                 int64_t rows, int64_t V, int64_t ignore_index,
+                                 cudaStream_t s);
+// dH *= dloss[0] (bf16 or fp32) and dW *= dloss[0], skipped when dloss is 1.
+cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
+                               int64_t n_dw, const float* dloss,
                                cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned* err, uint64_t timeout_ns,
                               cudaStream_t s);

@@ -1,5 +1,7 @@
 // The small kernels of the path: label count, log-sum-exp combine, loss
-// reduction, fp32 -> bf16 input conversion, and the bounded-wait probe.
+// reduction, fp32 -> bf16 input conversion, the fused path's in-place
+// exponentials -> gradient-logits pass and gradient scaling, and the
+// bounded-wait probe.
 #include "lce_device.cuh"
 
 namespace lce {
@@ -135,6 +137,112 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
   const int64_t want = (n + 255) / 256;
   const int grid = static_cast<int>(want < 4096 ? (want < 1 ? 1 : want) : 4096);
   k_f32_to_bf16<<<grid, 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+// In place over one row chunk of the fused forward+backward: E holds
+// e = 2^(u - m_t) (bf16), u = z log2 e, m_t the maximum of u over the
+// 256-column tile; with lse2 = lse log2 e the softmax is e 2^(m_t - lse2),
+// so G = e 2^(m_t - lse2) - [j == y] on rows that take part, 0 elsewhere.
+// One thread per 8 consecutive columns (a 16-byte vector; 8 divides the
+// 256-column tile, so a vector never straddles two tiles). Columns between
+// V and ldg are padding that nothing reads.
+__global__ void __launch_bounds__(256)
+    k_grad_from_exp(uint16_t* __restrict__ E, int64_t ldg,
+                    const float* __restrict__ tile_max, int64_t num_n,
+                    const float* __restrict__ lse,
+                    const int64_t* __restrict__ labels, int64_t rows,
+                    int64_t V, int64_t ignore_index) {
+  const int64_t nvec = (V + 7) / 8;
+  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const int64_t y = labels[row];
+    const bool valid = label_valid(y, V, ignore_index);
+    const float l2 = valid ? lse[row] * LOG2E : 0.f;
+    uint16_t* er = E + row * ldg;
+    const float* tm = tile_max + row * num_n;
+    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) +
+                     threadIdx.x;
+         v < nvec; v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t j0 = v * 8;
+      uint4* p4 = reinterpret_cast<uint4*>(er + j0);
+      if (!valid) {
+        *p4 = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const uint4 in = *p4;
+      const float sc = ex2(tm[j0 >> 8] - l2);
+      const int yo = static_cast<int>(y - j0);
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float lo = __uint_as_float(w[q] << 16) * sc;
+        float hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+        if (2 * q == yo) lo -= 1.f;
+        if (2 * q + 1 == yo) hi -= 1.f;
+        o[q] = pack_bf16x2(lo, hi);
+      }
+      *p4 = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
+                                 const float* tile_max, int64_t num_n,
+                                 const float* lse, const int64_t* labels,
+                                 int64_t rows, int64_t V, int64_t ignore_index,
+                                 cudaStream_t s) {
+  const int64_t nvec = (V + 7) / 8;
+  const int64_t gx = (nvec + 255) / 256;
+  dim3 grid(static_cast<unsigned>(gx < 1 ? 1 : gx),
+            static_cast<unsigned>(rows < 65535 ? rows : 65535));
+  k_grad_from_exp<<<grid, 256, 0, s>>>(E, ldg, tile_max, num_n, lse, labels,
+                                       rows, V, ignore_index);
+  return cudaGetLastError();
+}
+
+// dH *= d and dW *= d with d = dloss[0]; nothing to do when d == 1.
+// n_dh is a multiple of 8 (bf16) or 4 (fp32), n_dw a multiple of 4 (H is a
+// multiple of 8), so every access is a 16-byte vector.
+__global__ void k_scale_grads(void* __restrict__ dH, int dh_f32, int64_t n_dh,
+                              float* __restrict__ dW, int64_t n_dw,
+                              const float* __restrict__ dloss) {
+  const float d = *dloss;
+  if (d == 1.f) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (dh_f32) {
+    float4* p = static_cast<float4*>(dH);
+    for (int64_t i = t0; i < n_dh / 4; i += stride) {
+      float4 x = p[i];
+      x.x *= d; x.y *= d; x.z *= d; x.w *= d;
+      p[i] = x;
+    }
+  } else {
+    uint4* p = static_cast<uint4*>(dH);
+    for (int64_t i = t0; i < n_dh / 8; i += stride) {
+      const uint4 x = p[i];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        o[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * d,
+                           __uint_as_float(w[q] & 0xFFFF0000u) * d);
+      p[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  float4* q4 = reinterpret_cast<float4*>(dW);
+  for (int64_t i = t0; i < n_dw / 4; i += stride) {
+    float4 x = q4[i];
+    x.x *= d; x.y *= d; x.z *= d; x.w *= d;
+    q4[i] = x;
+  }
+}
+
+cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
+                               int64_t n_dw, const float* dloss,
+                               cudaStream_t s) {
+  k_scale_grads<<<1024, 256, 0, s>>>(dH, dh_f32, n_dh, dW, n_dw, dloss);
   return cudaGetLastError();
 }
 

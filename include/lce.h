@@ -124,6 +124,41 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
                         float* dW, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Forward and backward in one call, without recomputing the logits: for
+ * each row chunk, one tensor-core kernel computes the chunk's logits once
+ * and writes, besides the forward's per-row statistics, each 256-column
+ * tile's row maximum and the bf16 exponentials relative to it into the
+ * workspace; once the chunk's lse is known, a memory-bound pass turns them
+ * in place into softmax - onehot, which feeds the same dH and dW
+ * contractions as lce_backward. Executes 6 L H V flops instead of the
+ * 8 L H V of lce_forward + lce_backward, for about 6 bytes of extra HBM
+ * traffic per logit. Not on the pages, which describe only the forward's
+ * chunking ("Training Beyond 1M Tokens", section "The massive logits
+ * matrix: chunk it").
+ *   Arguments as lce_forward and lce_backward; loss, lse, dH and dW are all
+ *   outputs, the gradients being those of the loss itself (dloss = 1).
+ *   Scale them afterwards with lce_scale_gradients for another dloss.
+ * The softmax is rounded to bf16 as exp(z - tile max) before being
+ * rescaled, so G differs from lce_backward's by bf16 rounding only.
+ */
+lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
+                                const int64_t* labels, int64_t L, int64_t H,
+                                int64_t V, int64_t ignore_index,
+                                int64_t chunk_rows, float* loss, float* lse,
+                                void* dH, float* dW, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * dH *= dloss[0] and dW *= dloss[0] in place (dH of dtype dt, [L][H]; dW
+ * fp32 [V][H]; dloss a device float). Nothing is done when dloss[0] is
+ * exactly 1. For gradients from lce_forward_backward under another upstream
+ * gradient; bf16 dH is rounded again after the multiply.
+ */
+lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
+                               float* dW, int64_t V, const float* dloss,
+                               void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device. Returns LCE_ERR_TIMEOUT or LCE_ERR_LABEL_RANGE if a kernel
  * raised one since the last call (timeout first), LCE_ERR_CUDA if the
@@ -186,6 +221,18 @@ lce_status lce_forward_static(const void* h, const void* W,
                               float* lse, void* stream);
 
 /*
+ * Selects how the tensor-core contractions run, for the whole process:
+ * enable = 1: on CTA pairs (a cluster of two SMs issues tcgen05.mma with
+ * cta_group::2 on 256 x 256 tiles, each SM staging half of each operand);
+ * enable = 0: one CTA per 128 x 256 tile. Both give the same results up to
+ * fp32 summation order. The environment variable LCE_CTA_PAIR=0/1 sets the
+ * initial choice. lce_get_cta_pair returns the current one. No counterpart
+ * on the pages. Returns LCE_ERR_INVALID_ARG for other values.
+ */
+lce_status lce_set_cta_pair(int enable);
+int lce_get_cta_pair(void);
+
+/*
  * Per-kernel timing of this library's own launches, for benchmarks. No
  * counterpart on the pages. Between lce_profile_start() and
  * lce_profile_stop(), every kernel the calling thread launches through this
@@ -196,7 +243,7 @@ lce_status lce_forward_static(const void* h, const void* W,
  * per tensor-core contraction, 0 for the other kernels). Host-side state
  * only; events are created on first use and reused.
  */
-#define LCE_KERNEL_KINDS 10
+#define LCE_KERNEL_KINDS 13
 enum {
   LCE_K_COUNT_VALID = 0,
   LCE_K_GEMM_LSE = 1,
@@ -207,7 +254,10 @@ enum {
   LCE_K_GEMM_DH = 6,
   LCE_K_GEMM_DW = 7,
   LCE_K_TEST_GEMM = 8,
-  LCE_K_WAIT_PROBE = 9
+  LCE_K_WAIT_PROBE = 9,
+  LCE_K_GEMM_FUSED = 10,
+  LCE_K_GRAD_FROM_EXP = 11,
+  LCE_K_SCALE_GRADS = 12
 };
 
 typedef struct {

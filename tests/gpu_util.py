@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import os
+
 LOSS_RTOL = 1e-3
 GRAD_RFRO = 1e-2
 LSE_ATOL = 2e-3
@@ -36,12 +38,51 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().double().numpy()
 
 
-def run_gpu(h, W, y, dloss=1.0, chunk_rows=0, ignore_index=-100):
-    """Forward + backward through the library; returns host float64 arrays."""
+MODES = ["separate", "fused"]
+# contraction variants under test: single CTAs always; CTA pairs
+# (tcgen05 cta_group::2) when LCE_TEST_PAIR=1
+PAIRS = [False, True] if os.environ.get("LCE_TEST_PAIR") == "1" else [False]
+
+
+class cta_pair:
+    """Context: run the library's contractions on CTA pairs or single CTAs
+    (None leaves the process setting alone)."""
+
+    def __init__(self, pair):
+        self.pair = pair
+
+    def __enter__(self):
+        from chunked_lm_head_gemm_gb300 import _binding as B
+        self.before = B.get_cta_pair()
+        if self.pair is not None:
+            B.set_cta_pair(self.pair)
+
+    def __exit__(self, *exc):
+        from chunked_lm_head_gemm_gb300 import _binding as B
+        B.set_cta_pair(self.before)
+
+
+def run_gpu(h, W, y, dloss=1.0, chunk_rows=0, ignore_index=-100,
+            mode="separate", pair=None):
+    """Forward + backward through the library; returns host float64 arrays.
+
+    mode "separate": lce_forward then lce_backward (logits recomputed);
+    mode "fused": lce_forward_backward, then lce_scale_gradients by dloss.
+    pair: True/False selects CTA-pair or single-CTA contractions."""
+    with cta_pair(pair):
+        return _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode)
+
+
+def _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode):
     import chunked_lm_head_gemm_gb300 as lce
-    loss, lse = lce.forward(h, W, y, ignore_index)
     d = torch.full((), float(dloss), device=h.device)
-    dH, dW = lce.backward(h, W, y, lse, d, ignore_index, chunk_rows)
+    if mode == "fused":
+        loss, lse, dH, dW = lce.forward_backward(h, W, y, ignore_index,
+                                                 chunk_rows)
+        lce.scale_gradients(dH, dW, d)
+    else:
+        loss, lse = lce.forward(h, W, y, ignore_index)
+        dH, dW = lce.backward(h, W, y, lse, d, ignore_index, chunk_rows)
     status = lce.get_error()
     return dict(loss=float(loss.item()), lse=to64(lse), dH=to64(dH),
                 dW=to64(dW), status=status)

@@ -56,8 +56,11 @@ def test_workspace_size(lib):
     c = lib.lce_default_chunk_rows(L, H, V)
     assert c % 128 == 0 and 0 < c <= L
     assert f(L, H, V, 0, 0) >= c * V * 2
-    # plus the forward statistics: 16 splits x (max, sum) + the label logit
-    assert f(L, H, V, 0, 0) < c * V * 2 + (16 * 8 + 4 + 1) * L + (1 << 20)
+    # plus the forward statistics (16 splits x (max, sum) + the label logit)
+    # and the fused path's per-tile row maxima (chunk x ceil(V/256) floats)
+    tiles = -(-V // 256)
+    assert f(L, H, V, 0, 0) < (c * V * 2 + (16 * 8 + 4 + 1) * L +
+                               4 * c * tiles + (1 << 20))
     # peak extra memory is O(chunk * V), far below the L x V fp32 logits
     assert f(L, H, V, 0, 0) < L * V * 4 / 8
 
@@ -91,6 +94,12 @@ def test_bad_arguments_return_before_any_device_call(lib):
     assert lib.lce_test_gemm(null, p, p, 8, 8, 8, 0, 0, null) == 1
     assert lib.lce_test_gemm(p, p, p, 8, 12, 8, 0, 0, null) == 1
     assert lib.lce_test_wait_timeout(0, null) == 1
+    # the contraction variant switch is host state only
+    assert lib.lce_set_cta_pair(2) == 1
+    before = lib.lce_get_cta_pair()
+    assert lib.lce_set_cta_pair(1) == 0 and lib.lce_get_cta_pair() == 1
+    assert lib.lce_set_cta_pair(0) == 0 and lib.lce_get_cta_pair() == 0
+    assert lib.lce_set_cta_pair(before) == 0
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):

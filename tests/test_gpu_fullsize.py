@@ -74,3 +74,19 @@ def test_full_size(name):
     dH3, dW3 = lce.backward(h, W, y, lse, dloss, chunk_rows=4096)
     assert torch.equal(dH, dH3)
     assert rel_fro(to64(dW3), to64(dW)) < 1e-4
+    del dH3, dW3
+
+    # the fused forward+backward (no recompute): same loss and lse up to
+    # fp32 rounding, gradients within the parity bound of the separate path
+    # and of the oracle's sampled rows
+    loss4, lse4, dH4, dW4 = lce.forward_backward(h, W, y, workspace=ws)
+    assert lce.get_error() == 0
+    assert abs(loss4.item() - loss.item()) <= 1e-5 * abs(loss.item())
+    assert torch.max((lse4 - lse).abs()).item() <= 1e-4
+    assert rel_fro(to64(dH4), to64(dH)) <= GRAD_RFRO
+    assert rel_fro(to64(dW4), to64(dW)) <= GRAD_RFRO
+    e = rel_fro(to64(dH4[torch.from_numpy(rows).to(dev)]), r["dH"])
+    assert e <= GRAD_RFRO, f"fused: sampled dH rows rel Frobenius err {e}"
+    loss5, _, dH5, dW5 = lce.forward_backward(h, W, y, workspace=ws)
+    assert torch.equal(loss4, loss5) and torch.equal(dH4, dH5) and \
+        torch.equal(dW4, dW5)

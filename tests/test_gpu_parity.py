@@ -8,7 +8,8 @@ import torch
 import oracle
 from chunked_lm_head_gemm_gb300.inputs import (WORKLOADS, Workload,
                                                make_inputs)
-from tests.gpu_util import assert_parity, rel_fro, require_gpu, run_gpu
+from tests.gpu_util import (MODES, PAIRS, assert_parity, rel_fro,
+                            require_gpu, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -20,11 +21,13 @@ def _oracle(h, W, y, dloss=1.0, vrows=None):
     return f, b
 
 
-def test_tiny_workload():
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_workload(mode, pair):
     """512 x 256 x 4096, fp32 inputs, 10% ignored."""
     dev = require_gpu()
     h, W, y = make_inputs("tiny", seed=0, device=dev)
-    gpu = run_gpu(h, W, y)
+    gpu = run_gpu(h, W, y, mode=mode, pair=pair)
     assert gpu["status"] == 0
     f, b = _oracle(h, W, y)
     assert_parity(gpu, f, b)
@@ -43,36 +46,40 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name,L,H,V,dt,chunk,ign,wstd", EDGE,
                          ids=[e[0] for e in EDGE])
-def test_edge_shapes(name, L, H, V, dt, chunk, ign, wstd):
+def test_edge_shapes(name, L, H, V, dt, chunk, ign, wstd, mode, pair):
     dev = require_gpu()
     wl = Workload(name, L, H, V, dt, 1.0, wstd, "uniform", ignore_frac=ign)
     h, W, y = make_inputs(wl, seed=1, device=dev)
-    gpu = run_gpu(h, W, y, dloss=1.0, chunk_rows=chunk)
+    gpu = run_gpu(h, W, y, dloss=1.0, chunk_rows=chunk, mode=mode, pair=pair)
     assert gpu["status"] == 0
     f, b = _oracle(h, W, y)
     assert_parity(gpu, f, b)
 
 
-def test_single_class_gives_zero():
+@pytest.mark.parametrize("mode", MODES)
+def test_single_class_gives_zero(mode):
     """V = 1: every lse equals the one logit; loss and gradients vanish."""
     dev = require_gpu()
     wl = Workload("v1", 70, 16, 1, "bf16", 1.0, 0.5, "uniform")
     h, W, y = make_inputs(wl, seed=2, device=dev)
-    gpu = run_gpu(h, W, y)
+    gpu = run_gpu(h, W, y, mode=mode)
     z = (h.double() @ W.double().T)[:, 0].cpu().numpy()
     assert np.max(np.abs(gpu["lse"] - z)) < 1e-4 * max(1.0, np.max(np.abs(z)))
     assert abs(gpu["loss"]) < 1e-5
     assert np.max(np.abs(gpu["dH"])) < 1e-6 and np.max(np.abs(gpu["dW"])) < 1e-6
 
 
-def test_all_rows_ignored():
+@pytest.mark.parametrize("mode", MODES)
+def test_all_rows_ignored(mode):
     dev = require_gpu()
     wl = Workload("allign", 150, 32, 400, "bf16", 1.0, 0.1, "uniform")
     h, W, y = make_inputs(wl, seed=3, device=dev)
     y[:] = -100
-    gpu = run_gpu(h, W, y)
+    gpu = run_gpu(h, W, y, mode=mode)
     assert gpu["status"] == 0
     assert gpu["loss"] == 0.0
     assert np.all(gpu["dH"] == 0.0) and np.all(gpu["dW"] == 0.0)
@@ -80,7 +87,8 @@ def test_all_rows_ignored():
     assert np.max(np.abs(gpu["lse"] - f["lse"])) < 2e-3
 
 
-def test_labels_out_of_range_are_reported_and_ignored():
+@pytest.mark.parametrize("mode", MODES)
+def test_labels_out_of_range_are_reported_and_ignored(mode):
     dev = require_gpu()
     wl = Workload("bad", 260, 32, 500, "bf16", 1.0, 0.1, "uniform",
                   ignore_frac=0.1)
@@ -88,7 +96,7 @@ def test_labels_out_of_range_are_reported_and_ignored():
     y[3] = 500
     y[77] = -7
     y[200] = 10 ** 12
-    gpu = run_gpu(h, W, y)
+    gpu = run_gpu(h, W, y, mode=mode)
     import chunked_lm_head_gemm_gb300._binding as B
     assert gpu["status"] == B.LCE_ERR_LABEL_RANGE
     f, b = _oracle(h, W, y)
@@ -97,13 +105,14 @@ def test_labels_out_of_range_are_reported_and_ignored():
     assert B.get_error() == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("dloss", [0.0, 2.5, -0.75])
-def test_dloss_scaling(dloss):
+def test_dloss_scaling(dloss, mode):
     dev = require_gpu()
     wl = Workload("dl", 200, 64, 700, "bf16", 1.0, 0.1, "uniform",
                   ignore_frac=0.1)
     h, W, y = make_inputs(wl, seed=5, device=dev)
-    gpu = run_gpu(h, W, y, dloss=dloss)
+    gpu = run_gpu(h, W, y, dloss=dloss, mode=mode)
     if dloss == 0.0:
         assert np.all(gpu["dH"] == 0.0) and np.all(gpu["dW"] == 0.0)
         return
@@ -111,7 +120,8 @@ def test_dloss_scaling(dloss):
     assert_parity(gpu, f, b)
 
 
-def test_autograd_function_matches_explicit_calls():
+@pytest.mark.parametrize("mode", MODES)
+def test_autograd_function_matches_explicit_calls(mode):
     dev = require_gpu()
     import chunked_lm_head_gemm_gb300 as lce
     wl = Workload("ag", 300, 64, 900, "bf16", 1.0, 0.1, "uniform",
@@ -119,9 +129,9 @@ def test_autograd_function_matches_explicit_calls():
     h, W, y = make_inputs(wl, seed=6, device=dev)
     hh = h.clone().requires_grad_(True)
     WW = W.clone().requires_grad_(True)
-    loss = lce.linear_cross_entropy(hh, WW, y)
+    loss = lce.linear_cross_entropy(hh, WW, y, fused=(mode == "fused"))
     (3.0 * loss).backward()
-    gpu = run_gpu(h, W, y, dloss=3.0)
+    gpu = run_gpu(h, W, y, dloss=3.0, mode=mode)
     assert loss.item() == gpu["loss"]
     assert torch.equal(hh.grad.float().cpu(),
                        torch.from_numpy(gpu["dH"]).float())
@@ -132,15 +142,17 @@ SLICES = [("qwen3-0.6b", 256), ("qwen3-4b", 300), ("qwen3-8b", 256),
           ("qwen3-32b", 256)]
 
 
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name,rows", SLICES, ids=[s[0] for s in SLICES])
-def test_row_slice_of_head_shape(name, rows):
+def test_row_slice_of_head_shape(name, rows, mode, pair):
     """The first rows of each head shape (full H and V = 151936); dW is
     compared on the vocabulary rows the slice's labels touch, plus 256
     seeded others and the last id."""
     dev = require_gpu()
     wl = WORKLOADS[name].with_rows(rows)
     h, W, y = make_inputs(wl, seed=0, device=dev)
-    gpu = run_gpu(h, W, y, dloss=1.0)
+    gpu = run_gpu(h, W, y, dloss=1.0, mode=mode, pair=pair)
     assert gpu["status"] == 0
     yc = y.cpu().numpy()
     rs = np.random.default_rng(7)
