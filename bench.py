@@ -429,52 +429,123 @@ def main():
     gpu_launches = int(sum(v[0] for v in stats.values()))
 
     # ---- end to end: pinned host in, results out, inside the timed region --
+    # Every step copies its inputs (h, W, labels) from pinned host memory and
+    # reads its results (loss, dH, dW) back into pinned host memory. Two
+    # device buffer sets and two copy streams let step i+1's inputs arrive
+    # and step i-1's results leave while step i computes ("pipelined");
+    # "sequential_value" is the same loop with every copy on the compute
+    # stream.
     e2e = None
     if not args.no_e2e:
-        h_host = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
-        W_host = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
-        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        pin = dict(pin_memory=True)
+        h_host = torch.empty(h.shape, dtype=h.dtype, **pin)
+        W_host = torch.empty(W.shape, dtype=W.dtype, **pin)
+        y_host = torch.empty(y.shape, dtype=y.dtype, **pin)
         h_host.copy_(h)
         W_host.copy_(W)
         y_host.copy_(y)
-        loss_host = torch.empty((), dtype=torch.float32, pin_memory=True)
-        dH_host = torch.empty(dH.shape, dtype=dH.dtype, pin_memory=True)
-        dW_host = torch.empty(dW.shape, dtype=dW.dtype, pin_memory=True)
+        loss_host = torch.empty((), dtype=torch.float32, **pin)
+        dH_host = torch.empty(dH.shape, dtype=dH.dtype, **pin)
+        dW_host = torch.empty(dW.shape, dtype=dW.dtype, **pin)
+        bufs = [dict(h=h, W=W, y=y, loss=loss, lse=lse, dH=dH, dW=dW),
+                dict(h=torch.empty_like(h), W=torch.empty_like(W),
+                     y=torch.empty_like(y), loss=torch.empty_like(loss),
+                     lse=torch.empty_like(lse), dH=torch.empty_like(dH),
+                     dW=torch.empty_like(dW))]
 
-        def e2e_step():
-            h.copy_(h_host, non_blocking=True)
-            W.copy_(W_host, non_blocking=True)
-            y.copy_(y_host, non_blocking=True)
-            step()
-            loss_host.copy_(loss, non_blocking=True)
-            dH_host.copy_(dH, non_blocking=True)
-            dW_host.copy_(dW, non_blocking=True)
+        def compute(b):
+            if args.mode == "fused":
+                lce.forward_backward(b["h"], b["W"], b["y"], chunk_rows=chunk,
+                                     workspace=ws, loss_out=b["loss"],
+                                     lse_out=b["lse"], dH_out=b["dH"],
+                                     dW_out=b["dW"])
+                lce.scale_gradients(b["dH"], b["dW"], dloss)
+            else:
+                lce.forward(b["h"], b["W"], b["y"], workspace=ws,
+                            loss_out=b["loss"], lse_out=b["lse"])
+                lce.backward(b["h"], b["W"], b["y"], b["lse"], dloss,
+                             chunk_rows=chunk, workspace=ws, dH_out=b["dH"],
+                             dW_out=b["dW"])
 
-        e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        wall0 = time.perf_counter()
-        e0.record()
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-        te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64,
-                          device=dev)
-        if dist is not None:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        assert torch.isfinite(loss_host).item()
-        e2e = {"value": tokens / (te.item() / 1e3), "unit": "tokens/s",
+        def copy_in(b):
+            b["h"].copy_(h_host, non_blocking=True)
+            b["W"].copy_(W_host, non_blocking=True)
+            b["y"].copy_(y_host, non_blocking=True)
+
+        def copy_out(b):
+            loss_host.copy_(b["loss"], non_blocking=True)
+            dH_host.copy_(b["dH"], non_blocking=True)
+            dW_host.copy_(b["dW"], non_blocking=True)
+
+        def run_sequential(nsteps):
+            for _ in range(nsteps):
+                copy_in(bufs[0])
+                compute(bufs[0])
+                copy_out(bufs[0])
+
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+        comp = torch.cuda.current_stream(dev)
+
+        def run_pipelined(nsteps):
+            ev_in = [torch.cuda.Event() for _ in range(nsteps)]
+            ev_done = [torch.cuda.Event() for _ in range(nsteps)]
+            ev_out = [torch.cuda.Event() for _ in range(nsteps)]
+            start = torch.cuda.Event()
+            start.record(comp)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            for i in range(nsteps):
+                b = bufs[i % 2]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:  # step i-2 has finished reading this set
+                        s_in.wait_event(ev_done[i - 2])
+                    copy_in(b)
+                    ev_in[i].record(s_in)
+                comp.wait_event(ev_in[i])
+                if i >= 2:  # step i-2's results have left this set
+                    comp.wait_event(ev_out[i - 2])
+                compute(b)
+                ev_done[i].record(comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[i])
+                    copy_out(b)
+                    ev_out[i].record(s_out)
+            comp.wait_event(ev_out[nsteps - 1])
+
+        def time_e2e(fn):
+            fn(1)
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            wall0 = time.perf_counter()
+            e0.record()
+            fn(args.steps)
+            e1.record()
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - wall0
+            te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64,
+                              device=dev)
+            if dist is not None:
+                dist.all_reduce(te, op=dist.ReduceOp.MAX)
+            assert torch.isfinite(loss_host).item()
+            return tokens / (te.item() / 1e3), wall
+
+        seq_value, seq_wall = time_e2e(run_sequential)
+        pipe_value, pipe_wall = time_e2e(run_pipelined)
+        st = lce.get_error()
+        if st != 0:
+            raise RuntimeError(f"device error status {st} in the e2e loop")
+        e2e = {"value": pipe_value, "unit": "tokens/s",
                "h2d_bytes_per_step": int(h_host.nbytes + W_host.nbytes +
                                          y_host.nbytes),
                "d2h_bytes_per_step": int(loss_host.nbytes + dH_host.nbytes +
                                          dW_host.nbytes),
-               "wall_s": wall}
-        del h_host, W_host, dH_host, dW_host
+               "pipelined": True, "wall_s": pipe_wall,
+               "sequential_value": seq_value, "sequential_wall_s": seq_wall}
+        del h_host, W_host, dH_host, dW_host, bufs
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

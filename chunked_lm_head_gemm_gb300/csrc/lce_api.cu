@@ -131,7 +131,7 @@ lce_status device_info(DeviceInfo** out) {
 // Contractions on single CTAs (128 x 256 tiles) or on CTA pairs
 // (256 x 256 tiles, tcgen05 cta_group::2). LCE_CTA_PAIR=0/1 in the
 // environment or lce_set_cta_pair() choose; the default is kDefaultPair.
-constexpr int kDefaultPair = 0;
+constexpr int kDefaultPair = 1;
 std::atomic<int> g_pair_mode{-1};
 
 bool use_pair() {

@@ -11,8 +11,6 @@ import numpy as np
 import pytest
 import torch
 
-import os
-
 LOSS_RTOL = 1e-3
 GRAD_RFRO = 1e-2
 LSE_ATOL = 2e-3
@@ -39,9 +37,9 @@ def to64(t: torch.Tensor) -> np.ndarray:
 
 
 MODES = ["separate", "fused"]
-# contraction variants under test: single CTAs always; CTA pairs
-# (tcgen05 cta_group::2) when LCE_TEST_PAIR=1
-PAIRS = [False, True] if os.environ.get("LCE_TEST_PAIR") == "1" else [False]
+# contraction variants under test: single CTAs (128 x 256 tiles) and CTA
+# pairs (tcgen05 cta_group::2, 256 x 256 tiles; the library's default)
+PAIRS = [False, True]
 
 
 class cta_pair:
