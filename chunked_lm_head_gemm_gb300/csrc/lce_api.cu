@@ -10,6 +10,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include "../../include/lce.h"
@@ -219,6 +220,59 @@ lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
   return make_tmap(tm, base, mn_extent, k_rows, row_elems * 2, 64, BK);
 }
 
+// ---- tuning of the contractions' memory behaviour -----------------------
+// Per contraction kind: the L2 eviction priority of each operand's loads and
+// the tile grouping of tile-per-unit contractions; plus the L2 budget that
+// bounds the live A row panels when choosing column splits. Defaults are the
+// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,l2mb=M" (kinds lse,
+// grad, fused, dH, dW, test; H in 0..2; G >= 0) overrides them.
+enum TuneKind { T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_KINDS };
+struct Tune {
+  int a_hint[T_KINDS];
+  int b_hint[T_KINDS];
+  int group_n[T_KINDS];
+  double l2_budget;
+};
+
+const Tune& tune() {
+  static Tune t = [] {
+    Tune v{};
+    v.l2_budget = 48e6;
+    const char* env = std::getenv("LCE_TUNE");
+    if (!env) return v;
+    static const char* names[T_KINDS] = {"lse", "grad", "fused", "dH", "dW",
+                                         "test"};
+    std::string spec(env);
+    size_t pos = 0;
+    while (pos < spec.size()) {
+      size_t end = spec.find(',', pos);
+      if (end == std::string::npos) end = spec.size();
+      const std::string item = spec.substr(pos, end - pos);
+      pos = end + 1;
+      const size_t eq = item.find('=');
+      if (eq == std::string::npos) continue;
+      const std::string key = item.substr(0, eq);
+      const double val = std::atof(item.c_str() + eq + 1);
+      if (key == "l2mb") {
+        if (val > 0) v.l2_budget = val * 1e6;
+        continue;
+      }
+      const size_t dot = key.find('.');
+      if (dot == std::string::npos) continue;
+      const std::string kind = key.substr(0, dot), field = key.substr(dot + 1);
+      for (int k = 0; k < T_KINDS; ++k) {
+        if (kind != names[k]) continue;
+        const int iv = static_cast<int>(val);
+        if (field == "a" && iv >= 0 && iv <= 2) v.a_hint[k] = iv;
+        if (field == "b" && iv >= 0 && iv <= 2) v.b_hint[k] = iv;
+        if (field == "g" && iv >= 0) v.group_n[k] = iv;
+      }
+    }
+    return v;
+  }();
+  return t;
+}
+
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
@@ -230,7 +284,7 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 void choose_splits(int num_m, int num_n, int nsm, int64_t K, int* splits,
                    int* tps, int rows_per_unit = BM) {
   const double panel = static_cast<double>(rows_per_unit) * K * 2.0;
-  int s_min = static_cast<int>(std::ceil(nsm * panel / 48e6));
+  int s_min = static_cast<int>(std::ceil(nsm * panel / tune().l2_budget));
   const int s_max = std::max(1, std::min(kMaxSplits, num_n));
   s_min = std::max(1, std::min(s_min, s_max));
   const double work = static_cast<double>(num_m) * num_n;
@@ -268,6 +322,8 @@ GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps,
   g.tiles_per_split = tps;
   g.num_units = g.num_m * splits;
   g.timeout_ns = wait_timeout_ns();
+  g.group_n = 0;
+  g.a_hint = g.b_hint = 0;
   return g;
 }
 
@@ -285,6 +341,7 @@ struct GemmOperands {
   const void* b;
   int64_t b_ld;
   bool sweep;          // sweep all column tiles per row block (choose splits)
+  int kind;            // TuneKind
 };
 
 struct GemmPlan {
@@ -304,6 +361,10 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   int splits = num_n, tps = 1;
   if (o.sweep) choose_splits(num_m, num_n, slots, o.K, &splits, &tps, rows_unit);
   pl->g = make_geom(o.M, o.N, o.K, splits, tps, rows_unit);
+  const Tune& tn = tune();
+  pl->g.a_hint = tn.a_hint[o.kind];
+  pl->g.b_hint = tn.b_hint[o.kind];
+  if (!o.sweep) pl->g.group_n = tn.group_n[o.kind];
   lce_status st = o.a_mn ? tmap_mnmajor(&pl->ta, o.a, o.M, o.K, o.a_ld)
                          : tmap_kmajor(&pl->ta, o.a, o.K, o.M, o.a_ld, BM);
   if (st != LCE_OK) return st;
@@ -517,7 +578,7 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
 
   // logits = h W^T: M = L rows, N = V columns, K = H
   GemmPlan pl;
-  if ((st = plan_gemm({L, V, H, false, false, hb, H, Wb, H, true}, *dev,
+  if ((st = plan_gemm({L, V, H, false, false, hb, H, Wb, H, true, T_LSE}, *dev,
                       &pl)) != LCE_OK)
     return st;
   const GemmGeom& g = pl.g;
@@ -596,8 +657,8 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
     // (1) recompute z_c = h_c W^T and write G_c = softmax - onehot (bf16)
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true}, *dev,
-                          &pl)) != LCE_OK)
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true, T_GRAD},
+                          *dev, &pl)) != LCE_OK)
         return st;
       GradParams p{};
       p.labels = labels + c0;
@@ -613,7 +674,7 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
     // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false},
+      if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false, T_DH},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -631,7 +692,7 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
     // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
     {
       GemmPlan pl;
-      if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false},
+      if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false, T_DW},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -702,8 +763,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
     int splits = 1;
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true}, *dev,
-                          &pl)) != LCE_OK)
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true, T_FUSED},
+                          *dev, &pl)) != LCE_OK)
         return st;
       splits = pl.g.splits;
       FusedParams p{};
@@ -742,7 +803,7 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
     // (4) dH_c = G_c W / N
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false},
+      if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false, T_DH},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -760,7 +821,7 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
     // (5) dW (+)= G_c^T h_c / N
     {
       GemmPlan pl;
-      if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false},
+      if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false, T_DW},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -856,7 +917,7 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
   if (st != LCE_OK) return st;
   GemmPlan pl;
   if ((st = plan_gemm({M, N, K, a_mn != 0, b_mn != 0, A, a_mn ? M : K, B,
-                       b_mn ? N : K, false},
+                       b_mn ? N : K, false, T_TEST},
                       *dev, &pl)) != LCE_OK)
     return st;
   StoreParams p{};

@@ -121,6 +121,43 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// L2 eviction-priority policies for the hinted loads below.
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p = 0;
+  if (hint == 1)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+                 : "=l"(p));
+  else if (hint == 2)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
+                 : "=l"(p));
+  return p;
+}
+
+// As tma_load_2d, with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
+                                                 const CUtensorMap* tm,
+                                                 int32_t c0, int32_t c1,
+                                                 uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+
+// One operand box: hinted when the contraction asks for it.
+__device__ __forceinline__ void tma_load_op(uint32_t dst, const CUtensorMap* tm,
+                                            int32_t c0, int32_t c1,
+                                            uint32_t bar, int hint,
+                                            uint64_t policy) {
+  if (hint)
+    tma_load_2d_hint(dst, tm, c0, c1, bar, policy);
+  else
+    tma_load_2d(dst, tm, c0, c1, bar);
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 / tensor memory
 // ---------------------------------------------------------------------------
@@ -259,10 +296,24 @@ __device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u,
                                             int rows_per_unit = BM,
                                             int rank = 0) {
   Unit t;
-  t.m_blk = u / g.splits;
-  t.split = u - t.m_blk * g.splits;
-  t.n_first = t.split * g.tiles_per_split;
-  t.n_count = min(g.tiles_per_split, g.num_n - t.n_first);
+  if (g.group_n > 0 && g.tiles_per_split == 1) {
+    // groups of group_n column tiles; within a group, row blocks vary
+    // slowest so consecutive units share a row panel
+    const int per_group = g.num_m * g.group_n;
+    const int grp = u / per_group;
+    const int r = u - grp * per_group;
+    const int n0 = grp * g.group_n;
+    const int width = min(g.group_n, g.num_n - n0);
+    t.m_blk = r / width;
+    t.split = n0 + (r - t.m_blk * width);
+    t.n_first = t.split;
+    t.n_count = 1;
+  } else {
+    t.m_blk = u / g.splits;
+    t.split = u - t.m_blk * g.splits;
+    t.n_first = t.split * g.tiles_per_split;
+    t.n_count = min(g.tiles_per_split, g.num_n - t.n_first);
+  }
   t.row0 = static_cast<int64_t>(t.m_blk) * rows_per_unit +
            static_cast<int64_t>(rank) * BM;
   return t;
@@ -614,6 +665,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
                                               const SmemMap& sm,
                                               const WaitCtx& ctx) {
   uint32_t stage = 0, phase = 0, issued = 0;
+  const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
   for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
@@ -633,16 +685,18 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
         if (A_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_2d(sa + j * 64 * BK * 2, ta, m0 + 64 * j, k0, fb);
+            tma_load_op(sa + j * 64 * BK * 2, ta, m0 + 64 * j, k0, fb,
+                        g.a_hint, pa);
         } else {
-          tma_load_2d(sa, ta, k0, m0, fb);
+          tma_load_op(sa, ta, k0, m0, fb, g.a_hint, pa);
         }
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(sb + j * 64 * BK * 2, tb, n0 + 64 * j, k0, fb);
+            tma_load_op(sb + j * 64 * BK * 2, tb, n0 + 64 * j, k0, fb,
+                        g.b_hint, pb);
         } else {
-          tma_load_2d(sb, tb, k0, n0, fb);
+          tma_load_op(sb, tb, k0, n0, fb, g.b_hint, pb);
         }
         ++issued;
         if (++stage == STAGES) {
@@ -885,6 +939,31 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst,
+                                                      const CUtensorMap* tm,
+                                                      int32_t c0, int32_t c1,
+                                                      uint32_t bar_cluster,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], "
+      "%5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1),
+      "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_op_pair(uint32_t dst,
+                                                 const CUtensorMap* tm,
+                                                 int32_t c0, int32_t c1,
+                                                 uint32_t bar_cluster,
+                                                 int hint, uint64_t policy) {
+  if (hint)
+    tma_load_2d_pair_hint(dst, tm, c0, c1, bar_cluster, policy);
+  else
+    tma_load_2d_pair(dst, tm, c0, c1, bar_cluster);
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
                                                 uint32_t ncols) {
   asm volatile(
@@ -973,6 +1052,7 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   uint32_t stage = 0, phase = 0, issued = 0;
+  const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
   for (int u = cluster; ok && u < g.num_units; u += nclusters) {
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
@@ -993,16 +1073,18 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
         if (A_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_2d_pair(sa + j * 64 * BK * 2, ta, a0 + 64 * j, k0, fb);
+            tma_load_op_pair(sa + j * 64 * BK * 2, ta, a0 + 64 * j, k0, fb,
+                             g.a_hint, pa);
         } else {
-          tma_load_2d_pair(sa, ta, k0, a0, fb);
+          tma_load_op_pair(sa, ta, k0, a0, fb, g.a_hint, pa);
         }
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_2d_pair(sb + j * 64 * BK * 2, tb, b0 + 64 * j, k0, fb);
+            tma_load_op_pair(sb + j * 64 * BK * 2, tb, b0 + 64 * j, k0, fb,
+                             g.b_hint, pb);
         } else {
-          tma_load_2d_pair(sb, tb, k0, b0, fb);
+          tma_load_op_pair(sb, tb, k0, b0, fb, g.b_hint, pb);
         }
         ++issued;
         if (++stage == STAGES2) {

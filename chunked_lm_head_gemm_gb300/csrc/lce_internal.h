@@ -35,6 +35,13 @@ struct GemmGeom {
   int tiles_per_split;  // column tiles per run (the last run may be shorter)
   int num_units;        // num_m * splits
   uint64_t timeout_ns;  // limit of every wait inside the kernel
+  // Tile order when every unit is one tile (splits == num_n): 0 = row
+  // block major; g > 0 = groups of g column tiles, row blocks inside a
+  // group (a wave then touches fewer column panels).
+  int group_n;
+  // L2 eviction priority of each operand's TMA loads: 0 = default,
+  // 1 = evict first (streamed), 2 = evict last (reused).
+  int a_hint, b_hint;
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------
