@@ -412,14 +412,70 @@ bool sizes_ok(int64_t L, int64_t H, int64_t V) {
          V <= (1ll << 31) - BN && H <= (1ll << 31) - BK;
 }
 
-int64_t default_chunk(int64_t L, int64_t V) {
-  const double budget = 4.0 * (1ull << 30);  // bf16 gradient-logit chunk
+// Contraction slots and rows per work unit of the variant in use on the
+// current device: CTA pairs (co-resident clusters, 256 rows) or single CTAs
+// (SMs, 128 rows). Without a usable device, a GB300's values.
+void slot_model(int* slots, int* rows_unit) {
+  char saved[sizeof t_last_cuda_error];
+  std::memcpy(saved, t_last_cuda_error, sizeof saved);
+  DeviceInfo* dev = nullptr;
+  const bool have = device_info(&dev) == LCE_OK;
+  std::memcpy(t_last_cuda_error, saved, sizeof saved);
+  const bool pair = use_pair() && (!have || dev->pair_slots > 0);
+  *rows_unit = pair ? 2 * BM : BM;
+  if (have)
+    *slots = pair ? dev->pair_slots : dev->num_sms;
+  else
+    *slots = pair ? 76 : 152;
+}
+
+// Modelled time of one backward row chunk of cr rows, in units of one
+// 64-deep k-slice of one output tile on one slot: the three contractions'
+// waves times their k-slices, the dW read-add-write it adds (charged at a
+// quarter of its DRAM time) and a fixed launch overhead (~0.1 ms).
+double chunk_cost(int64_t cr, int64_t H, int64_t V, int slots, int rows_unit) {
+  const double unit_s = 2.0 * rows_unit * BN * BK / 1.5e15 * slots;
+  const int64_t nm = ceil_div(cr, rows_unit);
+  const int64_t nh = ceil_div(H, BN);
+  const int64_t nvn = ceil_div(V, BN), nvm = ceil_div(V, rows_unit);
+  const double dh =
+      static_cast<double>(ceil_div(nm * nh, slots)) * ceil_div(V, BK);
+  int splits = 1, tps = static_cast<int>(nvn);
+  choose_splits(static_cast<int>(nm), static_cast<int>(nvn), slots, H,
+                &splits, &tps, rows_unit);
+  const double lg = static_cast<double>(ceil_div(nm * splits, slots)) * tps *
+                    ceil_div(H, BK);
+  const double dw =
+      static_cast<double>(ceil_div(nvm * nh, slots)) * ceil_div(cr, BK);
+  const double rmw = (8.0 * V * H / 2.0e13) / unit_s;
+  const double overhead = 1.0e-4 / unit_s;
+  return dh + lg + dw + rmw + overhead;
+}
+
+// Row chunk of the backward when the caller passes 0: the multiple of 256
+// rows, with the gradient-logit chunk within 8 GiB, that minimises the
+// modelled time of all chunks (ties: the larger chunk).
+int64_t default_chunk(int64_t L, int64_t H, int64_t V) {
+  const double budget = 8.0 * (1ull << 30);
   const int64_t ldg = round_up(V, 8);
-  int64_t cmax = static_cast<int64_t>(budget / (2.0 * ldg)) / BM * BM;
-  cmax = std::max<int64_t>(cmax, BM);
-  const int64_t nchunks = ceil_div(L, cmax);
-  const int64_t c = round_up(ceil_div(L, nchunks), BM);
-  return std::min(c, round_up(L, BM));
+  const int64_t step = 2 * BM;
+  int64_t cmax = static_cast<int64_t>(budget / (2.0 * ldg)) / step * step;
+  cmax = std::max<int64_t>(cmax, step);
+  cmax = std::min(cmax, round_up(L, step));
+  int slots = 0, rows_unit = 0;
+  slot_model(&slots, &rows_unit);
+  int64_t best_c = cmax;
+  double best = -1.0;
+  for (int64_t c = cmax; c >= step; c -= step) {
+    const int64_t full = L / c, rest = L - full * c;
+    double cost = full * chunk_cost(c, H, V, slots, rows_unit);
+    if (rest) cost += chunk_cost(rest, H, V, slots, rows_unit);
+    if (best < 0 || cost < best * (1.0 - 1e-9)) {
+      best = cost;
+      best_c = c;
+    }
+  }
+  return std::min(best_c, L);
 }
 
 WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
@@ -431,7 +487,7 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
     off = static_cast<size_t>(round_up(static_cast<int64_t>(off + bytes), 256));
     return o;
   };
-  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : default_chunk(L, V);
+  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : default_chunk(L, H, V);
   w.ldg = round_up(V, 8);
   // per-256-row loss sums: one set over all rows (forward), or one set per
   // row chunk (fused forward+backward), whichever is longer
@@ -541,7 +597,7 @@ size_t lce_workspace_size(int64_t L, int64_t H, int64_t V, lce_dtype dt,
 
 int64_t lce_default_chunk_rows(int64_t L, int64_t H, int64_t V) {
   if (!sizes_ok(L, H, V)) return 0;
-  return default_chunk(L, V);
+  return default_chunk(L, H, V);
 }
 
 lce_status lce_forward(const void* h, const void* W, lce_dtype dt,

@@ -144,9 +144,25 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
 // e = 2^(u - m_t) (bf16), u = z log2 e, m_t the maximum of u over the
 // 256-column tile; with lse2 = lse log2 e the softmax is e 2^(m_t - lse2),
 // so G = e 2^(m_t - lse2) - [j == y] on rows that take part, 0 elsewhere.
-// One thread per 8 consecutive columns (a 16-byte vector; 8 divides the
+// Works on 16-byte vectors of 8 consecutive columns (8 divides the
 // 256-column tile, so a vector never straddles two tiles). Columns between
 // V and ldg are padding that nothing reads.
+__device__ __forceinline__ uint4 exp_to_grad(uint4 in, float sc, int yo) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float lo = __uint_as_float(w[q] << 16) * sc;
+    float hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+    if (2 * q == yo) lo -= 1.f;
+    if (2 * q + 1 == yo) hi -= 1.f;
+    o[q] = pack_bf16x2(lo, hi);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One block per row (grid-stride over rows); each thread keeps four
+// 16-byte vectors in flight.
 __global__ void __launch_bounds__(256)
     k_grad_from_exp(uint16_t* __restrict__ E, int64_t ldg,
                     const float* __restrict__ tile_max, int64_t num_n,
@@ -154,35 +170,35 @@ __global__ void __launch_bounds__(256)
                     const int64_t* __restrict__ labels, int64_t rows,
                     int64_t V, int64_t ignore_index) {
   const int64_t nvec = (V + 7) / 8;
-  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+  constexpr int U = 4;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const int64_t y = labels[row];
     const bool valid = label_valid(y, V, ignore_index);
-    const float l2 = valid ? lse[row] * LOG2E : 0.f;
-    uint16_t* er = E + row * ldg;
+    uint4* er = reinterpret_cast<uint4*>(E + row * ldg);
+    if (!valid) {
+      for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x)
+        er[v] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const float l2 = lse[row] * LOG2E;
     const float* tm = tile_max + row * num_n;
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) +
-                     threadIdx.x;
-         v < nvec; v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      const int64_t j0 = v * 8;
-      uint4* p4 = reinterpret_cast<uint4*>(er + j0);
-      if (!valid) {
-        *p4 = make_uint4(0u, 0u, 0u, 0u);
-        continue;
-      }
-      const uint4 in = *p4;
-      const float sc = ex2(tm[j0 >> 8] - l2);
-      const int yo = static_cast<int>(y - j0);
-      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-      uint32_t o[4];
+    for (int64_t v0 = threadIdx.x; v0 < nvec;
+         v0 += static_cast<int64_t>(U) * blockDim.x) {
+      uint4 in[U];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float lo = __uint_as_float(w[q] << 16) * sc;
-        float hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
-        if (2 * q == yo) lo -= 1.f;
-        if (2 * q + 1 == yo) hi -= 1.f;
-        o[q] = pack_bf16x2(lo, hi);
+      for (int k = 0; k < U; ++k) {
+        const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
+        if (v < nvec) in[k] = er[v];
       }
-      *p4 = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
+        if (v < nvec) {
+          const int64_t j0 = v * 8;
+          er[v] = exp_to_grad(in[k], ex2(tm[j0 >> 8] - l2),
+                              static_cast<int>(y - j0));
+        }
+      }
     }
   }
 }
@@ -192,10 +208,8 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
                                  cudaStream_t s) {
-  const int64_t nvec = (V + 7) / 8;
-  const int64_t gx = (nvec + 255) / 256;
-  dim3 grid(static_cast<unsigned>(gx < 1 ? 1 : gx),
-            static_cast<unsigned>(rows < 65535 ? rows : 65535));
+  const unsigned grid =
+      static_cast<unsigned>(rows < 1048576 ? (rows < 1 ? 1 : rows) : 1048576);
   k_grad_from_exp<<<grid, 256, 0, s>>>(E, ldg, tile_max, num_n, lse, labels,
                                        rows, V, ignore_index);
   return cudaGetLastError();
