@@ -26,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "lce_oracle.c")
+_SOURCES = [_SRC, os.path.join(_HERE, "mlp_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "liblce_oracle.so")
 _lib = None
 _lock = threading.Lock()
@@ -40,13 +41,14 @@ DT_BF16, DT_F32, DT_F64 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
-    """Compile lce_oracle.c into liblce_oracle.so next to it (gcc, -O2)."""
+    """Compile the oracle's C sources into liblce_oracle.so (gcc, -O2)."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f)
+                    for f in _SOURCES)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared",
-                    "-pthread", "-o", tmp, _SRC, "-lm"], check=True)
+                    "-pthread", "-o", tmp, *_SOURCES, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -67,6 +69,10 @@ def load_library(path: str):
     lib.lce_oracle_rows.restype = i32
     lib.lce_oracle_count_valid.argtypes = [p, i64, i64, i64, p]
     lib.lce_oracle_count_valid.restype = i64
+    if hasattr(lib, "mlp_oracle"):
+        lib.mlp_oracle.argtypes = [p, p, p, p, i32, i64, i64, i64, p, i32, p,
+                                   p, p, p, p]
+        lib.mlp_oracle.restype = i32
     return lib
 
 
@@ -204,3 +210,45 @@ def count_valid(labels, V: int, ignore_index: int = -100):
     n = _load().lce_oracle_count_valid(_ptr(y), y.shape[0], V, ignore_index,
                                        ctypes.byref(bad))
     return int(n), bool(bad.value)
+
+
+def mlp(x, Wg, Wu, Wd, dy=None, want_dx: bool = True, want_dW: bool = True,
+        nthreads: int | None = None):
+    """Gated MLP y = (silu(x Wg^T) * (x Wu^T)) Wd^T in float64, and its
+    backward for dy (float64-widened) when given.
+
+    x [L,H]; Wg, Wu [I,H]; Wd [H,I] (one dtype). Returns dict(y, dx, dWg,
+    dWu, dWd); gradients are None without dy or when not wanted."""
+    xn, dt = _as_input(x)
+    arrs = [_as_input(w) for w in (Wg, Wu, Wd)]
+    if any(a[1] != dt for a in arrs):
+        raise TypeError("x and the weights must have the same dtype")
+    gn, un, dn = (a[0] for a in arrs)
+    L, H = xn.shape
+    I = gn.shape[0]
+    assert gn.shape == (I, H) and un.shape == (I, H) and dn.shape == (H, I)
+    y = np.empty((L, H), np.float64)
+    dyn = None
+    dx = dWg = dWu = dWd = None
+    if dy is not None:
+        try:
+            import torch
+            if isinstance(dy, torch.Tensor):
+                dy = dy.detach().cpu().double().numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        dyn = np.ascontiguousarray(dy, dtype=np.float64)
+        assert dyn.shape == (L, H)
+        if want_dx:
+            dx = np.empty((L, H), np.float64)
+        if want_dW:
+            dWg = np.empty((I, H), np.float64)
+            dWu = np.empty((I, H), np.float64)
+            dWd = np.empty((H, I), np.float64)
+    st = _load().mlp_oracle(_ptr(xn), _ptr(gn), _ptr(un), _ptr(dn), dt, L, H,
+                            I, _ptr(dyn), nthreads or default_threads(),
+                            _ptr(y), _ptr(dx), _ptr(dWg), _ptr(dWu),
+                            _ptr(dWd))
+    if st != OK:
+        raise RuntimeError(f"mlp_oracle status {st}")
+    return dict(y=y, dx=dx, dWg=dWg, dWu=dWu, dWd=dWd)

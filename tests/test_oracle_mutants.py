@@ -15,6 +15,21 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 
+MLP_MUTANTS = {
+    "silu_grad_sign": ("return s * (1.0 + t * (1.0 - s));",
+                       "return s * (1.0 + t * s);"),
+    "du_uses_grad": ("j->du[r * j->I + i] = da * silu(g);",
+                     "j->du[r * j->I + i] = da * silu_grad(g);"),
+    "dx_drops_up": ("dxr[k] += cg * wg[k] + cu * wu[k];",
+                    "dxr[k] += cg * wg[k];"),
+    "dWd_transposed": ("double c = j->dy[r * j->H + h];",
+                       "double c = j->dy[r * j->H + (h + 1) % j->H];"),
+    "gate_up_swapped": ("j->a[r * j->I + i] = silu(sg) * su;",
+                        "j->a[r * j->I + i] = silu(su) * sg;"),
+    "da_wrong_index": ("for (int64_t h = 0; h < j->H; ++h) da += dyr[h] * j->Wd[h * j->I + i];",
+                       "for (int64_t h = 0; h < j->H; ++h) da += dyr[h] * j->Wd[i * j->H + h % j->H];"),
+}
+
 MUTANTS = {
     "drop_onehot": ("g[y] -= jb->gscale;", "(void)y;"),
     "onehot_sign": ("g[y] -= jb->gscale;", "g[y] += jb->gscale;"),
@@ -77,3 +92,41 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
 
 def test_unmutated_passes_all_pins(oracle_mod):
     assert not _caught(oracle_mod)
+
+
+def _mlp_caught(mod) -> bool:
+    from tests import test_mlp_oracle_pins as mp
+    checks = [
+        lambda o: mp.test_against_torch_autograd(o, 5, 3, 7, 1),
+        lambda o: mp.test_finite_differences(o),
+        lambda o: mp.test_up_projection_zero(o),
+        lambda o: mp.test_gate_projection_zero(o),
+    ]
+    for check in checks:
+        try:
+            check(mod)
+        except (AssertionError, RuntimeError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MLP_MUTANTS))
+def test_planted_mlp_mistake_is_caught(name, tmp_path, monkeypatch):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src_path = os.path.join(os.path.dirname(oracle._SRC), "mlp_oracle.c")
+    src = open(src_path).read()
+    old, new = MLP_MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutant = tmp_path / "mlp_mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmlpmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread",
+                    "-o", str(so), oracle._SRC, str(mutant), "-lm"],
+                   check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(so)))
+    assert _mlp_caught(oracle), f"planted mistake {name} passed every pin"
+
+
+def test_unmutated_mlp_passes_all_pins(oracle_mod):
+    assert not _mlp_caught(oracle_mod)
