@@ -24,6 +24,8 @@ Both paths are timed; the line reports the --mode one and lists both under
 
 --impl reference times the float64 oracle instead (host cores, bounded row
 sample per step) and prints the same line with "impl": "reference".
+--workload mlp times the sequence-tiled gated MLP (lce_mlp_forward +
+lce_mlp_backward) on a Qwen3 MLP shape instead (--config qwen3-8b-mlp ...).
 --gpus N under torchrun: N independent replicas, one per GPU (the library
 has no multi-GPU path), weak scaling, max time over ranks.
 """
@@ -270,6 +272,7 @@ def main():
     ap.add_argument("--mode", default="fused", choices=["separate", "fused"])
     ap.add_argument("--only-mode", action="store_true",
                     help="time only --mode (profiling runs)")
+    ap.add_argument("--workload", default="lce", choices=["lce", "mlp"])
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="contractions on CTA pairs (1) or single CTAs (0); "
                          "-1 keeps the library default")
@@ -277,6 +280,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
+    if args.workload == "mlp":
+        return bench_mlp(args)
     from chunked_lm_head_gemm_gb300.inputs import WORKLOADS
     wl = WORKLOADS[args.config]
     if args.rows:
@@ -582,6 +587,155 @@ def main():
             "peak_extra_bytes": int(ws.numel()),
         }
         print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def bench_mlp(args):
+    """The sequence-tiled gated MLP: y = (silu(x Wg^T) * (x Wu^T)) Wd^T,
+    forward + backward per step on one GPU (replicas under torchrun)."""
+    import torch
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    from chunked_lm_head_gemm_gb300.inputs import MLP_WORKLOADS, make_mlp_inputs
+    name = args.config if args.config.endswith("-mlp") else "qwen3-8b-mlp"
+    wl = MLP_WORKLOADS[name]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    metric = "sequence-tiled gated MLP fwd+bwd tokens/s"
+    if args.impl == "reference":
+        if rank == 0:
+            import oracle
+            from chunked_lm_head_gemm_gb300.inputs import make_mlp_inputs as mk
+            oracle.build()
+            rows = 8
+            x, Wg, Wu, Wd, dy = mk(wl.with_rows(rows), 0, "cpu")
+            for _ in range(args.warmup):
+                oracle.mlp(x, Wg, Wu, Wd, dy)
+            times = []
+            for _ in range(args.steps):
+                t0 = time.perf_counter()
+                oracle.mlp(x, Wg, Wu, Wd, dy)
+                times.append(time.perf_counter() - t0)
+            t = statistics.median(times)
+            v = rows / t
+            print(json.dumps({
+                "impl": "reference", "metric": metric, "value": v,
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t * 1e3,
+                "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "L": wl.L, "H": wl.H,
+                           "I": wl.I, "sample_rows": rows},
+                "cpu_baseline": {"value": v, "unit": "tokens/s",
+                                 "cores": oracle.default_threads(),
+                                 "kind": "oracle",
+                                 "sample": f"{rows} rows per step"},
+                "e2e": {"value": v, "unit": "tokens/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lce.load()
+    if args.cta_pair >= 0:
+        B.set_cta_pair(bool(args.cta_pair))
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=0, device=dev)
+    L, H, I = wl.L, wl.H, wl.I
+    chunk = args.chunk_rows
+    ws = torch.empty(lce.mlp_workspace_size(L, H, I, chunk),
+                     dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dWg = torch.empty(I, H, dtype=torch.float32, device=dev)
+    dWu = torch.empty(I, H, dtype=torch.float32, device=dev)
+    dWd = torch.empty(H, I, dtype=torch.float32, device=dev)
+
+    def step():
+        lce.mlp_forward(x, Wg, Wu, Wd, chunk, ws, y)
+        lce.mlp_backward(x, Wg, Wu, Wd, dy, chunk, ws, dx, dWg, dWu, dWd)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lce.get_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    B.profile_start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    stats = B.profile_stop()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    if lce.get_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    per_step = t.item() / 1e3 / args.steps
+    peaks, peak_src = load_peaks()
+    peak_t = peaks["bf16_tflops_sustained"]
+    kernels = {}
+    total_k_ms = sum(v[1] for v in stats.values()) or 1.0
+    for kname, (n, ms, fl) in stats.items():
+        kernels[kname] = {"launches": n, "ms_per_launch": ms / n,
+                          "share": ms / total_k_ms,
+                          "tflops": (fl / (ms / 1e3) / 1e12) if fl else None}
+    dname, (dn, dms, dfl) = max(stats.items(), key=lambda kv: kv[1][1])
+    achieved = dfl / (dms / 1e3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rows = 16
+        t0 = time.perf_counter()
+        oracle.mlp(x[:rows].cpu(), Wg.cpu(), Wu.cpu(), Wd.cpu(),
+                   dy[:rows].cpu())
+        tc = time.perf_counter() - t0
+        cpu = {"value": rows / tc, "unit": "tokens/s",
+               "cores": oracle.default_threads(), "kind": "oracle",
+               "sample": f"first {rows} rows, float64 forward + backward "
+                         f"(y, dx, dWg, dWu, dWd) in {tc:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": L * world / per_step,
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "L": L, "H": H, "I": I,
+                       "chunk_rows": chunk or "default",
+                       "cta_pair": B.get_cta_pair(),
+                       "l2": "inputs larger than L2, no flush"},
+            "tflops_model": 18.0 * L * H * I / per_step / 1e12,
+            "tflops_executed": 22.0 * L * H * I / per_step / 1e12,
+            "peak_note": (f"18LHI model flops (22LHI executed: the backward "
+                          f"recomputes gate/up) vs {peak_t} TFLOP/s bf16 "
+                          f"sustained ({peak_src})"),
+            "roofline": {"bound": "tensor", "achieved": achieved,
+                         "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": achieved / peak_t, "traffic": None,
+                         "kernel": dname, "flops_per_launch": dfl / dn},
+            "kernels": kernels,
+            "gpu_launches": int(sum(v[0] for v in stats.values())),
+            "clocks": clk, "cpu_baseline": cpu}), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 

@@ -12,15 +12,19 @@ include/lce.h; this package is the thin Python binding.
     loss, lse = lce.forward(h, W, labels)
     dH, dW = lce.backward(h, W, labels, lse, dloss)
     loss, lse, dH, dW = lce.forward_backward(h, W, labels)  # no recompute
+    y = lce.mlp_forward(x, Wg, Wu, Wd)          # sequence-tiled gated MLP
+    dx, dWg, dWu, dWd = lce.mlp_backward(x, Wg, Wu, Wd, dy)
 """
 from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
                        alloc_workspace, backward, default_chunk_rows, forward,
                        forward_backward, get_error, library_path,
-                       linear_cross_entropy, load, profile_start, profile_stop,
+                       linear_cross_entropy, load, mlp_backward, mlp_forward,
+                       mlp_workspace_size, profile_start, profile_stop,
                        scale_gradients, workspace_size)
 
 __all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "alloc_workspace",
            "backward", "default_chunk_rows", "forward", "forward_backward",
            "get_error", "library_path", "linear_cross_entropy", "load",
+           "mlp_backward", "mlp_forward", "mlp_workspace_size",
            "profile_start", "profile_stop", "scale_gradients",
            "workspace_size"]

@@ -36,9 +36,10 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_last_cuda_error", "lce_test_gemm", "lce_test_wait_timeout",
             "lce_profile_start", "lce_profile_stop", "lce_forward_static",
             "lce_forward_backward", "lce_scale_gradients",
-            "lce_set_cta_pair", "lce_get_cta_pair")
+            "lce_set_cta_pair", "lce_get_cta_pair", "lce_mlp_workspace_size",
+            "lce_mlp_forward", "lce_mlp_backward")
 
-KERNEL_KINDS = 13
+KERNEL_KINDS = 19
 
 
 class KernelStat(ctypes.Structure):
@@ -101,6 +102,14 @@ def load(build_if_missing: bool = False):
         lib.lce_forward_backward.restype = i32
         lib.lce_scale_gradients.argtypes = [p, i32, i64, i64, p, i64, p, p]
         lib.lce_scale_gradients.restype = i32
+        lib.lce_mlp_workspace_size.argtypes = [i64, i64, i64, i64]
+        lib.lce_mlp_workspace_size.restype = sz
+        lib.lce_mlp_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p,
+                                        sz, p]
+        lib.lce_mlp_forward.restype = i32
+        lib.lce_mlp_backward.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p,
+                                         p, p, p, p, sz, p]
+        lib.lce_mlp_backward.restype = i32
         lib.lce_set_cta_pair.argtypes = [i32]
         lib.lce_set_cta_pair.restype = i32
         lib.lce_get_cta_pair.argtypes = []
@@ -274,6 +283,72 @@ def tc_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int,
 def wait_timeout_probe(timeout_ns: int, device=None):
     st = load().lce_test_wait_timeout(timeout_ns, _stream_ptr(device))
     _check(st, "lce_test_wait_timeout")
+
+
+def _check_mlp(x, Wg, Wu, Wd):
+    ts = (x, Wg, Wu, Wd)
+    if not all(t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+               for t in ts):
+        raise ValueError("x, Wg, Wu, Wd must be contiguous bf16 CUDA tensors")
+    L, H = x.shape
+    I = Wg.shape[0]
+    if Wg.shape != (I, H) or Wu.shape != (I, H) or Wd.shape != (H, I):
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, Wg "
+                         f"{tuple(Wg.shape)}, Wu {tuple(Wu.shape)}, Wd "
+                         f"{tuple(Wd.shape)}")
+    return L, H, I
+
+
+def mlp_workspace_size(L: int, H: int, I: int, chunk_rows: int = 0) -> int:
+    n = load().lce_mlp_workspace_size(L, H, I, chunk_rows)
+    if n == 0:
+        raise ValueError(f"invalid MLP sizes L={L} H={H} I={I}")
+    return n
+
+
+def mlp_forward(x, Wg, Wu, Wd, chunk_rows: int = 0, workspace=None,
+                y_out=None):
+    """y = (silu(x Wg^T) * (x Wu^T)) Wd^T over row chunks (bf16)."""
+    lib = load()
+    L, H, I = _check_mlp(x, Wg, Wu, Wd)
+    if workspace is None:
+        workspace = torch.empty(mlp_workspace_size(L, H, I, chunk_rows),
+                                dtype=torch.uint8, device=x.device)
+    y = y_out if y_out is not None else torch.empty_like(x)
+    st = lib.lce_mlp_forward(x.data_ptr(), Wg.data_ptr(), Wu.data_ptr(),
+                             Wd.data_ptr(), L, H, I, chunk_rows, y.data_ptr(),
+                             workspace.data_ptr(), workspace.numel(),
+                             _stream_ptr(x.device))
+    _check(st, "lce_mlp_forward")
+    return y
+
+
+def mlp_backward(x, Wg, Wu, Wd, dy, chunk_rows: int = 0, workspace=None,
+                 dx_out=None, dWg_out=None, dWu_out=None, dWd_out=None):
+    """Returns (dx bf16 [L,H], dWg fp32 [I,H], dWu fp32 [I,H], dWd fp32
+    [H,I]) for upstream gradient dy, recomputing the chunk intermediates."""
+    lib = load()
+    L, H, I = _check_mlp(x, Wg, Wu, Wd)
+    if not (dy.is_cuda and dy.dtype == torch.bfloat16 and dy.is_contiguous()
+            and dy.shape == (L, H)):
+        raise ValueError("dy must be a contiguous bf16 CUDA [L,H] tensor")
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(mlp_workspace_size(L, H, I, chunk_rows),
+                                dtype=torch.uint8, device=dev)
+    dx = dx_out if dx_out is not None else torch.empty_like(x)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dWg = dWg_out if dWg_out is not None else torch.empty(I, H, **f32)
+    dWu = dWu_out if dWu_out is not None else torch.empty(I, H, **f32)
+    dWd = dWd_out if dWd_out is not None else torch.empty(H, I, **f32)
+    st = lib.lce_mlp_backward(x.data_ptr(), Wg.data_ptr(), Wu.data_ptr(),
+                              Wd.data_ptr(), dy.data_ptr(), L, H, I,
+                              chunk_rows, dx.data_ptr(), dWg.data_ptr(),
+                              dWu.data_ptr(), dWd.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(),
+                              _stream_ptr(dev))
+    _check(st, "lce_mlp_backward")
+    return dx, dWg, dWu, dWd
 
 
 def set_cta_pair(enable: bool):

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(OUT_DIR, "liblce.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["lce_api.cu", "lce_gemm_loss.cu", "lce_gemm_store.cu",
-           "lce_small.cu"]
+           "lce_gemm_mlp.cu", "lce_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]

@@ -40,10 +40,11 @@ lce_status cuda_fail(cudaError_t e, const char* where) {
 // When on, every kernel this thread launches is bracketed by two CUDA events
 // on its stream; stop() waits for them and sums durations per kernel kind.
 const char* const kKindNames[LCE_KERNEL_KINDS] = {
-    "count_valid", "gemm_lse",   "lse_combine",   "loss_finalize",
-    "f32_to_bf16", "gemm_grad",  "gemm_dH",       "gemm_dW",
-    "test_gemm",   "wait_probe", "gemm_fused",    "grad_from_exp",
-    "scale_grads"};
+    "count_valid",  "gemm_lse",     "lse_combine",   "loss_finalize",
+    "f32_to_bf16",  "gemm_grad",    "gemm_dH",       "gemm_dW",
+    "test_gemm",    "wait_probe",   "gemm_fused",    "grad_from_exp",
+    "scale_grads",  "mlp_gate_up",  "mlp_down",      "mlp_da",
+    "mlp_dx",       "mlp_dWd",      "mlp_dWgu"};
 
 struct ProfRec {
   int kind;
@@ -226,7 +227,9 @@ lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
 // bounds the live A row panels when choosing column splits. Defaults are the
 // values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,l2mb=M" (kinds lse,
 // grad, fused, dH, dW, test; H in 0..2; G >= 0) overrides them.
-enum TuneKind { T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_KINDS };
+enum TuneKind {
+  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_KINDS
+};
 struct Tune {
   int a_hint[T_KINDS];
   int b_hint[T_KINDS];
@@ -241,7 +244,7 @@ const Tune& tune() {
     const char* env = std::getenv("LCE_TUNE");
     if (!env) return v;
     static const char* names[T_KINDS] = {"lse", "grad", "fused", "dH", "dW",
-                                         "test"};
+                                         "test", "mlp"};
     std::string spec(env);
     size_t pos = 0;
     while (pos < spec.size()) {
@@ -342,12 +345,18 @@ struct GemmOperands {
   int64_t b_ld;
   bool sweep;          // sweep all column tiles per row block (choose splits)
   int kind;            // TuneKind
+  // B from two maps (GemmGeom::b_dual): 1 = along N (b2 has b's shape;
+  // tiles of 128 output columns), 2 = along K (b covers k < k_split, b2
+  // the rest; both have b's row stride)
+  int b_dual = 0;
+  const void* b2 = nullptr;
+  int64_t k_split = 0;
 };
 
 struct GemmPlan {
   bool pair;
   GemmGeom g;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tb2;
   int grid;
 };
 
@@ -357,20 +366,34 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   const int rows_unit = pl->pair ? 2 * BM : BM;
   const int slots = pl->pair ? dev.pair_slots : dev.num_sms;
   const int num_m = static_cast<int>(ceil_div(o.M, rows_unit));
-  const int num_n = static_cast<int>(ceil_div(o.N, BN));
+  const int tile_n = o.b_dual == 1 ? BN / 2 : BN;
+  const int num_n = static_cast<int>(ceil_div(o.N, tile_n));
   int splits = num_n, tps = 1;
   if (o.sweep) choose_splits(num_m, num_n, slots, o.K, &splits, &tps, rows_unit);
   pl->g = make_geom(o.M, o.N, o.K, splits, tps, rows_unit);
+  pl->g.num_n = num_n;
   const Tune& tn = tune();
   pl->g.a_hint = tn.a_hint[o.kind];
   pl->g.b_hint = tn.b_hint[o.kind];
   if (!o.sweep) pl->g.group_n = tn.group_n[o.kind];
+  pl->g.b_dual = o.b_dual;
+  pl->g.k_split_kb = o.b_dual == 2 ? static_cast<int>(o.k_split / BK) : 0;
   lce_status st = o.a_mn ? tmap_mnmajor(&pl->ta, o.a, o.M, o.K, o.a_ld)
                          : tmap_kmajor(&pl->ta, o.a, o.K, o.M, o.a_ld, BM);
   if (st != LCE_OK) return st;
-  st = o.b_mn ? tmap_mnmajor(&pl->tb, o.b, o.N, o.K, o.b_ld)
-              : tmap_kmajor(&pl->tb, o.b, o.K, o.N, o.b_ld,
-                            pl->pair ? BM : BN);
+  if (o.b_dual == 1) {  // K-major, 128-row boxes from each map
+    st = tmap_kmajor(&pl->tb, o.b, o.K, o.N, o.b_ld, BM);
+    if (st == LCE_OK) st = tmap_kmajor(&pl->tb2, o.b2, o.K, o.N, o.b_ld, BM);
+  } else if (o.b_dual == 2) {  // MN-major, K split between the maps
+    st = tmap_mnmajor(&pl->tb, o.b, o.N, o.k_split, o.b_ld);
+    if (st == LCE_OK)
+      st = tmap_mnmajor(&pl->tb2, o.b2, o.N, o.K - o.k_split, o.b_ld);
+  } else {
+    st = o.b_mn ? tmap_mnmajor(&pl->tb, o.b, o.N, o.K, o.b_ld)
+                : tmap_kmajor(&pl->tb, o.b, o.K, o.N, o.b_ld,
+                              pl->pair ? BM : BN);
+    pl->tb2 = pl->tb;
+  }
   if (st != LCE_OK) return st;
   const int units = std::max(1, std::min(pl->g.num_units, slots));
   pl->grid = pl->pair ? 2 * units : units;
@@ -396,9 +419,9 @@ cudaError_t run_fused(const GemmPlan& pl, const FusedParams& p, unsigned* err,
 cudaError_t run_store(const GemmPlan& pl, bool a_mn, bool b_mn,
                       const StoreParams& p, unsigned* err, cudaStream_t s) {
   return pl.pair ? launch_gemm_pair_store(a_mn, b_mn, pl.ta, pl.tb, pl.g, p,
-                                          err, pl.grid, s)
+                                          err, pl.grid, s, &pl.tb2)
                  : launch_gemm_store(a_mn, b_mn, pl.ta, pl.tb, pl.g, p, err,
-                                     pl.grid, s);
+                                     pl.grid, s, &pl.tb2);
 }
 
 struct WsLayout {
@@ -920,6 +943,221 @@ lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                      dloss, s);
   ps.done(0);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "scale_grads");
+}
+
+// ---- sequence-tiled gated MLP ----------------------------------------------
+
+}  // extern "C"
+
+namespace lce {
+namespace {
+
+struct MlpLayout {
+  size_t g, u, a, dgu, total;
+  int64_t chunk;
+};
+
+bool mlp_sizes_ok(int64_t L, int64_t H, int64_t I) {
+  return L >= 1 && H >= 8 && I >= 64 && H % 8 == 0 && I % 64 == 0 &&
+         L <= (1ll << 31) - 2 * BM && H <= (1ll << 30) && I <= (1ll << 29);
+}
+
+// Row chunk of the MLP: the chunk's four intermediates (g, u, a and
+// [dg | du], 10 I bytes per row) within 4 GiB, in multiples of 256 rows,
+// split evenly.
+int64_t mlp_default_chunk(int64_t L, int64_t I) {
+  const double budget = 4.0 * (1ull << 30);
+  const int64_t step = 2 * BM;
+  int64_t cmax = static_cast<int64_t>(budget / (10.0 * I)) / step * step;
+  cmax = std::max<int64_t>(cmax, step);
+  const int64_t n = ceil_div(L, cmax);
+  return std::min(round_up(ceil_div(L, n), step), L);
+}
+
+MlpLayout mlp_layout(int64_t L, int64_t I, int64_t chunk_rows) {
+  MlpLayout w{};
+  w.chunk = chunk_rows > 0 ? std::min(chunk_rows, L) : mlp_default_chunk(L, I);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off + bytes), 256));
+    return o;
+  };
+  const size_t plane = static_cast<size_t>(w.chunk) * I * 2;
+  w.g = take(plane);
+  w.u = take(plane);
+  w.a = take(plane);
+  w.dgu = take(2 * plane);
+  w.total = off;
+  return w;
+}
+
+// a_c = silu(x_c Wg^T) * (x_c Wu^T), optionally saving g_c and u_c.
+lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
+                       const void* Wg, const void* Wu, int64_t H, int64_t I,
+                       uint16_t* a, uint16_t* g, uint16_t* u, cudaStream_t s) {
+  GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false, T_MLP};
+  o.b_dual = 1;
+  o.b2 = Wu;
+  GemmPlan pl;
+  lce_status st = plan_gemm(o, dev, &pl);
+  if (st != LCE_OK) return st;
+  SwigluParams p{a, g, u, I};
+  ProfScope ps(LCE_K_MLP_GATE_UP, s);
+  cudaError_t e = launch_gemm_swiglu(pl.pair, pl.ta, pl.tb, pl.tb2, pl.g, p,
+                                     dev.err, pl.grid, s);
+  ps.done(2.0 * cr * H * 2 * I);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "mlp_gate_up");
+}
+
+// out (+)= scale * (A B) for the plain MLP contractions.
+lce_status mlp_store(const DeviceInfo& dev, const GemmOperands& o,
+                     const StoreParams& p, int kind, cudaStream_t s) {
+  GemmPlan pl;
+  lce_status st = plan_gemm(o, dev, &pl);
+  if (st != LCE_OK) return st;
+  ProfScope ps(kind, s);
+  cudaError_t e = run_store(pl, o.a_mn, o.b_mn, p, dev.err, s);
+  ps.done(2.0 * o.M * o.N * o.K);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "mlp contraction");
+}
+
+lce_status mlp_check(const void* x, const void* Wg, const void* Wu,
+                     const void* Wd, int64_t L, int64_t H, int64_t I) {
+  if (!x || !Wg || !Wu || !Wd) return LCE_ERR_INVALID_ARG;
+  if (!mlp_sizes_ok(L, H, I)) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
+    return LCE_ERR_INVALID_ARG;
+  return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+extern "C" {
+
+size_t lce_mlp_workspace_size(int64_t L, int64_t H, int64_t I,
+                              int64_t chunk_rows) {
+  if (!mlp_sizes_ok(L, H, I) || chunk_rows < 0) return 0;
+  return mlp_layout(L, I, chunk_rows).total;
+}
+
+lce_status lce_mlp_forward(const void* x, const void* Wg, const void* Wu,
+                           const void* Wd, int64_t L, int64_t H, int64_t I,
+                           int64_t chunk_rows, void* y, void* ws,
+                           size_t ws_bytes, void* stream) {
+  lce_status st = mlp_check(x, Wg, Wu, Wd, L, H, I);
+  if (st != LCE_OK) return st;
+  if (!y || !ws || !aligned16(y) || !aligned16(ws) || chunk_rows < 0)
+    return LCE_ERR_INVALID_ARG;
+  const MlpLayout w = mlp_layout(L, I, chunk_rows);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint16_t* A = reinterpret_cast<uint16_t*>(wsb + w.a);
+  for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
+    const int64_t cr = std::min(w.chunk, L - c0);
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * H;
+    // a_c = silu(x_c Wg^T) * (x_c Wu^T)
+    if ((st = mlp_gate_up(*dev, xc, cr, Wg, Wu, H, I, A, nullptr, nullptr,
+                          s)) != LCE_OK)
+      return st;
+    // y_c = a_c Wd^T
+    StoreParams p{};
+    p.out = static_cast<uint16_t*>(y) + c0 * H;
+    p.ldo = H;
+    p.out_f32 = 0;
+    if ((st = mlp_store(*dev, {cr, H, I, false, false, A, I, Wd, I, false,
+                               T_MLP},
+                        p, LCE_K_MLP_DOWN, s)) != LCE_OK)
+      return st;
+  }
+  return LCE_OK;
+}
+
+lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
+                            const void* Wd, const void* dy, int64_t L,
+                            int64_t H, int64_t I, int64_t chunk_rows,
+                            void* dx, float* dWg, float* dWu, float* dWd,
+                            void* ws, size_t ws_bytes, void* stream) {
+  lce_status st = mlp_check(x, Wg, Wu, Wd, L, H, I);
+  if (st != LCE_OK) return st;
+  if (!dy || !dx || !dWg || !dWu || !dWd || !ws || chunk_rows < 0)
+    return LCE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(dx) || !aligned16(dWg) ||
+      !aligned16(dWu) || !aligned16(dWd) || !aligned16(ws))
+    return LCE_ERR_INVALID_ARG;
+  const MlpLayout w = mlp_layout(L, I, chunk_rows);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint16_t* G = reinterpret_cast<uint16_t*>(wsb + w.g);
+  uint16_t* U = reinterpret_cast<uint16_t*>(wsb + w.u);
+  uint16_t* A = reinterpret_cast<uint16_t*>(wsb + w.a);
+  uint16_t* DGU = reinterpret_cast<uint16_t*>(wsb + w.dgu);
+  for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
+    const int64_t cr = std::min(w.chunk, L - c0);
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * H;
+    const uint16_t* dyc = static_cast<const uint16_t*>(dy) + c0 * H;
+    // (1) recompute g_c, u_c, a_c
+    if ((st = mlp_gate_up(*dev, xc, cr, Wg, Wu, H, I, A, G, U, s)) != LCE_OK)
+      return st;
+    // (2) da_c = dy_c Wd -> dg_c, du_c into [dg | du]
+    {
+      GemmOperands o{cr, I, H, false, true, dyc, H, Wd, I, false, T_MLP};
+      GemmPlan pl;
+      if ((st = plan_gemm(o, *dev, &pl)) != LCE_OK) return st;
+      SwigluBwdParams p{G, U, I, DGU, 2 * I, I};
+      ProfScope ps(LCE_K_MLP_DA, s);
+      cudaError_t e = launch_gemm_swiglu_bwd(pl.pair, pl.ta, pl.tb, pl.tb2,
+                                             pl.g, p, dev->err, pl.grid, s);
+      ps.done(2.0 * cr * I * H);
+      if (e != cudaSuccess) return cuda_fail(e, "mlp_da");
+    }
+    // (3) dx_c = [dg | du] [Wg ; Wu]  (K = 2I, B from two maps along K)
+    {
+      GemmOperands o{cr, H, 2 * I, false, true, DGU, 2 * I, Wg, H, false,
+                     T_MLP};
+      o.b_dual = 2;
+      o.b2 = Wu;
+      o.k_split = I;
+      StoreParams p{};
+      p.out = static_cast<uint16_t*>(dx) + c0 * H;
+      p.ldo = H;
+      if ((st = mlp_store(*dev, o, p, LCE_K_MLP_DX, s)) != LCE_OK) return st;
+    }
+    // (4) dWd (+)= dy_c^T a_c
+    {
+      StoreParams p{};
+      p.out = dWd;
+      p.ldo = I;
+      p.out_f32 = 1;
+      p.accumulate = c0 > 0;
+      if ((st = mlp_store(*dev, {H, I, cr, true, true, dyc, H, A, I, false,
+                                 T_MLP},
+                          p, LCE_K_MLP_DWD, s)) != LCE_OK)
+        return st;
+    }
+    // (5) [dWg ; dWu] (+)= [dg | du]^T x_c, rows >= I going to dWu
+    {
+      StoreParams p{};
+      p.out = dWg;
+      p.out2 = dWu;
+      p.split_row = I;
+      p.ldo = H;
+      p.out_f32 = 1;
+      p.accumulate = c0 > 0;
+      if ((st = mlp_store(*dev, {2 * I, H, cr, true, true, DGU, 2 * I, xc, H,
+                                 false, T_MLP},
+                          p, LCE_K_MLP_DWGU, s)) != LCE_OK)
+        return st;
+    }
+  }
+  return LCE_OK;
 }
 
 lce_status lce_get_error(void* stream) {

@@ -563,11 +563,19 @@ struct EpiStore {
   int64_t row;
   bool row_ok;
   float scale;
+  void* base;     // output holding this row
+  int64_t orow;   // the row's index in it
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
     row = t.row0 + r;
     row_ok = row < g.M;
+    base = p.out;
+    orow = row;
+    if (p.out2 != nullptr && row >= p.split_row) {
+      base = p.out2;
+      orow = row - p.split_row;
+    }
     scale = 1.f;
     if (p.n_valid != nullptr) {
       const unsigned long long n = *p.n_valid;
@@ -594,7 +602,7 @@ struct EpiStore {
       const bool full = j0 + 32 <= g.N;
       const int nv = full ? 32 : static_cast<int>(g.N - j0);
       if (p.out_f32) {
-        float* dst = static_cast<float*>(p.out) + row * p.ldo + j0;
+        float* dst = static_cast<float*>(base) + orow * p.ldo + j0;
         if (full) {
           float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -616,7 +624,7 @@ struct EpiStore {
             if (i < nv) dst[i] = p.accumulate ? dst[i] + v[i] : v[i];
         }
       } else {
-        uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.ldo + j0;
+        uint16_t* dst = static_cast<uint16_t*>(base) + orow * p.ldo + j0;
         if (full) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -629,6 +637,145 @@ struct EpiStore {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (i < nv) dst[i] = to_bf16_bits(v[i]);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(const Params&, const GemmGeom&,
+                                           const Unit&, int) {}
+};
+
+// 1 / (1 + 2^(-t log2 e)): the logistic function on the SFU.
+__device__ __forceinline__ float sigmoid_fast(float t) {
+  return __fdividef(1.f, 1.f + ex2(-t * LOG2E));
+}
+
+// Gated-MLP gate/up contraction with B dual along N: for the tile's 128
+// output columns, accumulator columns 0..127 are g and 128..255 are u;
+// writes a = silu(g) u (and g, u when asked) in bf16.
+struct EpiSwiGLU {
+  using Params = SwigluParams;
+  int64_t row;
+  bool row_ok;
+
+  __device__ __forceinline__ void begin_unit(const Params&, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = t.row0 + r;
+    row_ok = row < g.M;
+  }
+
+  __device__ __forceinline__ static void store32(uint16_t* dst, const float* v,
+                                                 int nv) {
+    if (nv == 32) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                           pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nv) dst[i] = to_bf16_bits(v[i]);
+    }
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t i0 = static_cast<int64_t>(n_blk) * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t j0 = i0 + c * 32;
+      if (j0 >= g.N) break;
+      float gv[32], uv[32];
+      tmem_ld32(taddr + c * 32, gv);
+      tmem_ld32(taddr + BN / 2 + c * 32, uv);
+      if (!row_ok) continue;
+      const int64_t rem = g.N - j0;
+      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int64_t off = row * p.ld + j0;
+      if (p.g) store32(p.g + off, gv, nv);
+      if (p.u) store32(p.u + off, uv, nv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) uv[i] *= gv[i] * sigmoid_fast(gv[i]);
+      store32(p.a + off, uv, nv);
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(const Params&, const GemmGeom&,
+                                           const Unit&, int) {}
+};
+
+// Gated-MLP backward: accumulator = da; dg = da u silu'(g),
+// du = da silu(g), with silu'(t) = s (1 + t (1 - s)), s the logistic.
+struct EpiSwiGLUBwd {
+  using Params = SwigluBwdParams;
+  int64_t row;
+  bool row_ok;
+
+  __device__ __forceinline__ void begin_unit(const Params&, const GemmGeom& g,
+                                             const Unit& t, int r) {
+    row = t.row0 + r;
+    row_ok = row < g.M;
+  }
+
+  __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
+                                       const Unit&, int n_blk, uint32_t taddr,
+                                       int) {
+    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int64_t j0 = n0 + c * 32;
+      if (j0 >= g.N) break;
+      float da[32];
+      tmem_ld32(taddr + c * 32, da);
+      if (!row_ok) continue;
+      const int64_t rem = g.N - j0;
+      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const uint16_t* gp = p.g + row * p.ld_gu + j0;
+      const uint16_t* up = p.u + row * p.ld_gu + j0;
+      uint16_t* dgp = p.dgu + row * p.ld_dgu + j0;
+      uint16_t* dup = dgp + p.du_off;
+      if (nv == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 g4 = reinterpret_cast<const uint4*>(gp)[q];
+          const uint4 u4 = reinterpret_cast<const uint4*>(up)[q];
+          const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+          const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+          uint32_t og[4], ou[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float dgv[2], duv[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float gx = __uint_as_float(h ? (gw[e] & 0xFFFF0000u)
+                                                 : (gw[e] << 16));
+              const float ux = __uint_as_float(h ? (uw[e] & 0xFFFF0000u)
+                                                 : (uw[e] << 16));
+              const float sg = sigmoid_fast(gx);
+              const float d = da[8 * q + 2 * e + h];
+              duv[h] = d * gx * sg;
+              dgv[h] = d * ux * sg * (1.f + gx * (1.f - sg));
+            }
+            og[e] = pack_bf16x2(dgv[0], dgv[1]);
+            ou[e] = pack_bf16x2(duv[0], duv[1]);
+          }
+          reinterpret_cast<uint4*>(dgp)[q] = make_uint4(og[0], og[1], og[2], og[3]);
+          reinterpret_cast<uint4*>(dup)[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= nv) continue;
+          const float gx = __uint_as_float(static_cast<uint32_t>(gp[i]) << 16);
+          const float ux = __uint_as_float(static_cast<uint32_t>(up[i]) << 16);
+          const float sg = sigmoid_fast(gx);
+          dup[i] = to_bf16_bits(da[i] * gx * sg);
+          dgp[i] = to_bf16_bits(da[i] * ux * sg * (1.f + gx * (1.f - sg)));
         }
       }
     }
@@ -661,6 +808,7 @@ struct SmemMap {
 template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
                                               const CUtensorMap* tb,
+                                              const CUtensorMap* tb2,
                                               const GemmGeom& g,
                                               const SmemMap& sm,
                                               const WaitCtx& ctx) {
@@ -690,13 +838,22 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
         } else {
           tma_load_op(sa, ta, k0, m0, fb, g.a_hint, pa);
         }
+        // B from the second map past the K split (dual along K)
+        const bool second = g.b_dual == 2 && kb >= g.k_split_kb;
+        const CUtensorMap* tbk = second ? tb2 : tb;
+        const int kq = second ? k0 - g.k_split_kb * BK : k0;
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_op(sb + j * 64 * BK * 2, tb, n0 + 64 * j, k0, fb,
+            tma_load_op(sb + j * 64 * BK * 2, tbk, n0 + 64 * j, kq, fb,
                         g.b_hint, pb);
+        } else if (g.b_dual == 1) {
+          // dual along N: 128 rows of each map, same rows
+          const int nr = (t.n_first + tt) * (BN / 2);
+          tma_load_op(sb, tb, k0, nr, fb, g.b_hint, pb);
+          tma_load_op(sb + (BN / 2) * BK * 2, tb2, k0, nr, fb, g.b_hint, pb);
         } else {
-          tma_load_op(sb, tb, k0, n0, fb, g.b_hint, pb);
+          tma_load_op(sb, tbk, kq, n0, fb, g.b_hint, pb);
         }
         ++issued;
         if (++stage == STAGES) {
@@ -802,7 +959,8 @@ __device__ __forceinline__ void role_epilogue(const GemmGeom& g,
 template <class Epi, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap ta,
-           const __grid_constant__ CUtensorMap tb, const GemmGeom g,
+           const __grid_constant__ CUtensorMap tb,
+           const __grid_constant__ CUtensorMap tb2, const GemmGeom g,
            const typename Epi::Params p, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -834,6 +992,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&ta);
     tma_prefetch_desc(&tb);
+    if (g.b_dual) tma_prefetch_desc(&tb2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -846,7 +1005,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const WaitCtx ctx{abort_flag, err, g.timeout_ns};
 
   if (warp == 0) {
-    if (lane == 0) role_producer<A_MN, B_MN>(&ta, &tb, g, sm, ctx);
+    if (lane == 0) role_producer<A_MN, B_MN>(&ta, &tb, &tb2, g, sm, ctx);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) role_mma<A_MN, B_MN>(g, sm, tmem_base, ctx);
@@ -867,12 +1026,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <class Epi, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb,
                           const GemmGeom& g, const typename Epi::Params& p,
-                          unsigned* err, int grid, cudaStream_t s) {
+                          unsigned* err, int grid, cudaStream_t s,
+                          const CUtensorMap* tb2 = nullptr) {
   auto kern = k_gemm<Epi, A_MN, B_MN>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, g, p, err);
+  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, tb2 ? *tb2 : tb, g,
+                                                   p, err);
   return cudaGetLastError();
 }
 
@@ -1045,6 +1206,7 @@ struct SmemMap2 {
 template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
                                                    const CUtensorMap* tb,
+                                                   const CUtensorMap* tb2,
                                                    const GemmGeom& g,
                                                    const SmemMap2& sm,
                                                    uint32_t rank,
@@ -1058,8 +1220,12 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
     const int a0 = static_cast<int>(t.row0);  // this CTA's 128 rows of A
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
-      // this CTA's 128 of the tile's 256 output columns
-      const int b0 = (t.n_first + tt) * BN + static_cast<int>(rank) * BM;
+      // this CTA's 128 of the tile's 256 output columns; dual along N: the
+      // leader takes the first map's 128 rows, the peer the second's
+      const bool dual_n = g.b_dual == 1;
+      const int b0 = dual_n ? (t.n_first + tt) * BM
+                            : (t.n_first + tt) * BN + static_cast<int>(rank) * BM;
+      const CUtensorMap* tbn = (dual_n && rank == 1) ? tb2 : tb;
       for (int kb = 0; kb < g.num_kb; ++kb) {
         if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
           ok = false;
@@ -1078,13 +1244,16 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
         } else {
           tma_load_op_pair(sa, ta, k0, a0, fb, g.a_hint, pa);
         }
+        const bool second = g.b_dual == 2 && kb >= g.k_split_kb;
+        const CUtensorMap* tbk = second ? tb2 : tbn;
+        const int kq = second ? k0 - g.k_split_kb * BK : k0;
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_op_pair(sb + j * 64 * BK * 2, tb, b0 + 64 * j, k0, fb,
+            tma_load_op_pair(sb + j * 64 * BK * 2, tbk, b0 + 64 * j, kq, fb,
                              g.b_hint, pb);
         } else {
-          tma_load_op_pair(sb, tb, k0, b0, fb, g.b_hint, pb);
+          tma_load_op_pair(sb, tbk, kq, b0, fb, g.b_hint, pb);
         }
         ++issued;
         if (++stage == STAGES2) {
@@ -1194,7 +1363,8 @@ __device__ __forceinline__ void role_epilogue_pair(
 template <class Epi, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap ta,
-                const __grid_constant__ CUtensorMap tb, const GemmGeom g,
+                const __grid_constant__ CUtensorMap tb,
+                const __grid_constant__ CUtensorMap tb2, const GemmGeom g,
                 const typename Epi::Params p, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1227,6 +1397,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&ta);
     tma_prefetch_desc(&tb);
+    if (g.b_dual) tma_prefetch_desc(&tb2);
   }
   // Both CTAs' barriers exist before either CTA signals the other's.
   cluster_sync_all();
@@ -1241,7 +1412,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const WaitCtx ctx{abort_flag, err, g.timeout_ns};
 
   if (warp == 0) {
-    if (lane == 0) role_producer_pair<A_MN, B_MN>(&ta, &tb, g, sm, rank, ctx);
+    if (lane == 0)
+      role_producer_pair<A_MN, B_MN>(&ta, &tb, &tb2, g, sm, rank, ctx);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) role_mma_pair<A_MN, B_MN>(g, sm, tmem_base, ctx);
@@ -1267,7 +1439,8 @@ template <class Epi, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb,
                                const GemmGeom& g,
                                const typename Epi::Params& p, unsigned* err,
-                               int grid, cudaStream_t s) {
+                               int grid, cudaStream_t s,
+                               const CUtensorMap* tb2 = nullptr) {
   auto kern = k_gemm_pair<Epi, A_MN, B_MN>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM2_SMEM_BYTES);
@@ -1284,7 +1457,7 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, g, p, err);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2 ? *tb2 : tb, g, p, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

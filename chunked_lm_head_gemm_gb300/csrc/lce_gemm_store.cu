@@ -8,14 +8,17 @@ namespace lce {
 cudaError_t launch_gemm_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const GemmGeom& g,
                               const StoreParams& p, unsigned* err, int grid,
-                              cudaStream_t s) {
+                              cudaStream_t s, const CUtensorMap* tb2) {
   if (!a_mn && !b_mn)
-    return launch_gemm_t<EpiStore, false, false>(ta, tb, g, p, err, grid, s);
+    return launch_gemm_t<EpiStore, false, false>(ta, tb, g, p, err, grid, s,
+                                                 tb2);
   if (!a_mn && b_mn)
-    return launch_gemm_t<EpiStore, false, true>(ta, tb, g, p, err, grid, s);
+    return launch_gemm_t<EpiStore, false, true>(ta, tb, g, p, err, grid, s,
+                                                tb2);
   if (a_mn && !b_mn)
-    return launch_gemm_t<EpiStore, true, false>(ta, tb, g, p, err, grid, s);
-  return launch_gemm_t<EpiStore, true, true>(ta, tb, g, p, err, grid, s);
+    return launch_gemm_t<EpiStore, true, false>(ta, tb, g, p, err, grid, s,
+                                                tb2);
+  return launch_gemm_t<EpiStore, true, true>(ta, tb, g, p, err, grid, s, tb2);
 }
 
 cudaError_t pair_max_active_clusters(int* n) {
@@ -40,17 +43,19 @@ cudaError_t pair_max_active_clusters(int* n) {
 cudaError_t launch_gemm_pair_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
                                    const CUtensorMap& tb, const GemmGeom& g,
                                    const StoreParams& p, unsigned* err,
-                                   int grid, cudaStream_t s) {
+                                   int grid, cudaStream_t s,
+                                   const CUtensorMap* tb2) {
   if (!a_mn && !b_mn)
     return launch_gemm_pair_t<EpiStore, false, false>(ta, tb, g, p, err, grid,
-                                                      s);
+                                                      s, tb2);
   if (!a_mn && b_mn)
     return launch_gemm_pair_t<EpiStore, false, true>(ta, tb, g, p, err, grid,
-                                                     s);
+                                                     s, tb2);
   if (a_mn && !b_mn)
     return launch_gemm_pair_t<EpiStore, true, false>(ta, tb, g, p, err, grid,
-                                                     s);
-  return launch_gemm_pair_t<EpiStore, true, true>(ta, tb, g, p, err, grid, s);
+                                                     s, tb2);
+  return launch_gemm_pair_t<EpiStore, true, true>(ta, tb, g, p, err, grid, s,
+                                                  tb2);
 }
 
 }  // namespace lce

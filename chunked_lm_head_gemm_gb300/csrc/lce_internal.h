@@ -42,6 +42,12 @@ struct GemmGeom {
   // L2 eviction priority of each operand's TMA loads: 0 = default,
   // 1 = evict first (streamed), 2 = evict last (reused).
   int a_hint, b_hint;
+  // B from two tensor maps: 0 = one map; 1 = along N, each 256-row B tile
+  // being 128 rows of the first map then the same 128 rows of the second
+  // (tiles then cover 128 output columns, num_n = ceil(N / 128)); 2 = along
+  // K, k-blocks from k_split_kb on read the second map (at k - k_split_kb).
+  int b_dual;
+  int k_split_kb;
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------
@@ -80,10 +86,34 @@ struct FusedParams {
   int64_t ignore_index;
 };
 
+// Gated-MLP gate/up contraction (B dual along N): accumulator columns
+// 0..127 hold g, 128..255 hold u for output columns [128 n, 128 n + 128);
+// writes a = silu(g) * u and, when the pointers are set, g and u (bf16).
+struct SwigluParams {
+  uint16_t* a;            // [M][ld]
+  uint16_t* g;            // [M][ld] or NULL
+  uint16_t* u;            // [M][ld] or NULL
+  int64_t ld;
+};
+
+// Gated-MLP backward: the accumulator is da = dy Wd; with the saved g, u
+// writes dg = da u silu'(g) at [row][col] and du = da silu(g) at
+// [row][du_off + col] (bf16).
+struct SwigluBwdParams {
+  const uint16_t* g;      // [M][ld_gu]
+  const uint16_t* u;      // [M][ld_gu]
+  int64_t ld_gu;
+  uint16_t* dgu;          // [M][ld_dgu]
+  int64_t ld_dgu;
+  int64_t du_off;
+};
+
 // Plain store of scale * acc (dH chunk, or the building-block test GEMM).
 struct StoreParams {
   void* out;              // [M][ldo]
   int64_t ldo;
+  void* out2;             // rows >= split_row go to out2 (row - split_row),
+  int64_t split_row;      // when out2 is not NULL
   int out_f32;            // 1: fp32 output, 0: bf16 output
   int accumulate;         // 1: out += scale*acc (fp32 only), 0: out = scale*acc
   const float* dloss;     // scale = dloss[0] / n_valid[0] (n_valid 0 -> 0);
@@ -97,6 +127,18 @@ struct StoreParams {
 cudaError_t launch_gemm_lse(const CUtensorMap& ta, const CUtensorMap& tb,
                             const GemmGeom& g, const LseParams& p,
                             unsigned* err, int grid, cudaStream_t s);
+// The gated-MLP contractions (gate/up with the SwiGLU epilogue, and da
+// with the SwiGLU backward epilogue); tb2 is the second B map (b_dual).
+cudaError_t launch_gemm_swiglu(bool pair, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tb2,
+                               const GemmGeom& g, const SwigluParams& p,
+                               unsigned* err, int grid, cudaStream_t s);
+cudaError_t launch_gemm_swiglu_bwd(bool pair, const CUtensorMap& ta,
+                                   const CUtensorMap& tb,
+                                   const CUtensorMap& tb2, const GemmGeom& g,
+                                   const SwigluBwdParams& p, unsigned* err,
+                                   int grid, cudaStream_t s);
+
 cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
                              const GemmGeom& g, const GradParams& p,
                              unsigned* err, int grid, cudaStream_t s);
@@ -106,7 +148,8 @@ cudaError_t launch_gemm_fused(const CUtensorMap& ta, const CUtensorMap& tb,
 cudaError_t launch_gemm_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const GemmGeom& g,
                               const StoreParams& p, unsigned* err, int grid,
-                              cudaStream_t s);
+                              cudaStream_t s,
+                              const CUtensorMap* tb2 = nullptr);
 
 // The same four contractions on CTA pairs (cluster of 2, tcgen05
 // cta_group::2, 256 x 256 tiles): geometry in units of 256 rows, grid even,
@@ -124,7 +167,8 @@ cudaError_t launch_gemm_pair_fused(const CUtensorMap& ta,
 cudaError_t launch_gemm_pair_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
                                    const CUtensorMap& tb, const GemmGeom& g,
                                    const StoreParams& p, unsigned* err,
-                                   int grid, cudaStream_t s);
+                                   int grid, cudaStream_t s,
+                                   const CUtensorMap* tb2 = nullptr);
 
 // How many CTA pairs of the contraction kernels can be resident at once
 // (clusters are placed within a GPC, so this can be below SMs / 2).

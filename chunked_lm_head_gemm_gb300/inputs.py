@@ -135,3 +135,44 @@ def make_inputs(wl: Workload | str, seed: int = 0, device="cpu"):
     h = make_hidden(wl, seed, device)
     W = make_weight(wl, seed, device)
     return h, W, y.to(device)
+
+
+
+@dataclasses.dataclass(frozen=True)
+class MlpWorkload:
+    """A Qwen3 MLP (gate/up I x H, down H x I) over L rows, all bf16."""
+    name: str
+    L: int
+    H: int
+    I: int
+    x_scale: float = 1.0
+    w_std: float = 0.02
+
+    def with_rows(self, L: int) -> "MlpWorkload":
+        return dataclasses.replace(self, L=L, name=f"{self.name}[L={L}]")
+
+
+# Qwen3 MLP widths (hidden H -> intermediate I), one 1M-token sequence's
+# per-GPU shard of 131072 rows (1M over 8 GPUs)
+MLP_WORKLOADS = {
+    "qwen3-0.6b-mlp": MlpWorkload("qwen3-0.6b-mlp", 131072, 1024, 3072),
+    "qwen3-4b-mlp": MlpWorkload("qwen3-4b-mlp", 131072, 2560, 9728),
+    "qwen3-8b-mlp": MlpWorkload("qwen3-8b-mlp", 131072, 4096, 12288),
+    "qwen3-32b-mlp": MlpWorkload("qwen3-32b-mlp", 131072, 5120, 25600),
+}
+
+
+def make_mlp_inputs(wl: MlpWorkload, seed: int = 0, device="cpu"):
+    """Returns (x [L,H], Wg [I,H], Wu [I,H], Wd [H,I], dy [L,H]), bf16;
+    generators seed*1000 + 10..14."""
+    def draw(shape, k, std):
+        g = _gen(seed, k, device)
+        t = torch.empty(*shape, device=device, dtype=torch.float32)
+        t.normal_(0.0, std, generator=g)
+        return t.to(torch.bfloat16)
+    x = draw((wl.L, wl.H), 10, wl.x_scale)
+    Wg = draw((wl.I, wl.H), 11, wl.w_std)
+    Wu = draw((wl.I, wl.H), 12, wl.w_std)
+    Wd = draw((wl.H, wl.I), 13, wl.w_std)
+    dy = draw((wl.L, wl.H), 14, 1.0)
+    return x, Wg, Wu, Wd, dy

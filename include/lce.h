@@ -221,6 +221,38 @@ lce_status lce_forward_static(const void* h, const void* W,
                               float* lse, void* stream);
 
 /*
+ * Sequence-tiled gated MLP. Source: "Training Beyond 1M Tokens", section
+ * "One GPU is not enough: split the sequence across many": one MLP line of
+ * the model is down_proj(act_fn(gate_proj(x)) * up_proj(x)), and its four
+ * L x I intermediates are what fills the card at long sequence length. With
+ * act_fn = SiLU (the Qwen3 models' activation):
+ *   y = (silu(x Wg^T) * (x Wu^T)) Wd^T
+ * computed over row chunks, so the intermediates exist only for one chunk
+ * (workspace: 10 * chunk_rows * I bytes). The backward recomputes g, u and
+ * a per chunk.
+ *   x   device bf16 [L][H];  Wg, Wu device bf16 [I][H];  Wd device bf16 [H][I]
+ *   y   device bf16 [L][H] out;  dy device bf16 [L][H]
+ *   dx  device bf16 [L][H] out;  dWg, dWu fp32 [I][H] out;  dWd fp32 [H][I] out
+ *   H % 8 == 0, I % 64 == 0; chunk_rows 0 = the library's default.
+ * The gate and up projections run as one tensor-core contraction (each
+ * 256-row B tile is 128 rows of Wg and the same 128 rows of Wu) whose
+ * epilogue writes silu(g) * u; the backward's da = dy Wd contraction writes
+ * dg = da u silu'(g) and du = da silu(g); dx = [dg | du] [Wg ; Wu] is one
+ * K = 2I contraction; weight gradients accumulate in fp32 in chunk order.
+ */
+size_t lce_mlp_workspace_size(int64_t L, int64_t H, int64_t I,
+                              int64_t chunk_rows);
+lce_status lce_mlp_forward(const void* x, const void* Wg, const void* Wu,
+                           const void* Wd, int64_t L, int64_t H, int64_t I,
+                           int64_t chunk_rows, void* y, void* ws,
+                           size_t ws_bytes, void* stream);
+lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
+                            const void* Wd, const void* dy, int64_t L,
+                            int64_t H, int64_t I, int64_t chunk_rows,
+                            void* dx, float* dWg, float* dWu, float* dWd,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Selects how the tensor-core contractions run, for the whole process:
  * enable = 1: on CTA pairs (a cluster of two SMs issues tcgen05.mma with
  * cta_group::2 on 256 x 256 tiles, each SM staging half of each operand);
@@ -243,7 +275,7 @@ int lce_get_cta_pair(void);
  * per tensor-core contraction, 0 for the other kernels). Host-side state
  * only; events are created on first use and reused.
  */
-#define LCE_KERNEL_KINDS 13
+#define LCE_KERNEL_KINDS 19
 enum {
   LCE_K_COUNT_VALID = 0,
   LCE_K_GEMM_LSE = 1,
@@ -257,7 +289,13 @@ enum {
   LCE_K_WAIT_PROBE = 9,
   LCE_K_GEMM_FUSED = 10,
   LCE_K_GRAD_FROM_EXP = 11,
-  LCE_K_SCALE_GRADS = 12
+  LCE_K_SCALE_GRADS = 12,
+  LCE_K_MLP_GATE_UP = 13,
+  LCE_K_MLP_DOWN = 14,
+  LCE_K_MLP_DA = 15,
+  LCE_K_MLP_DX = 16,
+  LCE_K_MLP_DWD = 17,
+  LCE_K_MLP_DWGU = 18
 };
 
 typedef struct {

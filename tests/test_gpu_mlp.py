@@ -1,0 +1,95 @@
+"""The sequence-tiled gated MLP on the GPU against its float64 oracle:
+y = (silu(x Wg^T) * (x Wu^T)) Wd^T and its backward, over row chunks, on
+single-CTA and CTA-pair contractions."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_lm_head_gemm_gb300.inputs import (MLP_WORKLOADS, MlpWorkload,
+                                               make_mlp_inputs)
+from tests.gpu_util import PAIRS, cta_pair, rel_fro, require_gpu, to64
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2  # relative Frobenius error, bf16 operands and intermediates
+
+
+def _run(x, Wg, Wu, Wd, dy, chunk):
+    import chunked_lm_head_gemm_gb300 as lce
+    y = lce.mlp_forward(x, Wg, Wu, Wd, chunk)
+    dx, dWg, dWu, dWd = lce.mlp_backward(x, Wg, Wu, Wd, dy, chunk)
+    assert lce.get_error() == 0
+    return dict(y=to64(y), dx=to64(dx), dWg=to64(dWg), dWu=to64(dWu),
+                dWd=to64(dWd))
+
+
+def _compare(gpu, ref):
+    for k in ("y", "dx", "dWg", "dWu", "dWd"):
+        e = rel_fro(gpu[k], ref[k])
+        assert e <= TOL, f"{k} rel Frobenius err {e}"
+
+
+SHAPES = [
+    # name, L, H, I, chunk, x_scale, w_std
+    ("tiny", 200, 64, 128, 0, 1.0, 0.1),
+    ("ragged", 333, 136, 192, 128, 1.0, 0.1),
+    ("one_row", 1, 8, 64, 0, 1.0, 0.3),
+    ("chunk_100", 300, 256, 320, 100, 1.0, 0.05),
+    ("multi_tile", 700, 512, 1024, 256, 1.0, 0.03),
+]
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("name,L,H,I,chunk,xs,ws", SHAPES,
+                         ids=[s_[0] for s_ in SHAPES])
+def test_mlp_against_oracle(name, L, H, I, chunk, xs, ws, pair):
+    dev = require_gpu()
+    wl = MlpWorkload(name, L, H, I, xs, ws)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=1, device=dev)
+    with cta_pair(pair):
+        gpu = _run(x, Wg, Wu, Wd, dy, chunk)
+    ref = oracle.mlp(x.cpu(), Wg.cpu(), Wu.cpu(), Wd.cpu(), dy.cpu())
+    _compare(gpu, ref)
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("name", ["qwen3-4b-mlp", "qwen3-8b-mlp"])
+def test_mlp_row_slice_of_qwen3_shape(name, pair):
+    """256 rows at the Qwen3 MLP widths (H, I), the oracle on all of it."""
+    dev = require_gpu()
+    wl = MLP_WORKLOADS[name].with_rows(256)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=0, device=dev)
+    with cta_pair(pair):
+        gpu = _run(x, Wg, Wu, Wd, dy, 0)
+    ref = oracle.mlp(x.cpu(), Wg.cpu(), Wu.cpu(), Wd.cpu(), dy.cpu())
+    _compare(gpu, ref)
+
+
+def test_mlp_chunking_and_determinism():
+    """Rows do not depend on the chunking (y, dx bitwise); weight gradients
+    only through fp32 summation order; reruns are bitwise identical."""
+    dev = require_gpu()
+    wl = MlpWorkload("det", 1536, 256, 512, 1.0, 0.05)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=3, device=dev)
+    a = _run(x, Wg, Wu, Wd, dy, 0)
+    b = _run(x, Wg, Wu, Wd, dy, 0)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    c = _run(x, Wg, Wu, Wd, dy, 512)
+    assert np.array_equal(a["y"], c["y"]) and np.array_equal(a["dx"], c["dx"])
+    for k in ("dWg", "dWu", "dWd"):
+        assert rel_fro(c[k], a[k]) < 1e-5, k
+
+
+def test_mlp_bad_arguments():
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    wl = MlpWorkload("bad", 64, 64, 96, 1.0, 0.1)  # I not a multiple of 64
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=0, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    with pytest.raises(lce.LCEError) as ei:
+        lce.mlp_forward(x, Wg, Wu, Wd, workspace=ws)
+    assert ei.value.status == B.LCE_ERR_INVALID_ARG
+    assert lce.get_error() == 0
