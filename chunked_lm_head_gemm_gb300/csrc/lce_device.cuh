@@ -722,30 +722,47 @@ struct EpiSwiGLUBwd {
     row_ok = row < g.M;
   }
 
+  // g and u of one 32-column chunk: 4 x 16-byte vectors each
+  struct GU {
+    uint4 g[4], u[4];
+  };
+
+  __device__ __forceinline__ void load_gu(const Params& p, int64_t j0,
+                                          GU& b) const {
+    const uint4* gp = reinterpret_cast<const uint4*>(p.g + row * p.ld_gu + j0);
+    const uint4* up = reinterpret_cast<const uint4*>(p.u + row * p.ld_gu + j0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      b.g[q] = gp[q];
+      b.u[q] = up[q];
+    }
+  }
+
+  // Whole 32-column chunks have their g and u loaded one chunk ahead, so
+  // the loads overlap the previous chunk's arithmetic and TMEM load.
   __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
                                        const Unit&, int n_blk, uint32_t taddr,
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+    GU nxt;
+    if (row_ok && n0 + 32 <= g.N) load_gu(p, n0, nxt);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int64_t j0 = n0 + c * 32;
       if (j0 >= g.N) break;
+      const GU cur = nxt;
+      const bool full = j0 + 32 <= g.N;
+      if (row_ok && c + 1 < BN / 32 && j0 + 64 <= g.N) load_gu(p, j0 + 32, nxt);
       float da[32];
       tmem_ld32(taddr + c * 32, da);
       if (!row_ok) continue;
-      const int64_t rem = g.N - j0;
-      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
-      const uint16_t* gp = p.g + row * p.ld_gu + j0;
-      const uint16_t* up = p.u + row * p.ld_gu + j0;
       uint16_t* dgp = p.dgu + row * p.ld_dgu + j0;
       uint16_t* dup = dgp + p.du_off;
-      if (nv == 32) {
+      if (full) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 g4 = reinterpret_cast<const uint4*>(gp)[q];
-          const uint4 u4 = reinterpret_cast<const uint4*>(up)[q];
-          const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-          const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+          const uint32_t gw[4] = {cur.g[q].x, cur.g[q].y, cur.g[q].z, cur.g[q].w};
+          const uint32_t uw[4] = {cur.u[q].x, cur.u[q].y, cur.u[q].z, cur.u[q].w};
           uint32_t og[4], ou[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -768,6 +785,9 @@ struct EpiSwiGLUBwd {
           reinterpret_cast<uint4*>(dup)[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
         }
       } else {
+        const int nv = static_cast<int>(g.N - j0);
+        const uint16_t* gp = p.g + row * p.ld_gu + j0;
+        const uint16_t* up = p.u + row * p.ld_gu + j0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (i >= nv) continue;
