@@ -196,7 +196,7 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* tile_max, int64_t num_n,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
-                                 cudaStream_t s);
+                                 int num_sms, cudaStream_t s);
 // dH *= dloss[0] (bf16 or fp32) and dW *= dloss[0], skipped when dloss is 1.
 cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
                                int64_t n_dw, const float* dloss,

@@ -161,39 +161,51 @@ __device__ __forceinline__ uint4 exp_to_grad(uint4 in, float sc, int yo) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// One block per row (grid-stride over rows); each thread keeps four
-// 16-byte vectors in flight.
-__global__ void __launch_bounds__(256)
+// The chunk's rows x ceil(V/8) 16-byte vectors are cut into one contiguous
+// range per block (so every block moves the same bytes, whatever the row
+// count), walked row segment by row segment; each thread keeps GFE_U vectors
+// in flight. Rows that do not take part are zeroed without being read.
+constexpr int GFE_THREADS = 256;
+constexpr int GFE_BLOCKS_PER_SM = 4;
+constexpr int GFE_U = 8;
+
+__global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
     k_grad_from_exp(uint16_t* __restrict__ E, int64_t ldg,
                     const float* __restrict__ tile_max, int64_t num_n,
                     const float* __restrict__ lse,
                     const int64_t* __restrict__ labels, int64_t rows,
                     int64_t V, int64_t ignore_index) {
   const int64_t nvec = (V + 7) / 8;
-  constexpr int U = 4;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  const int64_t total = rows * nvec;
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  int64_t pos = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t end = pos + per < total ? pos + per : total;
+  while (pos < end) {
+    const int64_t row = pos / nvec;
+    const int64_t vb = pos - row * nvec;
+    const int64_t ve = (end - pos < nvec - vb) ? vb + (end - pos) : nvec;
+    pos += ve - vb;
     const int64_t y = labels[row];
-    const bool valid = label_valid(y, V, ignore_index);
     uint4* er = reinterpret_cast<uint4*>(E + row * ldg);
-    if (!valid) {
-      for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x)
+    if (!label_valid(y, V, ignore_index)) {
+      for (int64_t v = vb + threadIdx.x; v < ve; v += GFE_THREADS)
         er[v] = make_uint4(0u, 0u, 0u, 0u);
       continue;
     }
     const float l2 = lse[row] * LOG2E;
     const float* tm = tile_max + row * num_n;
-    for (int64_t v0 = threadIdx.x; v0 < nvec;
-         v0 += static_cast<int64_t>(U) * blockDim.x) {
-      uint4 in[U];
+    for (int64_t v0 = vb + threadIdx.x; v0 < ve;
+         v0 += static_cast<int64_t>(GFE_U) * GFE_THREADS) {
+      uint4 in[GFE_U];
 #pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
-        if (v < nvec) in[k] = er[v];
+      for (int k = 0; k < GFE_U; ++k) {
+        const int64_t v = v0 + static_cast<int64_t>(k) * GFE_THREADS;
+        if (v < ve) in[k] = er[v];
       }
 #pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
-        if (v < nvec) {
+      for (int k = 0; k < GFE_U; ++k) {
+        const int64_t v = v0 + static_cast<int64_t>(k) * GFE_THREADS;
+        if (v < ve) {
           const int64_t j0 = v * 8;
           er[v] = exp_to_grad(in[k], ex2(tm[j0 >> 8] - l2),
                               static_cast<int>(y - j0));
@@ -207,11 +219,15 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* tile_max, int64_t num_n,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
-                                 cudaStream_t s) {
+                                 int num_sms, cudaStream_t s) {
+  const int64_t work = rows * ((V + 7) / 8);
+  const int64_t full = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) *
+                       GFE_BLOCKS_PER_SM;
+  const int64_t want = (work + GFE_THREADS - 1) / GFE_THREADS;
   const unsigned grid =
-      static_cast<unsigned>(rows < 1048576 ? (rows < 1 ? 1 : rows) : 1048576);
-  k_grad_from_exp<<<grid, 256, 0, s>>>(E, ldg, tile_max, num_n, lse, labels,
-                                       rows, V, ignore_index);
+      static_cast<unsigned>(want < full ? (want < 1 ? 1 : want) : full);
+  k_grad_from_exp<<<grid, GFE_THREADS, 0, s>>>(E, ldg, tile_max, num_n, lse,
+                                               labels, rows, V, ignore_index);
   return cudaGetLastError();
 }
 
