@@ -14,17 +14,20 @@ include/lce.h; this package is the thin Python binding.
     loss, lse, dH, dW = lce.forward_backward(h, W, labels)  # no recompute
     y = lce.mlp_forward(x, Wg, Wu, Wd)          # sequence-tiled gated MLP
     dx, dWg, dWu, dWd = lce.mlp_backward(x, Wg, Wu, Wd, dy)
+    from chunked_lm_head_gemm_gb300 import sharded   # rows split over ranks
+    loss, lse, dH, dW = sharded.forward_backward(h, W, labels, group)
 """
 from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
-                       alloc_workspace, backward, default_chunk_rows, forward,
-                       forward_backward, get_error, library_path,
-                       linear_cross_entropy, load, mlp_backward, mlp_forward,
-                       mlp_workspace_size, profile_start, profile_stop,
-                       scale_gradients, workspace_size)
+                       alloc_workspace, backward, count_valid,
+                       default_chunk_rows, forward, forward_backward,
+                       get_error, library_path, linear_cross_entropy, load,
+                       mlp_backward, mlp_forward, mlp_workspace_size,
+                       profile_start, profile_stop, scale_gradients,
+                       workspace_size)
 
 __all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "alloc_workspace",
-           "backward", "default_chunk_rows", "forward", "forward_backward",
-           "get_error", "library_path", "linear_cross_entropy", "load",
-           "mlp_backward", "mlp_forward", "mlp_workspace_size",
-           "profile_start", "profile_stop", "scale_gradients",
-           "workspace_size"]
+           "backward", "count_valid", "default_chunk_rows", "forward",
+           "forward_backward", "get_error", "library_path",
+           "linear_cross_entropy", "load", "mlp_backward", "mlp_forward",
+           "mlp_workspace_size", "profile_start", "profile_stop",
+           "scale_gradients", "workspace_size"]

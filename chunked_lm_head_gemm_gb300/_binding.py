@@ -37,7 +37,7 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_profile_start", "lce_profile_stop", "lce_forward_static",
             "lce_forward_backward", "lce_scale_gradients",
             "lce_set_cta_pair", "lce_get_cta_pair", "lce_mlp_workspace_size",
-            "lce_mlp_forward", "lce_mlp_backward")
+            "lce_mlp_forward", "lce_mlp_backward", "lce_count_valid")
 
 KERNEL_KINDS = 19
 
@@ -102,6 +102,8 @@ def load(build_if_missing: bool = False):
         lib.lce_forward_backward.restype = i32
         lib.lce_scale_gradients.argtypes = [p, i32, i64, i64, p, i64, p, p]
         lib.lce_scale_gradients.restype = i32
+        lib.lce_count_valid.argtypes = [p, i64, i64, i64, p, p]
+        lib.lce_count_valid.restype = i32
         lib.lce_mlp_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.lce_mlp_workspace_size.restype = sz
         lib.lce_mlp_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p,
@@ -260,6 +262,22 @@ def scale_gradients(dH: torch.Tensor, dW: torch.Tensor, dloss: torch.Tensor):
                                     _stream_ptr(dH.device))
     _check(st, "lce_scale_gradients")
     return dH, dW
+
+
+def count_valid(labels: torch.Tensor, V: int,
+                ignore_index: int = IGNORE_INDEX, out=None) -> torch.Tensor:
+    """Device int64 [1]: rows whose label is not ignore_index and lies in
+    [0, V) (the N of the mean loss); no host synchronisation."""
+    if labels.dtype != torch.int64 or labels.dim() != 1 or not labels.is_cuda:
+        raise ValueError("labels must be a 1-D int64 CUDA tensor")
+    labels = labels.contiguous()
+    if out is None:
+        out = torch.empty(1, dtype=torch.int64, device=labels.device)
+    st = load().lce_count_valid(labels.data_ptr(), labels.numel(), V,
+                                ignore_index, out.data_ptr(),
+                                _stream_ptr(labels.device))
+    _check(st, "lce_count_valid")
+    return out
 
 
 def get_error(device=None) -> int:

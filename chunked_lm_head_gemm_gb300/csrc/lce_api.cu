@@ -875,7 +875,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
     {
       ProfScope ps(LCE_K_GRAD_FROM_EXP, s);
       e = launch_grad_from_exp(E, w.ldg, tile_max, num_n, lse + c0,
-                               labels + c0, cr, V, ignore_index, s);
+                               labels + c0, cr, V, ignore_index, dev->num_sms,
+                               s);
       ps.done(0);
       if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
     }
@@ -943,6 +944,29 @@ lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                      dloss, s);
   ps.done(0);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "scale_grads");
+}
+
+lce_status lce_count_valid(const int64_t* labels, int64_t L, int64_t V,
+                           int64_t ignore_index, int64_t* n_valid,
+                           void* stream) {
+  if (!n_valid || (L > 0 && !labels) || L < 0 || V < 1) return LCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(n_valid) & 7u))
+    return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* n = reinterpret_cast<unsigned long long*>(n_valid);
+  cudaError_t e;
+  if (L == 0) {
+    e = cudaMemsetAsync(n, 0, sizeof(unsigned long long), s);
+  } else {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V, ignore_index, n, dev->err, s);
+    ps.done(0);
+  }
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "count_valid");
 }
 
 // ---- sequence-tiled gated MLP ----------------------------------------------

@@ -1,0 +1,85 @@
+"""The loss of a sequence whose rows are split over the processes of a group.
+
+Context parallelism gives each GPU one slice of a long sequence ("Training
+Beyond 1M Tokens", section "One GPU is not enough: split the sequence across
+many"); the LM-head loss then runs on each slice's rows. The loss of the
+whole sequence is the mean over ALL its valid rows, so the shards' own means
+cannot simply be averaged: with S_r the sum of the loss terms of shard r and
+N_r its valid rows (TRL PR #6845, "TRL: document 1M-token training and add a
+context-parallelism example", table "Assumptions", names an evaluation loss
+that comes out scaled by the number of shards when this is missed),
+
+    loss  = sum_r S_r / N,        N = sum_r N_r, S_r = N_r loss_r
+    dH_r  = (dloss N_r / N) dH'_r             stays on its shard
+    dW    = sum_r (dloss N_r / N) dW'_r
+
+where loss_r, dH'_r, dW'_r are the shard's own mean loss and its gradients.
+The exchange is one all-reduce of two float64 scalars and one sum of the
+V x H fp32 weight gradient. Every loss and gradient value comes from the
+library's kernels; this module only weighs and sums them across the group.
+With no group (or a group of one) it reduces to the single-process call.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+def _world(group) -> int:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return 1
+    return dist.get_world_size(group)
+
+
+def combine_loss(loss_local: torch.Tensor, n_local: torch.Tensor,
+                 group=None):
+    """(loss, weight) of the whole sequence from one shard's mean loss and
+    valid-row count: loss = sum_r N_r loss_r / sum_r N_r and weight =
+    N_r / sum_r N_r, both 0 when no row of any shard is valid. One
+    all-reduce (sum) of two float64 scalars over `group`; no host sync."""
+    n = n_local.reshape(()).to(torch.float64)
+    t = torch.stack([loss_local.reshape(()).to(torch.float64) * n, n])
+    if _world(group) > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    total = t[1]
+    safe = torch.where(total > 0, total, torch.ones_like(total))
+    zero = torch.zeros_like(total)
+    loss = torch.where(total > 0, t[0] / safe, zero)
+    weight = torch.where(total > 0, n / safe, zero)
+    return loss.to(torch.float32), weight
+
+
+def sum_weight_grad(dW: torch.Tensor, group=None) -> torch.Tensor:
+    """dW summed in place over the group (fp32, fixed by the backend's
+    reduction order)."""
+    if _world(group) > 1:
+        import torch.distributed as dist
+        dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=group)
+    return dW
+
+
+def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
+                     group=None, dloss: torch.Tensor | None = None,
+                     ignore_index: int = B.IGNORE_INDEX, chunk_rows: int = 0,
+                     workspace=None):
+    """This shard's rows of one sequence: returns (loss, lse, dH, dW) where
+    loss is the whole sequence's mean loss (identical on every process), lse
+    and dH are this shard's rows, and dW is the weight gradient of the whole
+    sequence (summed over the group). dloss defaults to 1."""
+    V = W.shape[0]
+    loss_r, lse, dH, dW = B.forward_backward(h, W, labels,
+                                             ignore_index=ignore_index,
+                                             chunk_rows=chunk_rows,
+                                             workspace=workspace)
+    n_r = B.count_valid(labels, V, ignore_index)
+    loss, weight = combine_loss(loss_r, n_r, group)
+    scale = weight.to(torch.float32)
+    if dloss is not None:
+        scale = scale * dloss.reshape(()).to(device=scale.device,
+                                             dtype=torch.float32)
+    B.scale_gradients(dH, dW, scale)
+    sum_weight_grad(dW, group)
+    return loss, lse, dH, dW

@@ -159,6 +159,25 @@ lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                void* stream);
 
 /*
+ * Count of rows that take part in the loss: n_valid[0] = #{i : labels[i] !=
+ * ignore_index and 0 <= labels[i] < V}. A label that is neither raises
+ * LCE_ERR_LABEL_RANGE in the device error word and is not counted, as in
+ * lce_forward. This is the N of the mean. When a sequence's rows are split
+ * over several processes, as context parallelism splits them ("Training
+ * Beyond 1M Tokens", section "One GPU is not enough: split the sequence
+ * across many"), the sequence's loss is sum_r N_r loss_r / sum_r N_r over the
+ * processes r, not the average of their losses; this call gives each N_r.
+ *   labels   device, [L] int64, 8-byte aligned (may be NULL when L = 0)
+ *   L        rows, >= 0; V >= 1
+ *   n_valid  device, [1] int64 out, 8-byte aligned
+ * Queues a memset and (for L > 0) one kernel on `stream`; argument errors
+ * return before anything is queued.
+ */
+lce_status lce_count_valid(const int64_t* labels, int64_t L, int64_t V,
+                           int64_t ignore_index, int64_t* n_valid,
+                           void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device. Returns LCE_ERR_TIMEOUT or LCE_ERR_LABEL_RANGE if a kernel
  * raised one since the last call (timeout first), LCE_ERR_CUDA if the

@@ -90,6 +90,12 @@ def test_bad_arguments_return_before_any_device_call(lib):
     # negative chunk
     assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, -5, p, p, p,
                             1 << 30, null) == 1
+    # label count: null output, misaligned labels, negative L, V < 1
+    assert lib.lce_count_valid(p, 8, 8, -100, null, null) == 1
+    assert lib.lce_count_valid(ctypes.c_void_p(0x1004), 8, 8, -100, p,
+                               null) == 1
+    assert lib.lce_count_valid(p, -1, 8, -100, p, null) == 1
+    assert lib.lce_count_valid(p, 8, 0, -100, p, null) == 1
     # test hooks
     assert lib.lce_test_gemm(null, p, p, 8, 8, 8, 0, 0, null) == 1
     assert lib.lce_test_gemm(p, p, p, 8, 12, 8, 0, 0, null) == 1

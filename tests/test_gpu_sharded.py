@@ -1,0 +1,107 @@
+"""Row-sharded loss on the GPU, the shards run one after another on one
+device: each shard's lce_forward_backward and lce_count_valid, weighed by
+N_r / N and summed on the host, must give the whole sequence's loss and
+gradients ("Training Beyond 1M Tokens", section "One GPU is not enough:
+split the sequence across many"). Also the valid-row count against the
+oracle, bit for bit."""
+import pytest
+import torch
+
+import oracle
+import chunked_lm_head_gemm_gb300 as lce
+from chunked_lm_head_gemm_gb300 import _binding as B
+from chunked_lm_head_gemm_gb300 import sharded
+from chunked_lm_head_gemm_gb300.inputs import Workload, make_inputs
+from tests.gpu_util import (GRAD_RFRO, LOSS_RTOL, PAIRS, cta_pair, rel_fro,
+                            require_gpu, to64)
+
+pytestmark = pytest.mark.gpu
+
+WL = Workload("shards", 1024, 256, 4096, "bf16", 1.0, 0.05, "uniform",
+              ignore_frac=0.2)
+# ragged shard boundaries (not multiples of the 128-row tile)
+BOUNDS = [0, 300, 800, 1024]
+
+
+@pytest.mark.parametrize("case", ["mixed", "ignored_head"])
+def test_count_valid_matches_oracle(case):
+    dev = require_gpu()
+    _, _, y = make_inputs(WL, seed=3, device=dev)
+    if case == "ignored_head":
+        y[:500] = -100
+    n = B.count_valid(y, WL.V)
+    ref, bad = oracle.count_valid(y.cpu(), WL.V)
+    assert B.get_error() == 0 and not bad
+    assert int(n.item()) == ref
+    # an empty label vector counts zero
+    empty = torch.empty(0, dtype=torch.int64, device=dev)
+    assert int(B.count_valid(empty, WL.V).item()) == 0
+
+
+def test_count_valid_label_out_of_range():
+    dev = require_gpu()
+    y = torch.tensor([0, 5, -100, 7, 99, -3], dtype=torch.int64, device=dev)
+    n = B.count_valid(y, 8)
+    assert B.get_error() == B.LCE_ERR_LABEL_RANGE
+    assert int(n.item()) == 3          # 0, 5, 7; 99 and -3 are out of range
+    assert oracle.count_valid(y.cpu(), 8) == (3, True)
+    assert B.get_error() == 0          # the error word was cleared
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+def test_sequential_shards_equal_whole_sequence(pair):
+    dev = require_gpu()
+    h, W, y = make_inputs(WL, seed=5, device=dev)
+    dloss = 0.5
+    with cta_pair(pair):
+        parts = []
+        for r0, r1 in zip(BOUNDS[:-1], BOUNDS[1:]):
+            loss_r, lse_r, dH_r, dW_r = lce.forward_backward(
+                h[r0:r1].contiguous(), W, y[r0:r1].contiguous())
+            n_r = B.count_valid(y[r0:r1].contiguous(), WL.V)
+            parts.append((loss_r, lse_r, dH_r, dW_r, n_r))
+        # the host-side combine: loss = sum N_r loss_r / N, weight N_r / N
+        n_tot = sum(p[4].to(torch.float64) for p in parts)
+        loss = sum(p[0].to(torch.float64) * p[4].to(torch.float64)
+                   for p in parts) / n_tot
+        dW = torch.zeros(WL.V, WL.H, dtype=torch.float32, device=dev)
+        dH = []
+        for loss_r, lse_r, dH_r, dW_r, n_r in parts:
+            scale = (n_r.to(torch.float64) / n_tot * dloss).to(torch.float32)
+            lce.scale_gradients(dH_r, dW_r, scale)
+            dH.append(dH_r)
+            dW += dW_r
+        dH = torch.cat(dH)
+        lse = torch.cat([p[1] for p in parts])
+        assert lce.get_error() == 0
+
+        whole = lce.forward_backward(h, W, y)
+        lce.scale_gradients(whole[2], whole[3],
+                            torch.full((), dloss, device=dev))
+    # GPU shards vs GPU whole: same kernels, other tiling and one more bf16
+    # rounding of dH after the weight
+    assert abs(loss.item() - whole[0].item()) <= 1e-5 * abs(whole[0].item())
+    # rows are independent; only the vocabulary split of the sum may differ
+    assert torch.max(torch.abs(lse - whole[1])).item() <= 1e-5
+    assert rel_fro(to64(dH), to64(whole[2])) <= 4e-3
+    assert rel_fro(to64(dW), to64(whole[3])) <= 1e-3
+
+    # and against the float64 oracle on the whole sequence
+    hc, Wc, yc = h.cpu(), W.cpu(), y.cpu()
+    f = oracle.forward(hc, Wc, yc)
+    b = oracle.backward(hc, Wc, yc, dloss=dloss)
+    assert abs(loss.item() - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert rel_fro(to64(dH), b["dH"]) <= GRAD_RFRO
+    assert rel_fro(to64(dW), b["dW"]) <= GRAD_RFRO
+
+
+def test_sharded_call_without_group_is_the_single_call():
+    dev = require_gpu()
+    h, W, y = make_inputs(WL, seed=6, device=dev)
+    d = torch.full((), 0.25, device=dev)
+    loss, lse, dH, dW = sharded.forward_backward(h, W, y, dloss=d)
+    ref = lce.forward_backward(h, W, y)
+    lce.scale_gradients(ref[2], ref[3], d)
+    assert lce.get_error() == 0
+    assert torch.equal(loss, ref[0]) and torch.equal(lse, ref[1])
+    assert torch.equal(dH, ref[2]) and torch.equal(dW, ref[3])
