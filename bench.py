@@ -259,6 +259,53 @@ def run_reference(args, wl) -> dict:
 # the CUDA path
 # ---------------------------------------------------------------------------
 
+def time_torch_chunked(h, W, y, chunk_rows: int, steps: int,
+                       warmup: int) -> dict:
+    """Context only, never part of the library: the pages' own chunked
+    scheme ("Training Beyond 1M Tokens", section "The massive logits matrix:
+    chunk it") in eager PyTorch on the same GPU -- per chunk of rows, cuBLAS
+    bf16 logits, fp32 cross-entropy, autograd backward at once (no
+    recompute), dW accumulated in W's dtype by autograd."""
+    import torch
+    import torch.nn.functional as F
+    L = h.shape[0]
+    n = (y != -100).sum().clamp(min=1).to(torch.float32)
+    Wl = W.detach().requires_grad_(True)
+    dH = torch.empty_like(h)
+
+    def step():
+        Wl.grad = None
+        total = torch.zeros((), dtype=torch.float32, device=h.device)
+        for c0 in range(0, L, chunk_rows):
+            c1 = min(L, c0 + chunk_rows)
+            hc = h[c0:c1].detach().requires_grad_(True)
+            z = F.linear(hc, Wl).float()
+            lc = F.cross_entropy(z, y[c0:c1], ignore_index=-100,
+                                 reduction="sum") / n
+            lc.backward()
+            dH[c0:c1] = hc.grad
+            total += lc.detach()
+        return total
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    H, V = h.shape[1], W.shape[0]
+    return {"impl": "eager PyTorch, autograd per chunk (context only)",
+            "chunk_rows": chunk_rows, "ms_per_step": ms,
+            "tokens_per_s": L / (ms / 1e3),
+            "tflops_model": 6.0 * L * H * V / (ms / 1e3) / 1e12,
+            "steps": steps, "warmup": warmup}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -278,6 +325,9 @@ def main():
                          "-1 keeps the library default")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--comparator", type=int, default=0, metavar="ROWS",
+                    help="also time the pages' chunked scheme in eager "
+                         "PyTorch with ROWS-row chunks (context only)")
     args = ap.parse_args()
 
     if args.workload == "mlp":
@@ -391,11 +441,25 @@ def main():
         return tt.item(), stats, clk
 
     modes = {}
+    phases = {}
     if not args.only_mode:
         for m in steps:
             if m != args.mode:
                 ms, _, _ = timed(steps[m], False)
                 modes[m] = ms
+        # the separate path's two calls on their own: forward (logits pass,
+        # loss) and backward (recompute, dH, dW) from the forward's lse
+        def step_fwd():
+            lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
+
+        def step_bwd():
+            lce.backward(h, W, y, lse, dloss, chunk_rows=chunk, workspace=ws,
+                         dH_out=dH, dW_out=dW)
+        for name, fn in (("forward", step_fwd), ("backward", step_bwd)):
+            ms, _, _ = timed(fn, False)
+            phases[name] = {"ms": ms / args.steps,
+                            "tflops": 2.0 * (1 if name == "forward" else 3)
+                            * L * H * V / (ms / args.steps / 1e3) / 1e12}
     elapsed_ms, stats, clk = timed(step, True)
     modes[args.mode] = elapsed_ms
     t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -413,6 +477,8 @@ def main():
                      "tflops_model": 6.0 * L * H * V / (ms / args.steps / 1e3)
                      / 1e12}
                  for m, ms in modes.items()}
+    if phases and "separate" in modes_out:
+        modes_out["separate"]["phases"] = phases
 
     # dominant kernel: largest total event time in the timed region
     kernels = {}
@@ -552,6 +618,10 @@ def main():
                "sequential_value": seq_value, "sequential_wall_s": seq_wall}
         del h_host, W_host, dH_host, dW_host, bufs
 
+    comparator = None
+    if args.comparator:
+        comparator = time_torch_chunked(h, W, y, args.comparator, 2, 1)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = min(L, 512)
@@ -586,6 +656,8 @@ def main():
             "cpu_baseline": cpu,
             "peak_extra_bytes": int(ws.numel()),
         }
+        if comparator:
+            out["comparator"] = comparator
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
