@@ -10,6 +10,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <numeric>
 #include <string>
 #include <vector>
 
@@ -225,8 +226,9 @@ lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
 // Per contraction kind: the L2 eviction priority of each operand's loads and
 // the tile grouping of tile-per-unit contractions; plus the L2 budget that
 // bounds the live A row panels when choosing column splits. Defaults are the
-// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,l2mb=M" (kinds lse,
-// grad, fused, dH, dW, test; H in 0..2; G >= 0) overrides them.
+// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,kind.s=S,l2mb=M"
+// (kinds lse, grad, fused, dH, dW, test, mlp; H in 0..2; G >= 0; S >= 1, the
+// placement stride GemmGeom::cl_stride) overrides them.
 enum TuneKind {
   T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_KINDS
 };
@@ -234,6 +236,7 @@ struct Tune {
   int a_hint[T_KINDS];
   int b_hint[T_KINDS];
   int group_n[T_KINDS];
+  int cl_stride[T_KINDS];
   double l2_budget;
 };
 
@@ -269,6 +272,7 @@ const Tune& tune() {
         if (field == "a" && iv >= 0 && iv <= 2) v.a_hint[k] = iv;
         if (field == "b" && iv >= 0 && iv <= 2) v.b_hint[k] = iv;
         if (field == "g" && iv >= 0) v.group_n[k] = iv;
+        if (field == "s" && iv >= 1) v.cl_stride[k] = iv;
       }
     }
     return v;
@@ -327,6 +331,7 @@ GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps,
   g.timeout_ns = wait_timeout_ns();
   g.group_n = 0;
   g.a_hint = g.b_hint = 0;
+  g.cl_stride = 1;
   return g;
 }
 
@@ -397,6 +402,8 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   if (st != LCE_OK) return st;
   const int units = std::max(1, std::min(pl->g.num_units, slots));
   pl->grid = pl->pair ? 2 * units : units;
+  const int stride = tn.cl_stride[o.kind];
+  if (stride > 1 && std::gcd(stride, units) == 1) pl->g.cl_stride = stride;
   return LCE_OK;
 }
 

@@ -319,6 +319,19 @@ __device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u,
   return t;
 }
 
+// The first unit of CTA (or cluster) `slot` of `slots`: slot * cl_stride mod
+// slots (a permutation when cl_stride is coprime with slots; the host
+// ensures it), so the units that run at the same time can be placed on
+// other SMs than consecutive slots would give. Off (1) by default: a trial
+// with several strides changed neither the DRAM re-reads nor the time.
+__device__ __forceinline__ int first_unit(const GemmGeom& g, int slot,
+                                          int slots) {
+  return g.cl_stride > 1
+             ? static_cast<int>((static_cast<int64_t>(slot) * g.cl_stride) %
+                                slots)
+             : slot;
+}
+
 // ---------------------------------------------------------------------------
 // epilogues: one thread per accumulator row, 32 columns per TMEM load
 // ---------------------------------------------------------------------------
@@ -835,7 +848,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
   uint32_t stage = 0, phase = 0, issued = 0;
   const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     const int m0 = t.m_blk * BM;
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
@@ -899,7 +912,7 @@ __device__ __forceinline__ void role_mma(const GemmGeom& g, const SmemMap& sm,
   constexpr uint32_t MN_LBO = 64 * BK * 2;  // one 64-wide MN box: 8 KB
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
       if (!mbar_wait(sm.tempty(acc), acc_phase ^ 1u, ctx, true)) {
@@ -952,7 +965,7 @@ __device__ __forceinline__ void role_epilogue(const GemmGeom& g,
   const int r = q * 32 + lane;
   uint32_t acc = 0, acc_phase = 0;
   Epi epi;
-  for (int u = blockIdx.x; u < g.num_units; u += gridDim.x) {
+  for (int u = first_unit(g, blockIdx.x, gridDim.x); u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     epi.begin_unit(p, g, t, r);
     bool ok = true;
@@ -1232,7 +1245,8 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
                                                    uint32_t rank,
                                                    const WaitCtx& ctx) {
   const bool leader = rank == 0;
-  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
   uint32_t stage = 0, phase = 0, issued = 0;
   const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
@@ -1301,7 +1315,8 @@ __device__ __forceinline__ void role_mma_pair(const GemmGeom& g,
                                               const WaitCtx& ctx) {
   constexpr uint32_t IDESC = idesc_pair_bf16_f32<A_MN, B_MN>();
   constexpr uint32_t MN_LBO = 64 * BK * 2;
-  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
   for (int u = cluster; ok && u < g.num_units; u += nclusters) {
@@ -1352,7 +1367,8 @@ __device__ __forceinline__ void role_epilogue_pair(
     int lane) {
   const int q = warp & 3;
   const int r = q * 32 + lane;
-  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
   uint32_t acc = 0, acc_phase = 0;
   Epi epi;
   for (int u = cluster; u < g.num_units; u += nclusters) {

@@ -48,6 +48,9 @@ struct GemmGeom {
   // K, k-blocks from k_split_kb on read the second map (at k - k_split_kb).
   int b_dual;
   int k_split_kb;
+  // Placement: CTA (or cluster) i starts at unit (i * cl_stride) mod the
+  // grid's CTAs (clusters); 1 = in order. Coprime with that count.
+  int cl_stride;
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------
