@@ -259,6 +259,51 @@ def run_reference(args, wl) -> dict:
 # the CUDA path
 # ---------------------------------------------------------------------------
 
+def time_vocab_slice(lce, B, h, W, y, P: int, chunk: int, steps: int,
+                     warmup: int) -> dict:
+    """One process's share of a P-way vocabulary-parallel step: the forward
+    statistics of its V/P slice of the head, the merge of P slices'
+    statistics (this slice's, repeated: the merge reads P of them either
+    way), and the slice's backward. The all-gather and all-reduce between
+    processes are not part of it (one GPU)."""
+    import torch
+    L, H = h.shape
+    V = W.shape[0]
+    Vs = (V + P - 1) // P
+    Ws = W[:Vs]
+    ws = lce.alloc_workspace(L, H, Vs, h.dtype, chunk, h.device)
+    d = torch.ones(1, dtype=torch.float32, device=h.device)
+
+    def step():
+        m, s, zy = B.forward_slice(h, Ws, y, 0, V, workspace=ws)
+        st = torch.stack([m, s, zy]).unsqueeze(0).expand(P, 3, L)
+        loss, lse = B.combine_slices(st[:, 0].contiguous(),
+                                     st[:, 1].contiguous(),
+                                     st[:, 2].contiguous(), y, V)
+        B.backward_slice(h, Ws, y, lse, d, 0, V, chunk_rows=chunk,
+                         workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if lce.get_error() != 0:
+        raise RuntimeError("device error in the vocabulary-slice step")
+    ms = e0.elapsed_time(e1) / steps
+    return {"shards": P, "slice_rows": Vs, "ms_per_step_per_process": ms,
+            "tokens_per_s": L / (ms / 1e3),
+            "tflops_per_process_executed": 8.0 * L * H * Vs / (ms / 1e3)
+            / 1e12,
+            "note": "forward slice + merge + recomputing backward slice; "
+                    "collectives not timed"}
+
+
 def time_torch_chunked(h, W, y, chunk_rows: int, steps: int,
                        warmup: int) -> dict:
     """Context only, never part of the library: the pages' own chunked
@@ -325,6 +370,10 @@ def main():
                          "-1 keeps the library default")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--vocab-shards", type=int, default=0, metavar="P",
+                    help="also time one process's share of a P-way "
+                         "vocabulary-parallel step (its V/P slice; the "
+                         "collectives are not timed)")
     ap.add_argument("--comparator", type=int, default=0, metavar="ROWS",
                     help="also time the pages' chunked scheme in eager "
                          "PyTorch with ROWS-row chunks (context only)")
@@ -618,6 +667,11 @@ def main():
                "sequential_value": seq_value, "sequential_wall_s": seq_wall}
         del h_host, W_host, dH_host, dW_host, bufs
 
+    vocab_par = None
+    if args.vocab_shards > 1:
+        vocab_par = time_vocab_slice(lce, B, h, W, y, args.vocab_shards,
+                                     chunk, args.steps, args.warmup)
+
     comparator = None
     if args.comparator:
         comparator = time_torch_chunked(h, W, y, args.comparator, 2, 1)
@@ -658,6 +712,8 @@ def main():
         }
         if comparator:
             out["comparator"] = comparator
+        if vocab_par:
+            out["vocab_parallel"] = vocab_par
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -16,6 +16,10 @@ include/lce.h; this package is the thin Python binding.
     dx, dWg, dWu, dWd = lce.mlp_backward(x, Wg, Wu, Wd, dy)
     from chunked_lm_head_gemm_gb300 import sharded   # rows split over ranks
     loss, lse, dH, dW = sharded.forward_backward(h, W, labels, group)
+    from chunked_lm_head_gemm_gb300 import vocab_parallel as vp  # head split
+    loss, lse = vp.forward(h, W[v0:v0 + Vs], labels, v0, V, group)
+    dH, dW_slice = vp.backward(h, W[v0:v0 + Vs], labels, lse, dloss, v0, V,
+                               group)
 """
 from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
                        alloc_workspace, backward, count_valid,

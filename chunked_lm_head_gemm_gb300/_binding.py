@@ -37,9 +37,11 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_profile_start", "lce_profile_stop", "lce_forward_static",
             "lce_forward_backward", "lce_scale_gradients",
             "lce_set_cta_pair", "lce_get_cta_pair", "lce_mlp_workspace_size",
-            "lce_mlp_forward", "lce_mlp_backward", "lce_count_valid")
+            "lce_mlp_forward", "lce_mlp_backward", "lce_count_valid",
+            "lce_forward_slice", "lce_combine_workspace_size",
+            "lce_combine_slices", "lce_backward_slice")
 
-KERNEL_KINDS = 19
+KERNEL_KINDS = 21
 
 
 class KernelStat(ctypes.Structure):
@@ -104,6 +106,18 @@ def load(build_if_missing: bool = False):
         lib.lce_scale_gradients.restype = i32
         lib.lce_count_valid.argtypes = [p, i64, i64, i64, p, p]
         lib.lce_count_valid.restype = i32
+        lib.lce_forward_slice.argtypes = [p, p, i32, p, i64, i64, i64, i64,
+                                          i64, i64, p, p, p, p, sz, p]
+        lib.lce_forward_slice.restype = i32
+        lib.lce_combine_workspace_size.argtypes = [i64]
+        lib.lce_combine_workspace_size.restype = sz
+        lib.lce_combine_slices.argtypes = [p, p, p, i64, p, i64, i64, i64, p,
+                                           p, p, sz, p]
+        lib.lce_combine_slices.restype = i32
+        lib.lce_backward_slice.argtypes = [p, p, i32, p, p, i64, i64, i64,
+                                           i64, i64, i64, p, i64, p, p, p, sz,
+                                           p]
+        lib.lce_backward_slice.restype = i32
         lib.lce_mlp_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.lce_mlp_workspace_size.restype = sz
         lib.lce_mlp_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p,
@@ -278,6 +292,90 @@ def count_valid(labels: torch.Tensor, V: int,
                                 _stream_ptr(labels.device))
     _check(st, "lce_count_valid")
     return out
+
+
+def forward_slice(h: torch.Tensor, W_slice: torch.Tensor,
+                  labels: torch.Tensor, v0: int, V_total: int,
+                  ignore_index: int = IGNORE_INDEX, workspace=None,
+                  out=None):
+    """One vocabulary slice (W_slice = rows v0 .. v0 + Vs - 1 of the head):
+    returns (m, s, zy), each float32 [L]: the slice's per-row max logit, sum
+    of exp(z - m), and label logit (0 where the label is elsewhere)."""
+    lib = load()
+    _check_inputs(h, W_slice, labels)
+    L, H = h.shape
+    Vs = W_slice.shape[0]
+    dev = h.device
+    if workspace is None:
+        workspace = alloc_workspace(L, H, Vs, h.dtype, 0, dev)
+    if out is None:
+        out = torch.empty(3, L, dtype=torch.float32, device=dev)
+    m, s, zy = out[0], out[1], out[2]
+    st = lib.lce_forward_slice(h.data_ptr(), W_slice.data_ptr(),
+                               _dtype_code(h), labels.data_ptr(), L, H, Vs,
+                               v0, V_total, ignore_index, m.data_ptr(),
+                               s.data_ptr(), zy.data_ptr(),
+                               workspace.data_ptr(), workspace.numel(),
+                               _stream_ptr(dev))
+    _check(st, "lce_forward_slice")
+    return m, s, zy
+
+
+def combine_slices(m: torch.Tensor, s: torch.Tensor, zy: torch.Tensor,
+                   labels: torch.Tensor, V_total: int,
+                   ignore_index: int = IGNORE_INDEX, workspace=None):
+    """m, s, zy: float32 [P, L] (every slice's forward_slice output, in the
+    same slice order on every process). Returns (loss, lse [L])."""
+    lib = load()
+    P, L = m.shape
+    for t in (m, s, zy):
+        if t.dtype != torch.float32 or t.shape != (P, L) or not t.is_cuda:
+            raise ValueError("m, s, zy must be CUDA float32 [P, L] tensors")
+    m, s, zy = m.contiguous(), s.contiguous(), zy.contiguous()
+    labels = labels.contiguous()
+    dev = m.device
+    if workspace is None:
+        workspace = torch.empty(lib.lce_combine_workspace_size(L),
+                                dtype=torch.uint8, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(L, dtype=torch.float32, device=dev)
+    st = lib.lce_combine_slices(m.data_ptr(), s.data_ptr(), zy.data_ptr(), P,
+                                labels.data_ptr(), L, V_total, ignore_index,
+                                loss.data_ptr(), lse.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(dev))
+    _check(st, "lce_combine_slices")
+    return loss, lse
+
+
+def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
+                   labels: torch.Tensor, lse: torch.Tensor,
+                   dloss: torch.Tensor, v0: int, V_total: int,
+                   ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
+                   workspace=None):
+    """One vocabulary slice's backward from the merged lse: returns
+    (dH_part [L,H] float32, whose sum over slices is dH; dW_slice [Vs,H])."""
+    lib = load()
+    _check_inputs(h, W_slice, labels)
+    L, H = h.shape
+    Vs = W_slice.shape[0]
+    dev = h.device
+    if lse.dtype != torch.float32 or lse.shape != (L,) or not lse.is_cuda:
+        raise ValueError("lse must be a CUDA float32 [L] tensor")
+    dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
+    if workspace is None:
+        workspace = alloc_workspace(L, H, Vs, h.dtype, chunk_rows, dev)
+    dH = torch.empty(L, H, dtype=torch.float32, device=dev)
+    dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
+    st = lib.lce_backward_slice(h.data_ptr(), W_slice.data_ptr(),
+                                _dtype_code(h), labels.data_ptr(),
+                                lse.data_ptr(), L, H, Vs, v0, V_total,
+                                ignore_index, dloss.data_ptr(), chunk_rows,
+                                dH.data_ptr(), dW.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(dev))
+    _check(st, "lce_backward_slice")
+    return dH, dW
 
 
 def get_error(device=None) -> int:

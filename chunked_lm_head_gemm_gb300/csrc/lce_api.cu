@@ -45,7 +45,8 @@ const char* const kKindNames[LCE_KERNEL_KINDS] = {
     "f32_to_bf16",  "gemm_grad",    "gemm_dH",       "gemm_dW",
     "test_gemm",    "wait_probe",   "gemm_fused",    "grad_from_exp",
     "scale_grads",  "mlp_gate_up",  "mlp_down",      "mlp_da",
-    "mlp_dx",       "mlp_dWd",      "mlp_dWgu"};
+    "mlp_dx",       "mlp_dWd",      "mlp_dWgu",      "slice_stats",
+    "combine_slices"};
 
 struct ProfRec {
   int kind;
@@ -434,6 +435,7 @@ cudaError_t run_store(const GemmPlan& pl, bool a_mn, bool b_mn,
 struct WsLayout {
   size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, tile_max,
       total;
+  size_t fwd_total;  // what the forward-only calls use: everything before G
   int64_t chunk, ldg;
 };
 
@@ -536,6 +538,7 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
   } else {
     w.h16 = w.w16 = 0;
   }
+  w.fwd_total = off;
   w.G = take(static_cast<size_t>(w.chunk) * w.ldg * 2);
   w.tile_max = take(static_cast<size_t>(w.chunk) * ceil_div(V, BN) * 4);
   w.total = off;
@@ -643,7 +646,7 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
       (reinterpret_cast<uintptr_t>(loss) & 3u))
     return LCE_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(L, H, V, dt, 0);
-  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  if (ws_bytes < w.fwd_total) return LCE_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
   lce_status st = device_info(&dev);
   if (st != LCE_OK) return st;
@@ -699,11 +702,20 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   return LCE_OK;
 }
 
-lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
-                        const int64_t* labels, const float* lse, int64_t L,
-                        int64_t H, int64_t V, int64_t ignore_index,
-                        const float* dloss, int64_t chunk_rows, void* dH,
-                        float* dW, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace lce {
+namespace {
+
+// The backward over the vocabulary columns [v0, v0 + V) of a vocabulary of
+// V_total (lce_backward: v0 = 0, V_total = V); dH in dt, or in fp32 when
+// dh_f32.
+lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
+                         const int64_t* labels, const float* lse, int64_t L,
+                         int64_t H, int64_t V, int64_t v0, int64_t V_total,
+                         int64_t ignore_index, const float* dloss,
+                         int64_t chunk_rows, void* dH, bool dh_f32, float* dW,
+                         void* ws, size_t ws_bytes, void* stream) {
   if (!h || !W || !labels || !lse || !dloss || !dH || !dW || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
@@ -728,13 +740,14 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
   cudaError_t e;
   {
     ProfScope ps(LCE_K_COUNT_VALID, s);
-    e = launch_count_valid(labels, L, V, ignore_index, n_valid, dev->err, s);
+    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid, dev->err,
+                           s);
     ps.done(0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
 
   uint16_t* G = reinterpret_cast<uint16_t*>(wsb + w.G);
-  const size_t dh_elem = dt == LCE_F32 ? 4 : 2;
+  const size_t dh_elem = (dh_f32 || dt == LCE_F32) ? 4 : 2;
 
   for (int64_t c0 = 0; c0 < L; c0 += w.chunk) {
     const int64_t cr = std::min(w.chunk, L - c0);
@@ -752,6 +765,8 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       p.G = G;
       p.ldg = w.ldg;
       p.ignore_index = ignore_index;
+      p.v0 = v0;
+      p.v_total = V_total;
       ProfScope ps(LCE_K_GEMM_GRAD, s);
       e = run_grad(pl, p, dev->err, s);
       ps.done(2.0 * cr * V * H);
@@ -766,7 +781,7 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       StoreParams p{};
       p.out = static_cast<uint8_t*>(dH) + c0 * H * dh_elem;
       p.ldo = H;
-      p.out_f32 = dt == LCE_F32;
+      p.out_f32 = dh_f32 || dt == LCE_F32;
       p.accumulate = 0;
       p.dloss = dloss;
       p.n_valid = n_valid;
@@ -794,6 +809,153 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
       if (e != cudaSuccess) return cuda_fail(e, "gemm_dW");
     }
   }
+  return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+extern "C" {
+
+lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
+                        const int64_t* labels, const float* lse, int64_t L,
+                        int64_t H, int64_t V, int64_t ignore_index,
+                        const float* dloss, int64_t chunk_rows, void* dH,
+                        float* dW, void* ws, size_t ws_bytes, void* stream) {
+  return backward_impl(h, W, dt, labels, lse, L, H, V, 0, V, ignore_index,
+                       dloss, chunk_rows, dH, false, dW, ws, ws_bytes, stream);
+}
+
+lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
+                              const int64_t* labels, const float* lse,
+                              int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                              int64_t V_total, int64_t ignore_index,
+                              const float* dloss, int64_t chunk_rows,
+                              float* dH_part, float* dW, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (v0 < 0 || Vs < 1 || V_total < 1 || v0 > V_total - Vs)
+    return LCE_ERR_INVALID_ARG;
+  return backward_impl(h, W, dt, labels, lse, L, H, Vs, v0, V_total,
+                       ignore_index, dloss, chunk_rows, dH_part, true, dW, ws,
+                       ws_bytes, stream);
+}
+
+lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
+                             const int64_t* labels, int64_t L, int64_t H,
+                             int64_t Vs, int64_t v0, int64_t V_total,
+                             int64_t ignore_index, float* m, float* s_out,
+                             float* zy, void* ws, size_t ws_bytes,
+                             void* stream) {
+  if (!h || !W || !labels || !m || !s_out || !zy || !ws)
+    return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
+    return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(m) & 3u) ||
+      (reinterpret_cast<uintptr_t>(s_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(zy) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, Vs, dt, 0);
+  if (ws_bytes < w.fwd_total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, Vs, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+  // the label range check against the whole vocabulary
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid,
+                           dev->err, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+  GemmPlan pl;
+  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true, T_LSE},
+                      *dev, &pl)) != LCE_OK)
+    return st;
+  LseParams p{};
+  p.labels = labels;
+  p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
+  p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  p.zy = reinterpret_cast<float*>(wsb + w.zy);
+  p.ignore_index = ignore_index;
+  p.v0 = v0;
+  p.v_total = V_total;
+  {
+    ProfScope ps(LCE_K_GEMM_LSE, s);
+    e = run_lse(pl, p, dev->err, s);
+    ps.done(2.0 * L * Vs * H);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_lse");
+  {
+    ProfScope ps(LCE_K_SLICE_STATS, s);
+    e = launch_slice_stats(p.part_m, p.part_s, pl.g.splits, p.zy, labels, L,
+                           v0, Vs, V_total, ignore_index, m, s_out, zy, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "slice_stats");
+  return LCE_OK;
+}
+
+size_t lce_combine_workspace_size(int64_t L) {
+  if (L < 1) return 0;
+  return 256 + static_cast<size_t>(ceil_div(L, COMBINE_ROWS)) * 8;
+}
+
+lce_status lce_combine_slices(const float* m, const float* s_in,
+                              const float* zy, int64_t P,
+                              const int64_t* labels, int64_t L,
+                              int64_t V_total, int64_t ignore_index,
+                              float* loss, float* lse, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (!m || !s_in || !zy || !labels || !loss || !lse || !ws || P < 1 ||
+      L < 1 || V_total < 1)
+    return LCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(m) & 3u) ||
+      (reinterpret_cast<uintptr_t>(s_in) & 3u) ||
+      (reinterpret_cast<uintptr_t>(zy) & 3u) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(ws))
+    return LCE_ERR_INVALID_ARG;
+  if (ws_bytes < lce_combine_workspace_size(L)) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb);
+  double* block_sums = reinterpret_cast<double*>(wsb + 256);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid,
+                           dev->err, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+  int nb = 0;
+  {
+    ProfScope ps(LCE_K_COMBINE_SLICES, s);
+    e = launch_combine_slices(m, s_in, zy, P, labels, L, V_total, ignore_index,
+                              lse, block_sums, &nb, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "combine_slices");
+  {
+    ProfScope ps(LCE_K_LOSS_FINALIZE, s);
+    e = launch_loss_finalize(block_sums, nb, n_valid, loss, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "loss_finalize");
   return LCE_OK;
 }
 

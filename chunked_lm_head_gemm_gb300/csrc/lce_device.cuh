@@ -282,6 +282,20 @@ __device__ __forceinline__ bool label_valid(int64_t y, int64_t V,
   return y != ignore_index && y >= 0 && y < V;
 }
 
+// Column of label y within a contraction over the vocabulary slice
+// [v0, v0 + n) of a vocabulary of v_total (v_total 0: the whole vocabulary,
+// v_total = n, v0 = 0): -1 when y is not in the slice. *takes_part: y is a
+// valid id of the whole vocabulary.
+__device__ __forceinline__ int label_column(int64_t y, int64_t n, int64_t v0,
+                                            int64_t v_total,
+                                            int64_t ignore_index,
+                                            bool* takes_part) {
+  const int64_t vt = v_total > 0 ? v_total : n;
+  *takes_part = label_valid(y, vt, ignore_index);
+  const int64_t yl = y - v0;
+  return (*takes_part && yl >= 0 && yl < n) ? static_cast<int>(yl) : -1;
+}
+
 // ---------------------------------------------------------------------------
 // unit decode
 // ---------------------------------------------------------------------------
@@ -352,8 +366,9 @@ struct EpiLse {
     row_ok = row < g.M;
     yv = -1;
     if (row_ok) {
-      const int64_t y = p.labels[row];
-      if (label_valid(y, g.N, p.ignore_index)) yv = static_cast<int>(y);
+      bool takes;
+      yv = label_column(p.labels[row], g.N, p.v0, p.v_total, p.ignore_index,
+                        &takes);
     }
     m2 = -INFINITY;
     s = 0.f;
@@ -411,21 +426,21 @@ struct EpiGrad {
   using Params = GradParams;
   int64_t row;
   bool row_ok;
-  int yv;
+  bool takes;  // the row takes part in the loss
+  int yv;      // label column in this contraction, or -1
   float lse2;
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
     row = t.row0 + r;
     row_ok = row < g.M;
+    takes = false;
     yv = -1;
     lse2 = 0.f;
     if (row_ok) {
-      const int64_t y = p.labels[row];
-      if (label_valid(y, g.N, p.ignore_index)) {
-        yv = static_cast<int>(y);
-        lse2 = p.lse[row] * LOG2E;
-      }
+      yv = label_column(p.labels[row], g.N, p.v0, p.v_total, p.ignore_index,
+                        &takes);
+      if (takes) lse2 = p.lse[row] * LOG2E;
     }
   }
 
@@ -443,7 +458,7 @@ struct EpiGrad {
       const int yo = yv - static_cast<int>(j0);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float gi = (yv >= 0) ? ex2(fmaf(v[i], LOG2E, -lse2)) : 0.f;
+        float gi = takes ? ex2(fmaf(v[i], LOG2E, -lse2)) : 0.f;
         if (i == yo) gi -= 1.f;
         v[i] = gi;
       }
@@ -488,8 +503,9 @@ struct EpiFused {
     row_ok = row < g.M;
     yv = -1;
     if (row_ok) {
-      const int64_t y = p.labels[row];
-      if (label_valid(y, g.N, p.ignore_index)) yv = static_cast<int>(y);
+      bool takes;
+      yv = label_column(p.labels[row], g.N, p.v0, p.v_total, p.ignore_index,
+                        &takes);
     }
     m2 = -INFINITY;
     s = 0.f;

@@ -21,6 +21,10 @@ constexpr int GEMM_THREADS = 192;           // 6 warps: TMA, MMA, 4 x epilogue
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 constexpr int TMEM_COLS = 512;              // two 256-column accumulators
 
+// Rows per block of the per-row combine kernels (one float64 loss sum per
+// block).
+constexpr int COMBINE_ROWS = 256;
+
 // Device error bits, OR-ed into the library's error word.
 constexpr unsigned ERRBIT_LABEL_RANGE = 1u << 4;
 constexpr unsigned ERRBIT_TIMEOUT = 1u << 5;
@@ -57,12 +61,18 @@ struct GemmGeom {
 
 // Forward logits tile -> per-row online (max, sum of exp) over the unit's
 // columns, plus the logit at the label.
+// Vocabulary slices (v0, v_total; both 0 for the whole vocabulary): the
+// contraction's N columns are the vocabulary ids [v0, v0 + N) of a
+// vocabulary of v_total; a row takes part when its label is a valid id of
+// the whole vocabulary, and its label column is y - v0 when that lies in
+// the slice.
 struct LseParams {
   const int64_t* labels;  // [M]
   float* part_m;          // [splits][M], running max in log2 units
   float* part_s;          // [splits][M], sum of 2^(u - max)
-  float* zy;              // [M], logit at the label (valid rows only)
+  float* zy;              // [M], logit at the label (rows whose label is here)
   int64_t ignore_index;
+  int64_t v0, v_total;
 };
 
 // Backward recompute tile -> G = softmax - onehot (unscaled), bf16.
@@ -72,6 +82,7 @@ struct GradParams {
   uint16_t* G;            // [M][ldg] bf16 bits
   int64_t ldg;
   int64_t ignore_index;
+  int64_t v0, v_total;    // vocabulary slice, as LseParams
 };
 
 // Fused forward+backward, logits of one row chunk -> per-split online
@@ -87,6 +98,7 @@ struct FusedParams {
   int64_t ldg;
   float* tile_max;        // [M][num_n], log2 units
   int64_t ignore_index;
+  int64_t v0, v_total;    // vocabulary slice, as LseParams
 };
 
 // Gated-MLP gate/up contraction (B dual along N): accumulator columns
@@ -188,6 +200,23 @@ cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
                                int64_t ignore_index, float* lse,
                                double* block_sums, int* nblocks_out,
                                cudaStream_t s);
+// Vocabulary slice: merge the per-split partials into the slice's per-row
+// max logit m (natural units) and sum of exp(z - m), and the label logit
+// (0 where the label is not in [v0, v0 + Vs)).
+cudaError_t launch_slice_stats(const float* part_m, const float* part_s,
+                               int splits, const float* zy_in,
+                               const int64_t* labels, int64_t L, int64_t v0,
+                               int64_t Vs, int64_t V_total,
+                               int64_t ignore_index, float* m, float* s_out,
+                               float* zy, cudaStream_t s);
+// P slices' statistics ([P][L] each) -> lse and per-256-row loss sums, the
+// slices merged in slice order.
+cudaError_t launch_combine_slices(const float* m, const float* s_in,
+                                  const float* zy, int64_t P,
+                                  const int64_t* labels, int64_t L,
+                                  int64_t V_total, int64_t ignore_index,
+                                  float* lse, double* block_sums,
+                                  int* nblocks_out, cudaStream_t s);
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
                                  const unsigned long long* n_valid,
                                  float* loss, cudaStream_t s);

@@ -47,7 +47,7 @@ cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
 // lse_i = ln 2 * (M + log2 sum_k s_k 2^(m_k - M)), M = max_k m_k, merging the
 // per-split partials in a fixed order; then a fixed-order block sum of
 // (lse_i - z_i,y_i) over rows that take part, in float64.
-constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_THREADS = COMBINE_ROWS;
 
 __global__ void __launch_bounds__(COMBINE_THREADS)
     k_lse_combine(const float* __restrict__ part_m,
@@ -93,6 +93,100 @@ cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
   k_lse_combine<<<nb, COMBINE_THREADS, 0, s>>>(part_m, part_s, splits, zy,
                                                labels, L, V, ignore_index, lse,
                                                block_sums);
+  return cudaGetLastError();
+}
+
+// Vocabulary slice [v0, v0 + Vs): per row, the split partials merged in
+// split order into the slice's max logit m = ln 2 * M (natural units) and
+// sum of exp(z - m) = sum_k s_k 2^(m_k - M); the label logit where the label
+// lies in the slice, else 0 (so that summing the slices' values gives it).
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    k_slice_stats(const float* __restrict__ part_m,
+                  const float* __restrict__ part_s, int splits,
+                  const float* __restrict__ zy_in,
+                  const int64_t* __restrict__ labels, int64_t L, int64_t v0,
+                  int64_t Vs, int64_t V_total, int64_t ignore_index,
+                  float* __restrict__ m, float* __restrict__ s,
+                  float* __restrict__ zy) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
+                    threadIdx.x;
+  if (i >= L) return;
+  float M = -INFINITY;
+  for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[k * L + i]);
+  float t = 0.f;
+  for (int k = 0; k < splits; ++k)
+    t += part_s[k * L + i] * exp2f(part_m[k * L + i] - M);
+  m[i] = M * LN2;
+  s[i] = t;
+  const int64_t y = labels[i];
+  const bool here = label_valid(y, V_total, ignore_index) && y >= v0 &&
+                    y < v0 + Vs;
+  zy[i] = here ? zy_in[i] : 0.f;
+}
+
+cudaError_t launch_slice_stats(const float* part_m, const float* part_s,
+                               int splits, const float* zy_in,
+                               const int64_t* labels, int64_t L, int64_t v0,
+                               int64_t Vs, int64_t V_total,
+                               int64_t ignore_index, float* m, float* s_out,
+                               float* zy, cudaStream_t s) {
+  const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
+  k_slice_stats<<<nb, COMBINE_THREADS, 0, s>>>(part_m, part_s, splits, zy_in,
+                                               labels, L, v0, Vs, V_total,
+                                               ignore_index, m, s_out, zy);
+  return cudaGetLastError();
+}
+
+// P vocabulary slices' (m, s, zy), each [P][L]: lse = M + ln sum_r s_r
+// exp(m_r - M) with M = max_r m_r, the label logit = sum_r zy_r, merged in
+// slice order; then per-256-row float64 sums of (lse - z_y) over rows that
+// take part, as k_lse_combine.
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    k_combine_slices(const float* __restrict__ m, const float* __restrict__ s,
+                     const float* __restrict__ zy, int64_t P,
+                     const int64_t* __restrict__ labels, int64_t L,
+                     int64_t V_total, int64_t ignore_index,
+                     float* __restrict__ lse,
+                     double* __restrict__ block_sums) {
+  __shared__ double warp_sums[COMBINE_THREADS / 32];
+  const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
+                    threadIdx.x;
+  double term = 0.0;
+  if (i < L) {
+    float M = -INFINITY;
+    for (int64_t r = 0; r < P; ++r) M = fmaxf(M, m[r * L + i]);
+    float t = 0.f, z = 0.f;
+    for (int64_t r = 0; r < P; ++r) {
+      t += s[r * L + i] * exp2f((m[r * L + i] - M) * LOG2E);
+      z += zy[r * L + i];
+    }
+    const float l = M + log2f(t) * LN2;
+    lse[i] = l;
+    if (label_valid(labels[i], V_total, ignore_index))
+      term = static_cast<double>(l) - static_cast<double>(z);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = term;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double b = 0.0;
+    for (int w = 0; w < COMBINE_THREADS / 32; ++w) b += warp_sums[w];
+    block_sums[blockIdx.x] = b;
+  }
+}
+
+cudaError_t launch_combine_slices(const float* m, const float* s_in,
+                                  const float* zy, int64_t P,
+                                  const int64_t* labels, int64_t L,
+                                  int64_t V_total, int64_t ignore_index,
+                                  float* lse, double* block_sums,
+                                  int* nblocks_out, cudaStream_t s) {
+  const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
+  *nblocks_out = nb;
+  k_combine_slices<<<nb, COMBINE_THREADS, 0, s>>>(m, s_in, zy, P, labels, L,
+                                                  V_total, ignore_index, lse,
+                                                  block_sums);
   return cudaGetLastError();
 }
 

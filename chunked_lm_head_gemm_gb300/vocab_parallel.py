@@ -1,0 +1,78 @@
+"""The loss with the LM head split by vocabulary over the processes of a group.
+
+Each process holds all of h and one slice of the head's rows, W[v0, v0 + Vs)
+of a vocabulary of V_total (tensor parallelism on the head). "Training Beyond
+1M Tokens", section "The massive logits matrix: chunk it", explains that rows
+split cleanly because the softmax runs along one row's vocabulary; split the
+vocabulary instead and each row's log-sum-exp must be merged from the slices:
+
+    forward   each slice: m_r = max_j z_ij, s_r = sum_j exp(z_ij - m_r), and
+              the label logit if the label is in the slice (else 0)
+              exchange: all-gather of (m, s, zy), 3 L floats per process
+              every process: lse = M + ln sum_r s_r exp(m_r - M), M = max_r m_r,
+              loss = mean over valid rows of lse - z_y (same bits everywhere)
+    backward  each slice: G_r = dloss/N (exp(z - lse) - [j == y]) on its
+              columns, dW_r = G_r^T h (stays local), dH_r = G_r W_r
+              exchange: all-reduce (sum) of the fp32 dH_r, L H floats
+
+Every loss and gradient value comes from the library's kernels; this module
+only moves the statistics and partial sums between processes. With no group
+(or a group of one) the one slice is the whole vocabulary.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+def _world(group) -> int:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return 1
+    return dist.get_world_size(group)
+
+
+def gather_stats(stats: torch.Tensor, group=None) -> torch.Tensor:
+    """stats [3, L] (m, s, zy of this process's slice) -> [P, 3, L] in rank
+    order, the same on every process."""
+    world = _world(group)
+    if world == 1:
+        return stats.unsqueeze(0)
+    import torch.distributed as dist
+    out = torch.empty((world * stats.shape[0],) + tuple(stats.shape[1:]),
+                      dtype=stats.dtype, device=stats.device)
+    dist.all_gather_into_tensor(out, stats.contiguous(), group=group)
+    return out.view((world,) + tuple(stats.shape))
+
+
+def sum_partials(dH_part: torch.Tensor, group=None) -> torch.Tensor:
+    """The slices' dH partials summed in place over the group (fp32)."""
+    if _world(group) > 1:
+        import torch.distributed as dist
+        dist.all_reduce(dH_part, op=dist.ReduceOp.SUM, group=group)
+    return dH_part
+
+
+def forward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
+            v0: int, V_total: int, group=None,
+            ignore_index: int = B.IGNORE_INDEX, workspace=None):
+    """Returns (loss, lse [L]) of the whole vocabulary on every process."""
+    m, s, zy = B.forward_slice(h, W_slice, labels, v0, V_total, ignore_index,
+                               workspace)
+    allst = gather_stats(torch.stack([m, s, zy]), group)
+    return B.combine_slices(allst[:, 0].contiguous(), allst[:, 1].contiguous(),
+                            allst[:, 2].contiguous(), labels, V_total,
+                            ignore_index)
+
+
+def backward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
+             lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
+             group=None, ignore_index: int = B.IGNORE_INDEX,
+             chunk_rows: int = 0, workspace=None):
+    """Returns (dH [L,H] float32, summed over the group; dW of this slice
+    [Vs,H] float32)."""
+    dH_part, dW = B.backward_slice(h, W_slice, labels, lse, dloss, v0,
+                                   V_total, ignore_index, chunk_rows,
+                                   workspace)
+    return sum_partials(dH_part, group), dW

@@ -78,6 +78,8 @@ typedef enum {
  * chunk (0 = the library's default). Returns 0 for invalid sizes.
  * The dominant term is chunk_rows * round_up(V, 8) * 2 bytes (the bf16
  * gradient-logit chunk); with LCE_F32 add bf16 copies of h and W.
+ * lce_forward and lce_forward_slice use only the regions before the
+ * gradient-logit chunk, so any chunk_rows gives them enough.
  */
 size_t lce_workspace_size(int64_t L, int64_t H, int64_t V, lce_dtype dt,
                           int64_t chunk_rows);
@@ -157,6 +159,70 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
 lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                float* dW, int64_t V, const float* dloss,
                                void* stream);
+
+/*
+ * Vocabulary-parallel form (several processes each hold a slice of the
+ * head's rows, W[v0 .. v0 + Vs) of a vocabulary of V_total, and all of h).
+ * "Training Beyond 1M Tokens", section "The massive logits matrix: chunk
+ * it", explains that rows split cleanly because the softmax runs along one
+ * row's vocabulary; splitting the vocabulary instead needs, per row, each
+ * slice's maximum logit m and sum of exp(z - m), merged exactly as
+ * lse = M + ln sum_r s_r exp(m_r - M), M = max_r m_r. Three calls:
+ *
+ * lce_forward_slice: one slice's statistics.
+ *   h        device [L][H] of dt (every row)
+ *   W        device [Vs][H] of dt: rows v0 .. v0 + Vs - 1 of the head
+ *   labels   device [L] int64, ids of the whole vocabulary
+ *   v0, Vs, V_total   0 <= v0, v0 + Vs <= V_total
+ *   m, s     device [L] float32 out: max_j z_ij and sum_j exp(z_ij - m_i)
+ *            over the slice's columns j
+ *   zy       device [L] float32 out: z_{i, y_i} where y_i lies in the slice
+ *            and takes part, else 0 (so the slices' values sum to it)
+ *   ws       workspace of lce_workspace_size(L, H, Vs, dt, chunk_rows)
+ * Labels outside [0, V_total) that are not ignore_index raise
+ * LCE_ERR_LABEL_RANGE (the row is ignored everywhere).
+ */
+lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
+                             const int64_t* labels, int64_t L, int64_t H,
+                             int64_t Vs, int64_t v0, int64_t V_total,
+                             int64_t ignore_index, float* m, float* s,
+                             float* zy, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * lce_combine_slices: the P slices' statistics, gathered by the caller into
+ * m, s, zy (device [P][L] float32 each, slice r at offset r * L, any slice
+ * order as long as every process uses the same), merged per row in slice
+ * order into lse (device [L] float32 out) and the mean loss over valid rows
+ * (device [1] float32 out, 0 if none). ws: device, 16-byte aligned, at least
+ * lce_combine_workspace_size(L) bytes (any slice call's workspace is
+ * larger). Every process that runs it on the same gathered input gets the
+ * same bits.
+ */
+size_t lce_combine_workspace_size(int64_t L);
+lce_status lce_combine_slices(const float* m, const float* s, const float* zy,
+                              int64_t P, const int64_t* labels, int64_t L,
+                              int64_t V_total, int64_t ignore_index,
+                              float* loss, float* lse, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/*
+ * lce_backward_slice: one slice's share of the backward, given the merged
+ * lse: G_s = dloss/N (exp(z - lse) - [j == y]) over the slice's columns
+ * (N counted over the whole vocabulary's valid labels), recomputing the
+ * logits chunk by chunk as lce_backward does.
+ *   dH_part  device [L][H] float32 out: G_s W_s; the sum over the slices is
+ *            dH (the caller's all-reduce)
+ *   dW       device [Vs][H] float32 out: this slice's rows of dW
+ *   other arguments as lce_forward_slice and lce_backward
+ */
+lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
+                              const int64_t* labels, const float* lse,
+                              int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                              int64_t V_total, int64_t ignore_index,
+                              const float* dloss, int64_t chunk_rows,
+                              float* dH_part, float* dW, void* ws,
+                              size_t ws_bytes, void* stream);
 
 /*
  * Count of rows that take part in the loss: n_valid[0] = #{i : labels[i] !=
@@ -294,7 +360,7 @@ int lce_get_cta_pair(void);
  * per tensor-core contraction, 0 for the other kernels). Host-side state
  * only; events are created on first use and reused.
  */
-#define LCE_KERNEL_KINDS 19
+#define LCE_KERNEL_KINDS 21
 enum {
   LCE_K_COUNT_VALID = 0,
   LCE_K_GEMM_LSE = 1,
@@ -314,7 +380,9 @@ enum {
   LCE_K_MLP_DA = 15,
   LCE_K_MLP_DX = 16,
   LCE_K_MLP_DWD = 17,
-  LCE_K_MLP_DWGU = 18
+  LCE_K_MLP_DWGU = 18,
+  LCE_K_SLICE_STATS = 19,
+  LCE_K_COMBINE_SLICES = 20
 };
 
 typedef struct {

@@ -96,6 +96,19 @@ def test_bad_arguments_return_before_any_device_call(lib):
                                null) == 1
     assert lib.lce_count_valid(p, -1, 8, -100, p, null) == 1
     assert lib.lce_count_valid(p, 8, 0, -100, p, null) == 1
+    # vocabulary slices: slice past the vocabulary, negative offset
+    assert lib.lce_forward_slice(p, p, 0, p, 8, 8, 8, 4, 10, -100, p, p, p,
+                                 p, 1 << 30, null) == 1
+    assert lib.lce_forward_slice(p, p, 0, p, 8, 8, 8, -1, 10, -100, p, p, p,
+                                 p, 1 << 30, null) == 1
+    assert lib.lce_backward_slice(p, p, 0, p, p, 8, 8, 8, 4, 10, -100, p, 0,
+                                  p, p, p, 1 << 30, null) == 1
+    assert lib.lce_combine_slices(p, p, p, 0, p, 8, 10, -100, p, p, p,
+                                  1 << 20, null) == 1
+    assert lib.lce_combine_slices(p, p, p, 2, p, 8, 10, -100, p, p, p, 8,
+                                  null) == 3
+    assert lib.lce_combine_workspace_size(0) == 0
+    assert lib.lce_combine_workspace_size(300) == 256 + 2 * 8
     # test hooks
     assert lib.lce_test_gemm(null, p, p, 8, 8, 8, 0, 0, null) == 1
     assert lib.lce_test_gemm(p, p, p, 8, 12, 8, 0, 0, null) == 1

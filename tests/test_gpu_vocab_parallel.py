@@ -1,0 +1,136 @@
+"""Vocabulary-parallel form on one GPU, the slices run one after another:
+each slice's statistics against the float64 oracle applied to that slice's
+sub-vocabulary, the merged lse and loss against the oracle on the whole
+vocabulary, and the slices' backward (sum of dH partials, concatenated dW)
+against the oracle's gradients."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunked_lm_head_gemm_gb300 as lce
+from chunked_lm_head_gemm_gb300 import _binding as B
+from chunked_lm_head_gemm_gb300 import vocab_parallel as vp
+from chunked_lm_head_gemm_gb300.inputs import Workload, make_inputs
+from tests.gpu_util import (GRAD_RFRO, LOSS_RTOL, LSE_ATOL, PAIRS, cta_pair,
+                            rel_fro, require_gpu, to64)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, L, H, V, slice sizes, chunk_rows
+    ("three_ragged", 300, 64, 1000, [333, 333, 334], 0),
+    ("four_even", 513, 128, 4096, [1024] * 4, 256),
+    ("uneven_tiny_slice", 200, 40, 777, [700, 70, 7], 96),
+]
+
+
+def _bounds(sizes):
+    out, v0 = [], 0
+    for n in sizes:
+        out.append((v0, n))
+        v0 += n
+    return out
+
+
+def _slice_oracle(h, Ws, y, v0, Vs):
+    """The oracle's forward on the sub-vocabulary: labels in the slice
+    mapped to local ids, the rest ignored (they add no label logit)."""
+    y = y.clone()
+    local = (y >= v0) & (y < v0 + Vs)
+    y[~local] = -100
+    y[local] -= v0
+    return oracle.forward(h, Ws, y), local.numpy()
+
+
+def _inputs(name, L, H, V, seed=11):
+    wl = Workload(name, L, H, V, "bf16", 1.0, 0.1, "uniform", ignore_frac=0.1)
+    return make_inputs(wl, seed=seed, device=require_gpu())
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("name,L,H,V,sizes,chunk", CASES,
+                         ids=[c[0] for c in CASES])
+def test_slices_forward_backward(name, L, H, V, sizes, chunk, pair):
+    h, W, y = _inputs(name, L, H, V)
+    hc, Wc, yc = h.cpu(), W.cpu(), y.cpu()
+    dloss = torch.full((), 0.5, device=h.device)
+    with cta_pair(pair):
+        stats = []
+        for v0, Vs in _bounds(sizes):
+            m, s, zy = B.forward_slice(h, W[v0:v0 + Vs], y, v0, V)
+            stats.append(torch.stack([m, s, zy]))
+            # the slice's own statistics against the oracle on its columns
+            f_s, local = _slice_oracle(hc, Wc[v0:v0 + Vs], yc, v0, Vs)
+            lse_s = (m.double() + torch.log(s.double())).cpu().numpy()
+            assert np.max(np.abs(lse_s - f_s["lse"])) <= LSE_ATOL
+            zy_h = zy.cpu().numpy()
+            assert np.all(zy_h[~local] == 0.0)
+            assert np.max(np.abs(zy_h[local] - f_s["zy"][local]),
+                          initial=0.0) <= LSE_ATOL
+        allst = torch.stack(stats)
+        loss, lse = B.combine_slices(allst[:, 0].contiguous(),
+                                     allst[:, 1].contiguous(),
+                                     allst[:, 2].contiguous(), y, V)
+        dH = torch.zeros(L, H, dtype=torch.float32, device=h.device)
+        dWs = []
+        for v0, Vs in _bounds(sizes):
+            dH_part, dW_s = B.backward_slice(h, W[v0:v0 + Vs], y, lse, dloss,
+                                             v0, V, chunk_rows=chunk)
+            dH += dH_part
+            dWs.append(dW_s)
+        dW = torch.cat(dWs)
+        assert lce.get_error() == 0
+    f = oracle.forward(hc, Wc, yc)
+    b = oracle.backward(hc, Wc, yc, dloss=0.5)
+    assert abs(loss.item() - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.max(np.abs(to64(lse) - f["lse"])) <= LSE_ATOL
+    assert rel_fro(to64(dH), b["dH"]) <= GRAD_RFRO
+    assert rel_fro(to64(dW), b["dW"]) <= GRAD_RFRO
+    # and against the whole-vocabulary call on the same GPU
+    with cta_pair(pair):
+        loss1, lse1 = lce.forward(h, W, y)
+        dH1, dW1 = lce.backward(h, W, y, lse1, dloss, chunk_rows=chunk)
+    assert abs(loss.item() - loss1.item()) <= 1e-5 * abs(loss1.item())
+    assert torch.max(torch.abs(lse - lse1)).item() <= 1e-4
+    # lse differs in the last bits, which flips a few bf16 roundings of G
+    assert rel_fro(to64(dW), to64(dW1)) <= 1e-3
+    # dH1 is rounded to bf16 once; the fp32 sum of partials is not
+    assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
+
+
+def test_labels_out_of_range_and_in_other_slices():
+    h, W, y = _inputs("bad", 260, 32, 600)
+    y[3] = 600          # past the whole vocabulary: an error, row ignored
+    y[9] = -5
+    y[10] = 599         # last id, in the second slice only
+    sizes = [300, 300]
+    stats = []
+    for k, (v0, Vs) in enumerate(_bounds(sizes)):
+        stats.append(torch.stack(B.forward_slice(h, W[v0:v0 + Vs], y, v0,
+                                                 600)))
+        assert B.get_error() == B.LCE_ERR_LABEL_RANGE
+    allst = torch.stack(stats)
+    loss, lse = B.combine_slices(allst[:, 0].contiguous(),
+                                 allst[:, 1].contiguous(),
+                                 allst[:, 2].contiguous(), y, 600)
+    assert B.get_error() == B.LCE_ERR_LABEL_RANGE
+    f = oracle.forward(h.cpu(), W.cpu(), y.cpu())
+    assert f["status"] == oracle.LABEL_RANGE
+    assert abs(loss.item() - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.max(np.abs(to64(lse) - f["lse"])) <= LSE_ATOL
+    assert allst[0, 2, 10].item() == 0.0 and allst[1, 2, 10].item() != 0.0
+
+
+def test_module_without_group_is_one_slice():
+    h, W, y = _inputs("one", 384, 64, 2000)
+    d = torch.full((), 1.0, device=h.device)
+    loss, lse = vp.forward(h, W, y, 0, 2000)
+    dH, dW = vp.backward(h, W, y, lse, d, 0, 2000)
+    loss1, lse1 = lce.forward(h, W, y)
+    dH1, dW1 = lce.backward(h, W, y, lse1, d)
+    assert lce.get_error() == 0
+    assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
+    assert torch.max(torch.abs(lse - lse1)).item() <= 1e-5
+    assert rel_fro(to64(dW), to64(dW1)) <= 1e-3
+    assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
