@@ -218,7 +218,11 @@ def cpu_baseline(wl, h_cpu, W_cpu, y_cpu, target_s: float = 20.0) -> dict:
             "sample": (f"first {rows} of {wl.L} rows of {wl.name} (full "
                        f"H={wl.H}, V={wl.V}); float64 forward + backward "
                        f"(lse, loss, dH, full dW) in {t:.1f} s; tokens/s = "
-                       f"sample rows / time")}
+                       f"sample rows / time"),
+            "extrapolated_full_step_s": wl.L * t / rows,
+            "extrapolated_note": ("not measured: the sample's time scaled to "
+                                  "all rows (the float64 dW pass grows with "
+                                  "the rows like the rest)")}
 
 
 def run_reference(args, wl) -> dict:
