@@ -39,7 +39,8 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_set_cta_pair", "lce_get_cta_pair", "lce_mlp_workspace_size",
             "lce_mlp_forward", "lce_mlp_backward", "lce_count_valid",
             "lce_forward_slice", "lce_combine_workspace_size",
-            "lce_combine_slices", "lce_backward_slice")
+            "lce_combine_slices", "lce_backward_slice", "lce_set_wave_sync",
+            "lce_get_wave_sync")
 
 KERNEL_KINDS = 21
 
@@ -130,6 +131,10 @@ def load(build_if_missing: bool = False):
         lib.lce_set_cta_pair.restype = i32
         lib.lce_get_cta_pair.argtypes = []
         lib.lce_get_cta_pair.restype = i32
+        lib.lce_set_wave_sync.argtypes = [i32]
+        lib.lce_set_wave_sync.restype = i32
+        lib.lce_get_wave_sync.argtypes = []
+        lib.lce_get_wave_sync.restype = i32
         lib.lce_forward_static.argtypes = [p, p, p, i64, i64, i64, i64, p, p,
                                            p]
         lib.lce_forward_static.restype = i32
@@ -474,6 +479,15 @@ def set_cta_pair(enable: bool):
 
 def get_cta_pair() -> bool:
     return bool(load().lce_get_cta_pair())
+
+
+def set_wave_sync(enable: bool):
+    """Wave pacing of the contractions on (default) or off; same results."""
+    _check(load().lce_set_wave_sync(1 if enable else 0), "lce_set_wave_sync")
+
+
+def get_wave_sync() -> bool:
+    return bool(load().lce_get_wave_sync())
 
 
 def profile_start():

@@ -281,6 +281,20 @@ const Tune& tune() {
   return t;
 }
 
+// Wave pacing of the contractions (GemmGeom::wave_ctr): on unless
+// LCE_WAVE_SYNC=0 or lce_set_wave_sync(0).
+std::atomic<int> g_wave_mode{-1};
+
+bool wave_sync_on() {
+  int v = g_wave_mode.load();
+  if (v < 0) {
+    const char* env = std::getenv("LCE_WAVE_SYNC");
+    v = (env && *env) ? (std::atoi(env) != 0) : 1;
+    g_wave_mode.store(v);
+  }
+  return v != 0;
+}
+
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
@@ -408,6 +422,42 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   return LCE_OK;
 }
 
+// Turn on wave pacing for one launch: the counter is zeroed on the stream
+// first. A wait runs out after ~two tiles' worth of MMA time at full rate.
+cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
+  if (!wave_sync_on()) return cudaSuccess;
+  const GemmGeom& g = pl->g;
+  const int slots = pl->pair ? pl->grid / 2 : pl->grid;
+  // the most output tiles any CTA (cluster) walks, as the kernels assign
+  // them (first unit, then every slots-th)
+  uint32_t most = 0;
+  for (int c = 0; c < slots; ++c) {
+    const int first = g.cl_stride > 1
+                          ? static_cast<int>((static_cast<int64_t>(c) *
+                                              g.cl_stride) % slots)
+                          : c;
+    uint32_t n = 0;
+    for (int u = first; u < g.num_units; u += slots) {
+      if (g.group_n > 0 && g.tiles_per_split == 1) {
+        n += 1;
+      } else {
+        const int split = u % g.splits;
+        n += static_cast<uint32_t>(
+            std::min(g.tiles_per_split, g.num_n - split * g.tiles_per_split));
+      }
+    }
+    most = std::max(most, n);
+  }
+  const double tile_flops = 2.0 * (pl->pair ? 2 * BM : BM) * BN * g.K;
+  const double per_slot = 1.5e15 / (pl->pair ? 76 : 152);
+  const double ns = 2.0 * tile_flops / per_slot * 1e9;
+  pl->g.wave_ctr = static_cast<unsigned*>(ctr);
+  pl->g.wave_wait_ns = static_cast<uint32_t>(
+      std::min(2.0e6, std::max(2.0e4, ns)));
+  pl->g.wave_steps = most;
+  return cudaMemsetAsync(ctr, 0, sizeof(unsigned), s);
+}
+
 cudaError_t run_lse(const GemmPlan& pl, const LseParams& p, unsigned* err,
                     cudaStream_t s) {
   return pl.pair ? launch_gemm_pair_lse(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
@@ -436,6 +486,7 @@ struct WsLayout {
   size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, tile_max,
       total;
   size_t fwd_total;  // what the forward-only calls use: everything before G
+  size_t sync;       // wave-pacing counter of the gradient contractions
   int64_t chunk, ldg;
 };
 
@@ -528,6 +579,7 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
                            ceil_div(L - (nchunks - 1) * w.chunk, 256);
   const int64_t nb = std::max(ceil_div(L, 256), nb_fused);
   w.n_valid = take(8);
+  w.sync = take(8);
   w.block_sums = take(nb * 8);
   w.part_m = take(static_cast<size_t>(kMaxSplits) * L * 4);
   w.part_s = take(static_cast<size_t>(kMaxSplits) * L * 4);
@@ -677,6 +729,8 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
   p.zy = reinterpret_cast<float*>(wsb + w.zy);
   p.ignore_index = ignore_index;
+  e = pace(&pl, wsb + w.sync, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pace");
   {
     ProfScope ps(LCE_K_GEMM_LSE, s);
     e = run_lse(pl, p, dev->err, s);
@@ -767,6 +821,8 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       p.ignore_index = ignore_index;
       p.v0 = v0;
       p.v_total = V_total;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_GRAD, s);
       e = run_grad(pl, p, dev->err, s);
       ps.done(2.0 * cr * V * H);
@@ -785,6 +841,8 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       p.accumulate = 0;
       p.dloss = dloss;
       p.n_valid = n_valid;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_DH, s);
       e = run_store(pl, false, true, p, dev->err, s);
       ps.done(2.0 * cr * H * V);
@@ -803,6 +861,8 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       p.accumulate = c0 > 0;
       p.dloss = dloss;
       p.n_valid = n_valid;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_DW, s);
       e = run_store(pl, true, true, p, dev->err, s);
       ps.done(2.0 * V * H * cr);
@@ -889,6 +949,8 @@ lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
   p.ignore_index = ignore_index;
   p.v0 = v0;
   p.v_total = V_total;
+  e = pace(&pl, wsb + w.sync, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pace");
   {
     ProfScope ps(LCE_K_GEMM_LSE, s);
     e = run_lse(pl, p, dev->err, s);
@@ -1024,6 +1086,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       p.ldg = w.ldg;
       p.tile_max = tile_max;
       p.ignore_index = ignore_index;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_FUSED, s);
       e = run_fused(pl, p, dev->err, s);
       ps.done(2.0 * cr * V * H);
@@ -1062,6 +1126,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       p.accumulate = 0;
       p.dloss = nullptr;
       p.n_valid = n_valid;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_DH, s);
       e = run_store(pl, false, true, p, dev->err, s);
       ps.done(2.0 * cr * H * V);
@@ -1080,6 +1146,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       p.accumulate = c0 > 0;
       p.dloss = nullptr;
       p.n_valid = n_valid;
+      e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_GEMM_DW, s);
       e = run_store(pl, true, true, p, dev->err, s);
       ps.done(2.0 * V * H * cr);
@@ -1440,6 +1508,14 @@ lce_status lce_set_cta_pair(int enable) {
 }
 
 int lce_get_cta_pair(void) { return use_pair() ? 1 : 0; }
+
+lce_status lce_set_wave_sync(int enable) {
+  if (enable != 0 && enable != 1) return LCE_ERR_INVALID_ARG;
+  g_wave_mode.store(enable);
+  return LCE_OK;
+}
+
+int lce_get_wave_sync(void) { return wave_sync_on() ? 1 : 0; }
 
 lce_status lce_profile_start(void) {
   if (t_prof.on) return LCE_ERR_INVALID_ARG;

@@ -297,6 +297,33 @@ __device__ __forceinline__ int label_column(int64_t y, int64_t n, int64_t v0,
 }
 
 // ---------------------------------------------------------------------------
+// wave pacing (GemmGeom::wave_ctr)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void wave_wait(const GemmGeom& g, uint32_t target) {
+  if (!g.wave_ctr || target == 0) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "l"(g.wave_ctr)
+                 : "memory");
+    if (v >= target) return;
+    if (globaltimer_ns() - t0 > g.wave_wait_ns) return;
+    __nanosleep(64);
+  }
+}
+
+__device__ __forceinline__ void wave_arrive(const GemmGeom& g) {
+  if (g.wave_ctr) atomicAdd(g.wave_ctr, 1u);
+}
+
+__device__ __forceinline__ void wave_finish(const GemmGeom& g, uint32_t done) {
+  if (g.wave_ctr && g.wave_steps > done)
+    atomicAdd(g.wave_ctr, g.wave_steps - done);
+}
+
+// ---------------------------------------------------------------------------
 // unit decode
 // ---------------------------------------------------------------------------
 struct Unit {
@@ -864,10 +891,13 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
   uint32_t stage = 0, phase = 0, issued = 0;
   const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
-  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units; u += gridDim.x) {
+  uint32_t step = 0;  // output tiles whose loads this CTA has issued
+  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units;
+       u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     const int m0 = t.m_blk * BM;
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      wave_wait(g, step * gridDim.x);
       const int n0 = (t.n_first + tt) * BN;
       for (int kb = 0; kb < g.num_kb; ++kb) {
         if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
@@ -910,8 +940,13 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
           phase ^= 1u;
         }
       }
+      if (ok) {
+        wave_arrive(g);
+        ++step;
+      }
     }
   }
+  wave_finish(g, step);
   // Drain: every copy issued must have landed before the CTA may exit.
   for (int s = 0; s < STAGES; ++s) {
     const uint32_t cnt = issued / STAGES + (static_cast<uint32_t>(s) < issued % STAGES ? 1u : 0u);
@@ -1266,10 +1301,12 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
   uint32_t stage = 0, phase = 0, issued = 0;
   const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
+  uint32_t step = 0;  // output tiles whose loads this CTA has issued
   for (int u = cluster; ok && u < g.num_units; u += nclusters) {
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
     const int a0 = static_cast<int>(t.row0);  // this CTA's 128 rows of A
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
+      if (leader) wave_wait(g, step * static_cast<uint32_t>(nclusters));
       // this CTA's 128 of the tile's 256 output columns; dual along N: the
       // leader takes the first map's 128 rows, the peer the second's
       const bool dual_n = g.b_dual == 1;
@@ -1311,8 +1348,13 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
           phase ^= 1u;
         }
       }
+      if (ok) {
+        if (leader) wave_arrive(g);
+        ++step;
+      }
     }
   }
+  if (leader) wave_finish(g, step);
   // Drain: the leader's full barriers count both CTAs' copies; once they
   // have all completed no copy of either CTA is still in flight.
   if (leader) {

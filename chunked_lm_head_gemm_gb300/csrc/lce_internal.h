@@ -55,6 +55,18 @@ struct GemmGeom {
   // Placement: CTA (or cluster) i starts at unit (i * cl_stride) mod the
   // grid's CTAs (clusters); 1 = in order. Coprime with that count.
   int cl_stride;
+  // Wave pacing (nullptr: off): before its s-th output tile (s >= 1) a
+  // CTA's (a pair's leader's) producer waits until *wave_ctr >= s * (CTAs or
+  // clusters of the grid), i.e. until every CTA has issued the loads of s
+  // tiles, for at most wave_wait_ns; after issuing a tile's loads it adds 1,
+  // and when done it adds wave_steps minus its tile count (wave_steps = the
+  // most tiles any CTA has), so finished CTAs hold no one back. Keeps the
+  // CTAs that share operand panels at the same K position so the panels
+  // are read from L2, not DRAM. Only a hint: a wait that runs out goes on.
+  // The counter is zeroed before every launch.
+  unsigned* wave_ctr;
+  uint32_t wave_wait_ns;
+  uint32_t wave_steps;
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------

@@ -350,6 +350,20 @@ lce_status lce_set_cta_pair(int enable);
 int lce_get_cta_pair(void);
 
 /*
+ * Wave pacing of the persistent tensor-core contractions, for the whole
+ * process: enable = 1 (the default) keeps the CTAs that read the same
+ * operand panels within about one output tile of each other, so a panel
+ * is fetched from DRAM once per wave of tiles instead of once per CTA that
+ * drifted out of L2's reach (a bounded wait on a counter in the workspace
+ * before each tile; a wait that runs out goes on, so results never depend
+ * on it). enable = 0: every CTA runs free. Results are bit-identical either
+ * way. LCE_WAVE_SYNC=0/1 sets the initial choice. No counterpart on the
+ * pages. Returns LCE_ERR_INVALID_ARG for other values.
+ */
+lce_status lce_set_wave_sync(int enable);
+int lce_get_wave_sync(void);
+
+/*
  * Per-kernel timing of this library's own launches, for benchmarks. No
  * counterpart on the pages. Between lce_profile_start() and
  * lce_profile_stop(), every kernel the calling thread launches through this

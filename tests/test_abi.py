@@ -119,6 +119,11 @@ def test_bad_arguments_return_before_any_device_call(lib):
     assert lib.lce_set_cta_pair(1) == 0 and lib.lce_get_cta_pair() == 1
     assert lib.lce_set_cta_pair(0) == 0 and lib.lce_get_cta_pair() == 0
     assert lib.lce_set_cta_pair(before) == 0
+    assert lib.lce_set_wave_sync(2) == 1
+    before = lib.lce_get_wave_sync()
+    assert lib.lce_set_wave_sync(0) == 0 and lib.lce_get_wave_sync() == 0
+    assert lib.lce_set_wave_sync(1) == 0 and lib.lce_get_wave_sync() == 1
+    assert lib.lce_set_wave_sync(before) == 0
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
