@@ -227,9 +227,11 @@ lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
 // Per contraction kind: the L2 eviction priority of each operand's loads and
 // the tile grouping of tile-per-unit contractions; plus the L2 budget that
 // bounds the live A row panels when choosing column splits. Defaults are the
-// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,kind.s=S,l2mb=M"
-// (kinds lse, grad, fused, dH, dW, test, mlp; H in 0..2; G >= 0; S >= 1, the
-// placement stride GemmGeom::cl_stride) overrides them.
+// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,kind.s=S,kind.p=P,
+// l2mb=M,pace_us=P" (kinds lse, grad, fused, dH, dW, test, mlp; H in 0..2;
+// G >= 0; S >= 1, the placement stride GemmGeom::cl_stride; P the least
+// time in us between two wave-pacing waits, GemmGeom::wave_period, < 0 for
+// none; pace_us sets it for every kind) overrides them.
 enum TuneKind {
   T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_KINDS
 };
@@ -239,12 +241,16 @@ struct Tune {
   int group_n[T_KINDS];
   int cl_stride[T_KINDS];
   double l2_budget;
+  // wave pacing: at least this long between two waits (0: before every
+  // tile); < 0: no pacing for this kind
+  double pace_ns[T_KINDS];
 };
 
 const Tune& tune() {
   static Tune t = [] {
     Tune v{};
     v.l2_budget = 48e6;
+    v.pace_ns[T_MLP] = -1.0;  // the MLP contractions run unpaced
     const char* env = std::getenv("LCE_TUNE");
     if (!env) return v;
     static const char* names[T_KINDS] = {"lse", "grad", "fused", "dH", "dW",
@@ -264,6 +270,10 @@ const Tune& tune() {
         if (val > 0) v.l2_budget = val * 1e6;
         continue;
       }
+      if (key == "pace_us") {
+        for (int k = 0; k < T_KINDS; ++k) v.pace_ns[k] = val * 1e3;
+        continue;
+      }
       const size_t dot = key.find('.');
       if (dot == std::string::npos) continue;
       const std::string kind = key.substr(0, dot), field = key.substr(dot + 1);
@@ -274,6 +284,7 @@ const Tune& tune() {
         if (field == "b" && iv >= 0 && iv <= 2) v.b_hint[k] = iv;
         if (field == "g" && iv >= 0) v.group_n[k] = iv;
         if (field == "s" && iv >= 1) v.cl_stride[k] = iv;
+        if (field == "p") v.pace_ns[k] = val * 1e3;
       }
     }
     return v;
@@ -347,6 +358,7 @@ GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps,
   g.group_n = 0;
   g.a_hint = g.b_hint = 0;
   g.cl_stride = 1;
+  g.wave_period = 1;
   return g;
 }
 
@@ -375,6 +387,7 @@ struct GemmOperands {
 
 struct GemmPlan {
   bool pair;
+  int kind;  // TuneKind
   GemmGeom g;
   CUtensorMap ta, tb, tb2;
   int grid;
@@ -383,6 +396,7 @@ struct GemmPlan {
 lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
                      GemmPlan* pl) {
   pl->pair = use_pair() && dev.pair_slots > 0;
+  pl->kind = o.kind;
   const int rows_unit = pl->pair ? 2 * BM : BM;
   const int slots = pl->pair ? dev.pair_slots : dev.num_sms;
   const int num_m = static_cast<int>(ceil_div(o.M, rows_unit));
@@ -425,7 +439,8 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
 // Turn on wave pacing for one launch: the counter is zeroed on the stream
 // first. A wait runs out after ~two tiles' worth of MMA time at full rate.
 cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
-  if (!wave_sync_on()) return cudaSuccess;
+  if (!wave_sync_on() || !ctr || tune().pace_ns[pl->kind] < 0)
+    return cudaSuccess;
   const GemmGeom& g = pl->g;
   const int slots = pl->pair ? pl->grid / 2 : pl->grid;
   // the most output tiles any CTA (cluster) walks, as the kernels assign
@@ -450,7 +465,10 @@ cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
   }
   const double tile_flops = 2.0 * (pl->pair ? 2 * BM : BM) * BN * g.K;
   const double per_slot = 1.5e15 / (pl->pair ? 76 : 152);
-  const double ns = 2.0 * tile_flops / per_slot * 1e9;
+  const double tile_ns = tile_flops / per_slot * 1e9;
+  const double ns = 2.0 * tile_ns;
+  pl->g.wave_period = static_cast<uint32_t>(
+      std::max(1.0, std::floor(tune().pace_ns[pl->kind] / tile_ns)));
   pl->g.wave_ctr = static_cast<unsigned*>(ctr);
   pl->g.wave_wait_ns = static_cast<uint32_t>(
       std::min(2.0e6, std::max(2.0e4, ns)));
@@ -1214,7 +1232,7 @@ namespace lce {
 namespace {
 
 struct MlpLayout {
-  size_t g, u, a, dgu, total;
+  size_t sync, g, u, a, dgu, total;
   int64_t chunk;
 };
 
@@ -1245,6 +1263,7 @@ MlpLayout mlp_layout(int64_t L, int64_t I, int64_t chunk_rows) {
     return o;
   };
   const size_t plane = static_cast<size_t>(w.chunk) * I * 2;
+  w.sync = take(8);
   w.g = take(plane);
   w.u = take(plane);
   w.a = take(plane);
@@ -1256,7 +1275,8 @@ MlpLayout mlp_layout(int64_t L, int64_t I, int64_t chunk_rows) {
 // a_c = silu(x_c Wg^T) * (x_c Wu^T), optionally saving g_c and u_c.
 lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
                        const void* Wg, const void* Wu, int64_t H, int64_t I,
-                       uint16_t* a, uint16_t* g, uint16_t* u, cudaStream_t s) {
+                       uint16_t* a, uint16_t* g, uint16_t* u, void* ctr,
+                       cudaStream_t s) {
   GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false, T_MLP};
   o.b_dual = 1;
   o.b2 = Wu;
@@ -1264,21 +1284,26 @@ lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
   lce_status st = plan_gemm(o, dev, &pl);
   if (st != LCE_OK) return st;
   SwigluParams p{a, g, u, I};
+  cudaError_t e = pace(&pl, ctr, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pace");
   ProfScope ps(LCE_K_MLP_GATE_UP, s);
-  cudaError_t e = launch_gemm_swiglu(pl.pair, pl.ta, pl.tb, pl.tb2, pl.g, p,
-                                     dev.err, pl.grid, s);
+  e = launch_gemm_swiglu(pl.pair, pl.ta, pl.tb, pl.tb2, pl.g, p, dev.err,
+                         pl.grid, s);
   ps.done(2.0 * cr * H * 2 * I);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "mlp_gate_up");
 }
 
 // out (+)= scale * (A B) for the plain MLP contractions.
 lce_status mlp_store(const DeviceInfo& dev, const GemmOperands& o,
-                     const StoreParams& p, int kind, cudaStream_t s) {
+                     const StoreParams& p, int kind, void* ctr,
+                     cudaStream_t s) {
   GemmPlan pl;
   lce_status st = plan_gemm(o, dev, &pl);
   if (st != LCE_OK) return st;
+  cudaError_t e = pace(&pl, ctr, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pace");
   ProfScope ps(kind, s);
-  cudaError_t e = run_store(pl, o.a_mn, o.b_mn, p, dev.err, s);
+  e = run_store(pl, o.a_mn, o.b_mn, p, dev.err, s);
   ps.done(2.0 * o.M * o.N * o.K);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "mlp contraction");
 }
@@ -1323,7 +1348,7 @@ lce_status lce_mlp_forward(const void* x, const void* Wg, const void* Wu,
     const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * H;
     // a_c = silu(x_c Wg^T) * (x_c Wu^T)
     if ((st = mlp_gate_up(*dev, xc, cr, Wg, Wu, H, I, A, nullptr, nullptr,
-                          s)) != LCE_OK)
+                          wsb + w.sync, s)) != LCE_OK)
       return st;
     // y_c = a_c Wd^T
     StoreParams p{};
@@ -1332,7 +1357,7 @@ lce_status lce_mlp_forward(const void* x, const void* Wg, const void* Wu,
     p.out_f32 = 0;
     if ((st = mlp_store(*dev, {cr, H, I, false, false, A, I, Wd, I, false,
                                T_MLP},
-                        p, LCE_K_MLP_DOWN, s)) != LCE_OK)
+                        p, LCE_K_MLP_DOWN,wsb + w.sync, s)) != LCE_OK)
       return st;
   }
   return LCE_OK;
@@ -1365,7 +1390,8 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
     const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * H;
     const uint16_t* dyc = static_cast<const uint16_t*>(dy) + c0 * H;
     // (1) recompute g_c, u_c, a_c
-    if ((st = mlp_gate_up(*dev, xc, cr, Wg, Wu, H, I, A, G, U, s)) != LCE_OK)
+    if ((st = mlp_gate_up(*dev, xc, cr, Wg, Wu, H, I, A, G, U, wsb + w.sync,
+                          s)) != LCE_OK)
       return st;
     // (2) da_c = dy_c Wd -> dg_c, du_c into [dg | du]
     {
@@ -1373,9 +1399,11 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       GemmPlan pl;
       if ((st = plan_gemm(o, *dev, &pl)) != LCE_OK) return st;
       SwigluBwdParams p{G, U, I, DGU, 2 * I, I};
+      cudaError_t e = pace(&pl, wsb + w.sync, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_MLP_DA, s);
-      cudaError_t e = launch_gemm_swiglu_bwd(pl.pair, pl.ta, pl.tb, pl.tb2,
-                                             pl.g, p, dev->err, pl.grid, s);
+      e = launch_gemm_swiglu_bwd(pl.pair, pl.ta, pl.tb, pl.tb2, pl.g, p,
+                                 dev->err, pl.grid, s);
       ps.done(2.0 * cr * I * H);
       if (e != cudaSuccess) return cuda_fail(e, "mlp_da");
     }
@@ -1389,7 +1417,9 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       StoreParams p{};
       p.out = static_cast<uint16_t*>(dx) + c0 * H;
       p.ldo = H;
-      if ((st = mlp_store(*dev, o, p, LCE_K_MLP_DX, s)) != LCE_OK) return st;
+      if ((st = mlp_store(*dev, o, p, LCE_K_MLP_DX, wsb + w.sync, s)) !=
+          LCE_OK)
+        return st;
     }
     // (4) dWd (+)= dy_c^T a_c
     {
@@ -1400,7 +1430,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       p.accumulate = c0 > 0;
       if ((st = mlp_store(*dev, {H, I, cr, true, true, dyc, H, A, I, false,
                                  T_MLP},
-                          p, LCE_K_MLP_DWD, s)) != LCE_OK)
+                          p, LCE_K_MLP_DWD,wsb + w.sync, s)) != LCE_OK)
         return st;
     }
     // (5) [dWg ; dWu] (+)= [dg | du]^T x_c, rows >= I going to dWu
@@ -1414,7 +1444,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       p.accumulate = c0 > 0;
       if ((st = mlp_store(*dev, {2 * I, H, cr, true, true, DGU, 2 * I, xc, H,
                                  false, T_MLP},
-                          p, LCE_K_MLP_DWGU, s)) != LCE_OK)
+                          p, LCE_K_MLP_DWGU,wsb + w.sync, s)) != LCE_OK)
         return st;
     }
   }

@@ -897,7 +897,8 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
     const Unit t = decode_unit(g, u);
     const int m0 = t.m_blk * BM;
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
-      wave_wait(g, step * gridDim.x);
+      if (g.wave_period <= 1 || step % g.wave_period == 0)
+        wave_wait(g, step * gridDim.x);
       const int n0 = (t.n_first + tt) * BN;
       for (int kb = 0; kb < g.num_kb; ++kb) {
         if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
@@ -1306,7 +1307,8 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
     const int a0 = static_cast<int>(t.row0);  // this CTA's 128 rows of A
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
-      if (leader) wave_wait(g, step * static_cast<uint32_t>(nclusters));
+      if (leader && (g.wave_period <= 1 || step % g.wave_period == 0))
+        wave_wait(g, step * static_cast<uint32_t>(nclusters));
       // this CTA's 128 of the tile's 256 output columns; dual along N: the
       // leader takes the first map's 128 rows, the peer the second's
       const bool dual_n = g.b_dual == 1;

@@ -67,6 +67,7 @@ struct GemmGeom {
   unsigned* wave_ctr;
   uint32_t wave_wait_ns;
   uint32_t wave_steps;
+  uint32_t wave_period;  // wait before every wave_period-th tile only (>= 1)
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------
