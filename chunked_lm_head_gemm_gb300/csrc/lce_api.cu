@@ -228,12 +228,12 @@ lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
 // the tile grouping of tile-per-unit contractions; plus the L2 budget that
 // bounds the live A row panels when choosing column splits. Defaults are the
 // values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,kind.s=S,kind.p=P,
-// l2mb=M,pace_us=P" (kinds lse, grad, fused, dH, dW, test, mlp; H in 0..2;
+// l2mb=M,pace_us=P" (kinds lse, grad, fused, dH, dW, test, mlp, mlpgu; H in 0..2;
 // G >= 0; S >= 1, the placement stride GemmGeom::cl_stride; P the least
 // time in us between two wave-pacing waits, GemmGeom::wave_period, < 0 for
 // none; pace_us sets it for every kind) overrides them.
 enum TuneKind {
-  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_KINDS
+  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_MLP_GU, T_KINDS
 };
 struct Tune {
   int a_hint[T_KINDS];
@@ -250,11 +250,15 @@ const Tune& tune() {
   static Tune t = [] {
     Tune v{};
     v.l2_budget = 48e6;
-    v.pace_ns[T_MLP] = -1.0;  // the MLP contractions run unpaced
+    // the MLP contractions run unpaced: paced, the gate/up contraction (its
+    // heavy epilogue) and da lose more to the waits than dx, dWd and dWgu
+    // gain, and the MLP step measured the same either way
+    v.pace_ns[T_MLP] = -1.0;
+    v.pace_ns[T_MLP_GU] = -1.0;
     const char* env = std::getenv("LCE_TUNE");
     if (!env) return v;
     static const char* names[T_KINDS] = {"lse", "grad", "fused", "dH", "dW",
-                                         "test", "mlp"};
+                                         "test", "mlp", "mlpgu"};
     std::string spec(env);
     size_t pos = 0;
     while (pos < spec.size()) {
@@ -1277,7 +1281,7 @@ lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
                        const void* Wg, const void* Wu, int64_t H, int64_t I,
                        uint16_t* a, uint16_t* g, uint16_t* u, void* ctr,
                        cudaStream_t s) {
-  GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false, T_MLP};
+  GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false, T_MLP_GU};
   o.b_dual = 1;
   o.b2 = Wu;
   GemmPlan pl;
