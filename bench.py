@@ -62,6 +62,16 @@ def _flatten(d, out=None):
     return out
 
 
+# The pages' whole-step number for the workload that is exactly one GPU's
+# shard of their run: Qwen3-8B, one 1M-token sequence over 8 H100s, 131072
+# rows per GPU (TRL PR #6845 page, "TRL: document 1M-token training and add
+# a context-parallelism example", table under "Measured"). Context only.
+PAGES_STEP = {
+    "qwen3-8b": {"model": "Qwen3-8B", "tokens": 1048576, "gpus": "8 x H100",
+                 "s_per_step": 364.0, "peak_gb": 56.2},
+}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -714,6 +724,14 @@ def main():
             "cpu_baseline": cpu,
             "peak_extra_bytes": int(ws.numel()),
         }
+        ctx = PAGES_STEP.get(wl.name.split("[")[0])
+        if ctx and not args.rows:
+            out["pages_context"] = dict(
+                ctx, loss_share_of_step=(ms_per_step / 1e3) / ctx["s_per_step"],
+                note=("the pages' whole training step, of which this "
+                      "workload is one GPU's shard of the loss; context "
+                      "only; loss_share_of_step = this fwd+bwd time on one "
+                      "GB300 over that step time"))
         if comparator:
             out["comparator"] = comparator
         if vocab_par:
