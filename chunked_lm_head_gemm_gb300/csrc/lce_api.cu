@@ -181,7 +181,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 // elements of a box read as zero.
 lce_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner,
                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                     uint32_t box_outer) {
+                     uint32_t box_outer,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tmap_encoder();
   if (!enc) {
     std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error,
@@ -194,7 +195,7 @@ lce_status make_tmap(CUtensorMap* tm, const void* base, uint64_t inner,
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -221,6 +222,15 @@ lce_status tmap_kmajor(CUtensorMap* tm, const void* base, int64_t k_extent,
 lce_status tmap_mnmajor(CUtensorMap* tm, const void* base, int64_t mn_extent,
                         int64_t k_rows, int64_t row_elems) {
   return make_tmap(tm, base, mn_extent, k_rows, row_elems * 2, 64, BK);
+}
+
+// Store map of a bf16 [rows][row_elems] matrix of `cols` valid columns, in
+// the 32-row x 32-column boxes (64 bytes per row, 64-byte swizzle) that an
+// epilogue warp stages in shared memory (EPI_BOX).
+lce_status tmap_store_box(CUtensorMap* tm, const void* base, int64_t cols,
+                          int64_t rows, int64_t row_elems) {
+  return make_tmap(tm, base, cols, rows, row_elems * 2, EPI_BOX, EPI_BOX,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // ---- tuning of the contractions' memory behaviour -----------------------
@@ -485,16 +495,19 @@ cudaError_t run_lse(const GemmPlan& pl, const LseParams& p, unsigned* err,
   return pl.pair ? launch_gemm_pair_lse(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
                  : launch_gemm_lse(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
 }
-cudaError_t run_grad(const GemmPlan& pl, const GradParams& p, unsigned* err,
-                     cudaStream_t s) {
-  return pl.pair ? launch_gemm_pair_grad(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
-                 : launch_gemm_grad(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
+cudaError_t run_grad(const GemmPlan& pl, const GradParams& p,
+                     const CUtensorMap& tg, unsigned* err, cudaStream_t s) {
+  return pl.pair ? launch_gemm_pair_grad(pl.ta, pl.tb, tg, pl.g, p, err,
+                                         pl.grid, s)
+                 : launch_gemm_grad(pl.ta, pl.tb, tg, pl.g, p, err, pl.grid,
+                                    s);
 }
-cudaError_t run_fused(const GemmPlan& pl, const FusedParams& p, unsigned* err,
-                      cudaStream_t s) {
-  return pl.pair
-             ? launch_gemm_pair_fused(pl.ta, pl.tb, pl.g, p, err, pl.grid, s)
-             : launch_gemm_fused(pl.ta, pl.tb, pl.g, p, err, pl.grid, s);
+cudaError_t run_fused(const GemmPlan& pl, const FusedParams& p,
+                      const CUtensorMap& te, unsigned* err, cudaStream_t s) {
+  return pl.pair ? launch_gemm_pair_fused(pl.ta, pl.tb, te, pl.g, p, err,
+                                          pl.grid, s)
+                 : launch_gemm_fused(pl.ta, pl.tb, te, pl.g, p, err, pl.grid,
+                                     s);
 }
 cudaError_t run_store(const GemmPlan& pl, bool a_mn, bool b_mn,
                       const StoreParams& p, unsigned* err, cudaStream_t s) {
@@ -845,8 +858,10 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       p.v_total = V_total;
       e = pace(&pl, wsb + w.sync, s);
       if (e != cudaSuccess) return cuda_fail(e, "pace");
+      CUtensorMap tg;
+      if ((st = tmap_store_box(&tg, G, V, cr, w.ldg)) != LCE_OK) return st;
       ProfScope ps(LCE_K_GEMM_GRAD, s);
-      e = run_grad(pl, p, dev->err, s);
+      e = run_grad(pl, p, tg, dev->err, s);
       ps.done(2.0 * cr * V * H);
       if (e != cudaSuccess) return cuda_fail(e, "gemm_grad");
     }
@@ -1110,8 +1125,10 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       p.ignore_index = ignore_index;
       e = pace(&pl, wsb + w.sync, s);
       if (e != cudaSuccess) return cuda_fail(e, "pace");
+      CUtensorMap te;
+      if ((st = tmap_store_box(&te, E, V, cr, w.ldg)) != LCE_OK) return st;
       ProfScope ps(LCE_K_GEMM_FUSED, s);
-      e = run_fused(pl, p, dev->err, s);
+      e = run_fused(pl, p, te, dev->err, s);
       ps.done(2.0 * cr * V * H);
       if (e != cudaSuccess) return cuda_fail(e, "gemm_fused");
     }

@@ -147,6 +147,40 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
       : "memory");
 }
 
+// TMA bulk store of one 2D box from this CTA's shared memory to global
+// memory (bulk-group completion), and the group bookkeeping around it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm,
+                                             uint32_t src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], "
+      "[%1];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most one committed group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until every committed group has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make this thread's ordinary shared-memory writes visible to TMA reads.
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
+                                             uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 // One operand box: hinted when the contraction asks for it.
 __device__ __forceinline__ void tma_load_op(uint32_t dst, const CUtensorMap* tm,
                                             int32_t c0, int32_t c1,
@@ -377,10 +411,51 @@ __device__ __forceinline__ int first_unit(const GemmGeom& g, int slot,
 // epilogues: one thread per accumulator row, 32 columns per TMEM load
 // ---------------------------------------------------------------------------
 
+// What every epilogue may use besides its parameters: the store map and
+// the two shared-memory staging buffers of this warp (EPI_BUF_BYTES each,
+// 1 KB aligned, for 64-byte-swizzled EPI_BOX x EPI_BOX bf16 boxes), and how
+// many boxes this warp has handed to TMA so far. Set by the epilogue role.
+struct EpiBase {
+  const CUtensorMap* te = nullptr;
+  uint32_t stage = 0;
+  uint32_t nstored = 0;
+
+  // Warp-collective: the 32 x 32 bf16 box of this warp's rows [wrow0,
+  // wrow0 + 32) and columns [j0, j0 + 32), lane l holding row wrow0 + l in
+  // v, goes through this warp's next staging buffer (row r at r * 64 bytes,
+  // its 16-byte pieces in 64-byte-swizzle order) and out by one TMA store,
+  // which drops the rows and columns past the map's extent. Two buffers
+  // alternate; a buffer is reused once the store before last has read it.
+  __device__ __forceinline__ void store_box(const float (&v)[32], int64_t j0,
+                                            int64_t wrow0) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t buf = stage + (nstored & 1u) * EPI_BUF_BYTES;
+    if (lane == 0 && nstored >= 2) bulk_wait_read1();
+    __syncwarp();
+    const uint32_t rowa = buf + lane * 64u;
+    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(rowa + ((static_cast<uint32_t>(q) ^ sw) << 4),
+                   pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                   pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                   pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(te, buf, static_cast<int32_t>(j0),
+                   static_cast<int32_t>(wrow0));
+      bulk_commit();
+    }
+    ++nstored;
+  }
+};
+
 // Forward: per-row running (max, sum 2^(u-max)) in log2 units over the
 // unit's columns; the logit at the label is written by the one tile that
 // holds that column.
-struct EpiLse {
+struct EpiLse : EpiBase {
   using Params = LseParams;
   float m2, s;
   int64_t row;
@@ -449,7 +524,7 @@ struct EpiLse {
 // Backward recompute: G = exp(z - lse) - [j == y] for rows that take part,
 // 0 for the others, rounded to bf16. The dloss/N scale is applied later, in
 // fp32, by the dH and dW epilogues.
-struct EpiGrad {
+struct EpiGrad : EpiBase {
   using Params = GradParams;
   int64_t row;
   bool row_ok;
@@ -481,7 +556,6 @@ struct EpiGrad {
       if (j0 >= g.N) break;
       float v[32];
       tmem_ld32(taddr + c * 32, v);
-      if (!row_ok) continue;
       const int yo = yv - static_cast<int>(j0);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -489,21 +563,9 @@ struct EpiGrad {
         if (i == yo) gi -= 1.f;
         v[i] = gi;
       }
-      uint16_t* dst = p.G + row * p.ldg + j0;
-      if (j0 + 32 <= g.N) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                             pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                             pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      } else {
-        const int nv = static_cast<int>(g.N - j0);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nv) dst[i] = to_bf16_bits(v[i]);
-      }
+      // rows past M and columns past N hold junk that the store drops
+      const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
+      if (wrow0 < g.M) store_box(v, j0, wrow0);  // warp-uniform test
     }
   }
 
@@ -517,7 +579,7 @@ struct EpiGrad {
 // sums the fp32 values. (m_t, sum) then merge into the row's running
 // (max, sum) exactly as in EpiLse, and m_t is stored so that a later pass
 // can turn e into softmax - onehot once the row's lse is known.
-struct EpiFused {
+struct EpiFused : EpiBase {
   using Params = FusedParams;
   float m2, s;
   int64_t row;
@@ -565,8 +627,13 @@ struct EpiFused {
         if (i < nv) mx[i & 3] = fmaxf(mx[i & 3], v[i] * LOG2E);
     }
     const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    // pass 2: exponentials relative to the tile maximum
+    // pass 2: exponentials relative to the tile maximum. Each 32-column
+    // chunk of the warp's 32 rows goes through a shared-memory box (row r
+    // at r * 64 bytes, its 16-byte pieces in 64-byte-swizzle order) and out
+    // by one TMA store, which writes whole rows' segments and drops the
+    // rows past M and the columns past N.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int64_t j0 = n0 + c * 32;
@@ -580,21 +647,7 @@ struct EpiFused {
         v[i] = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
         acc[i & 3] += v[i];
       }
-      if (!row_ok) continue;
-      uint16_t* dst = p.E + row * p.ldg + j0;
-      if (nv == 32) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                             pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                             pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nv) dst[i] = to_bf16_bits(v[i]);
-      }
+      if (wrow0 < g.M) store_box(v, j0, wrow0);  // warp-uniform test
     }
     const float st = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     const float mn = fmaxf(m2, mt);
@@ -614,7 +667,7 @@ struct EpiFused {
 
 // out[row][col] (+)= scale * acc, fp32 or bf16. scale = dloss / N when the
 // parameters carry them (N = 0 gives 0; a missing dloss counts as 1), else 1.
-struct EpiStore {
+struct EpiStore : EpiBase {
   using Params = StoreParams;
   int64_t row;
   bool row_ok;
@@ -710,7 +763,7 @@ __device__ __forceinline__ float sigmoid_fast(float t) {
 // Gated-MLP gate/up contraction with B dual along N: for the tile's 128
 // output columns, accumulator columns 0..127 are g and 128..255 are u;
 // writes a = silu(g) u (and g, u when asked) in bf16.
-struct EpiSwiGLU {
+struct EpiSwiGLU : EpiBase {
   using Params = SwigluParams;
   int64_t row;
   bool row_ok;
@@ -767,7 +820,7 @@ struct EpiSwiGLU {
 
 // Gated-MLP backward: accumulator = da; dg = da u silu'(g),
 // du = da silu(g), with silu'(t) = s (1 + t (1 - s)), s the logistic.
-struct EpiSwiGLUBwd {
+struct EpiSwiGLUBwd : EpiBase {
   using Params = SwigluBwdParams;
   int64_t row;
   bool row_ok;
@@ -1012,11 +1065,14 @@ __device__ __forceinline__ void role_epilogue(const GemmGeom& g,
                                               const SmemMap& sm,
                                               uint32_t tmem_base,
                                               const WaitCtx& ctx, int warp,
-                                              int lane) {
+                                              int lane, const CUtensorMap* te,
+                                              uint32_t stage_base) {
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const int r = q * 32 + lane;
   uint32_t acc = 0, acc_phase = 0;
   Epi epi;
+  epi.te = te;
+  epi.stage = stage_base + static_cast<uint32_t>(q) * 2u * EPI_BUF_BYTES;
   for (int u = first_unit(g, blockIdx.x, gridDim.x); u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     epi.begin_unit(p, g, t, r);
@@ -1036,9 +1092,13 @@ __device__ __forceinline__ void role_epilogue(const GemmGeom& g,
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (!ok) return;
+    if (!ok) break;
     epi.end_unit(p, g, t, r);
   }
+  // every TMA store of this warp has finished reading shared memory and
+  // writing global memory before the CTA may exit
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 template <class Epi, bool A_MN, bool B_MN>
@@ -1096,7 +1156,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) role_mma<A_MN, B_MN>(g, sm, tmem_base, ctx);
     __syncwarp();
   } else {
-    role_epilogue<Epi>(g, p, sm, tmem_base, ctx, warp, lane);
+    role_epilogue<Epi>(g, p, sm, tmem_base, ctx, warp, lane, &tb2,
+                       base + STAGES * STAGE_BYTES + 1024);
   }
 
   tc_fence_before();
@@ -1424,13 +1485,15 @@ template <class Epi>
 __device__ __forceinline__ void role_epilogue_pair(
     const GemmGeom& g, const typename Epi::Params& p, const SmemMap2& sm,
     uint32_t tmem_base, uint32_t rank, const WaitCtx& ctx, int warp,
-    int lane) {
+    int lane, const CUtensorMap* te, uint32_t stage_base) {
   const int q = warp & 3;
   const int r = q * 32 + lane;
   const int nclusters = gridDim.x >> 1;
   const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
   uint32_t acc = 0, acc_phase = 0;
   Epi epi;
+  epi.te = te;
+  epi.stage = stage_base + static_cast<uint32_t>(q) * 2u * EPI_BUF_BYTES;
   for (int u = cluster; u < g.num_units; u += nclusters) {
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
     epi.begin_unit(p, g, t, r);
@@ -1451,9 +1514,13 @@ __device__ __forceinline__ void role_epilogue_pair(
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (!ok) return;
+    if (!ok) break;
     epi.end_unit(p, g, t, r);
   }
+  // every TMA store of this warp has finished reading shared memory and
+  // writing global memory before the CTA may exit
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 template <class Epi, bool A_MN, bool B_MN>
@@ -1515,7 +1582,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0 && rank == 0) role_mma_pair<A_MN, B_MN>(g, sm, tmem_base, ctx);
     __syncwarp();
   } else {
-    role_epilogue_pair<Epi>(g, p, sm, tmem_base, rank, ctx, warp, lane);
+    role_epilogue_pair<Epi>(g, p, sm, tmem_base, rank, ctx, warp, lane, &tb2,
+                            base + STAGES2 * STAGE2_BYTES + 1024);
   }
 
   tc_fence_before();
@@ -1529,7 +1597,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-constexpr int GEMM2_SMEM_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 256;
+constexpr int GEMM2_SMEM_BYTES =
+    1024 + STAGES2 * STAGE2_BYTES + 1024 + EPI_STAGE_BYTES;
 
 template <class Epi, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb,

@@ -16,16 +16,24 @@ cudaError_t launch_gemm_lse(const CUtensorMap& ta, const CUtensorMap& tb,
   return launch_gemm_t<EpiLse, false, false>(ta, tb, g, p, err, grid, s);
 }
 
+// tg: store map of the chunk's gradient logits (tmap_store_box), handed to
+// the kernel in the second-B slot, which this contraction does not use.
 cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
-                             const GemmGeom& g, const GradParams& p,
-                             unsigned* err, int grid, cudaStream_t s) {
-  return launch_gemm_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s);
+                             const CUtensorMap& tg, const GemmGeom& g,
+                             const GradParams& p, unsigned* err, int grid,
+                             cudaStream_t s) {
+  return launch_gemm_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s,
+                                              &tg);
 }
 
+// te: store map of the chunk's exponentials (tmap_store_box), handed to the
+// kernel in the second-B slot, which this contraction does not use.
 cudaError_t launch_gemm_fused(const CUtensorMap& ta, const CUtensorMap& tb,
-                              const GemmGeom& g, const FusedParams& p,
-                              unsigned* err, int grid, cudaStream_t s) {
-  return launch_gemm_t<EpiFused, false, false>(ta, tb, g, p, err, grid, s);
+                              const CUtensorMap& te, const GemmGeom& g,
+                              const FusedParams& p, unsigned* err, int grid,
+                              cudaStream_t s) {
+  return launch_gemm_t<EpiFused, false, false>(ta, tb, g, p, err, grid, s,
+                                               &te);
 }
 
 cudaError_t launch_gemm_pair_lse(const CUtensorMap& ta, const CUtensorMap& tb,
@@ -35,17 +43,20 @@ cudaError_t launch_gemm_pair_lse(const CUtensorMap& ta, const CUtensorMap& tb,
 }
 
 cudaError_t launch_gemm_pair_grad(const CUtensorMap& ta, const CUtensorMap& tb,
-                                  const GemmGeom& g, const GradParams& p,
-                                  unsigned* err, int grid, cudaStream_t s) {
-  return launch_gemm_pair_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s);
+                                  const CUtensorMap& tg, const GemmGeom& g,
+                                  const GradParams& p, unsigned* err, int grid,
+                                  cudaStream_t s) {
+  return launch_gemm_pair_t<EpiGrad, false, false>(ta, tb, g, p, err, grid, s,
+                                                   &tg);
 }
 
 cudaError_t launch_gemm_pair_fused(const CUtensorMap& ta,
-                                   const CUtensorMap& tb, const GemmGeom& g,
+                                   const CUtensorMap& tb,
+                                   const CUtensorMap& te, const GemmGeom& g,
                                    const FusedParams& p, unsigned* err,
                                    int grid, cudaStream_t s) {
   return launch_gemm_pair_t<EpiFused, false, false>(ta, tb, g, p, err, grid,
-                                                    s);
+                                                    s, &te);
 }
 
 }  // namespace lce

@@ -18,7 +18,13 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;           // 6 warps: TMA, MMA, 4 x epilogue
-constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// Epilogue staging for TMA stores: per epilogue warp two buffers of one
+// EPI_BOX x EPI_BOX bf16 box (32 rows x 64 bytes), after the barriers.
+constexpr int EPI_BOX = 32;
+constexpr int EPI_BUF_BYTES = EPI_BOX * EPI_BOX * 2;     // 2 KB
+constexpr int EPI_STAGE_BYTES = 4 * 2 * EPI_BUF_BYTES;  // 16 KB
+constexpr int GEMM_SMEM_BYTES =
+    1024 + STAGES * STAGE_BYTES + 1024 + EPI_STAGE_BYTES;
 constexpr int TMEM_COLS = 512;              // two 256-column accumulators
 
 // Rows per block of the per-row combine kernels (one float64 loss sum per
@@ -92,7 +98,8 @@ struct LseParams {
 struct GradParams {
   const int64_t* labels;  // [M], rows of this chunk
   const float* lse;       // [M], rows of this chunk
-  uint16_t* G;            // [M][ldg] bf16 bits
+  uint16_t* G;            // [M][ldg] bf16 bits (the kernel writes it through
+                          // the store map launched with it, not this pointer)
   int64_t ldg;
   int64_t ignore_index;
   int64_t v0, v_total;    // vocabulary slice, as LseParams
@@ -107,7 +114,8 @@ struct FusedParams {
   float* part_m;          // [splits][M]
   float* part_s;          // [splits][M]
   float* zy;              // [M]
-  uint16_t* E;            // [M][ldg] bf16 bits
+  uint16_t* E;            // [M][ldg] bf16 bits (written through the store
+                          // map launched with the kernel)
   int64_t ldg;
   float* tile_max;        // [M][num_n], log2 units
   int64_t ignore_index;
@@ -168,9 +176,11 @@ cudaError_t launch_gemm_swiglu_bwd(bool pair, const CUtensorMap& ta,
                                    int grid, cudaStream_t s);
 
 cudaError_t launch_gemm_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                             const CUtensorMap& tg,
                              const GemmGeom& g, const GradParams& p,
                              unsigned* err, int grid, cudaStream_t s);
 cudaError_t launch_gemm_fused(const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& te,
                               const GemmGeom& g, const FusedParams& p,
                               unsigned* err, int grid, cudaStream_t s);
 cudaError_t launch_gemm_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
@@ -186,10 +196,12 @@ cudaError_t launch_gemm_pair_lse(const CUtensorMap& ta, const CUtensorMap& tb,
                                  const GemmGeom& g, const LseParams& p,
                                  unsigned* err, int grid, cudaStream_t s);
 cudaError_t launch_gemm_pair_grad(const CUtensorMap& ta, const CUtensorMap& tb,
+                                  const CUtensorMap& tg,
                                   const GemmGeom& g, const GradParams& p,
                                   unsigned* err, int grid, cudaStream_t s);
 cudaError_t launch_gemm_pair_fused(const CUtensorMap& ta,
-                                   const CUtensorMap& tb, const GemmGeom& g,
+                                   const CUtensorMap& tb,
+                                   const CUtensorMap& te, const GemmGeom& g,
                                    const FusedParams& p, unsigned* err,
                                    int grid, cudaStream_t s);
 cudaError_t launch_gemm_pair_store(bool a_mn, bool b_mn, const CUtensorMap& ta,
