@@ -297,25 +297,45 @@ def time_vocab_slice(lce, B, h, W, y, P: int, chunk: int, steps: int,
         B.backward_slice(h, Ws, y, lse, d, 0, V, chunk_rows=chunk,
                          workspace=ws)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    if lce.get_error() != 0:
-        raise RuntimeError("device error in the vocabulary-slice step")
-    ms = e0.elapsed_time(e1) / steps
+    wsx = B.slice_exp_workspace(L, H, Vs, h.dtype, h.device)
+
+    def step_exp():
+        m, s, zy = B.forward_slice_exp(h, Ws, y, 0, V, wsx)
+        st = torch.stack([m, s, zy]).unsqueeze(0).expand(P, 3, L)
+        loss, lse = B.combine_slices(st[:, 0].contiguous(),
+                                     st[:, 1].contiguous(),
+                                     st[:, 2].contiguous(), y, V)
+        B.backward_slice_exp(h, Ws, y, lse, d, 0, V, wsx)
+
+    def timed_ms(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        if lce.get_error() != 0:
+            raise RuntimeError("device error in the vocabulary-slice step")
+        return e0.elapsed_time(e1) / steps
+
+    ms = timed_ms(step)
+    ms_exp = timed_ms(step_exp)
+    del wsx
     return {"shards": P, "slice_rows": Vs, "ms_per_step_per_process": ms,
             "tokens_per_s": L / (ms / 1e3),
             "tflops_per_process_executed": 8.0 * L * H * Vs / (ms / 1e3)
             / 1e12,
-            "note": "forward slice + merge + recomputing backward slice; "
-                    "collectives not timed"}
+            "keep_exp": {"ms_per_step_per_process": ms_exp,
+                         "tokens_per_s": L / (ms_exp / 1e3),
+                         "tflops_per_process_executed":
+                             6.0 * L * H * Vs / (ms_exp / 1e3) / 1e12},
+            "note": "forward slice + merge + recomputing backward slice "
+                    "(keep_exp: the slice's exponentials kept between the "
+                    "two, no recompute); collectives not timed"}
 
 
 def time_torch_chunked(h, W, y, chunk_rows: int, steps: int,

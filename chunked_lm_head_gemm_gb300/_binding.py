@@ -40,7 +40,8 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_mlp_forward", "lce_mlp_backward", "lce_count_valid",
             "lce_forward_slice", "lce_combine_workspace_size",
             "lce_combine_slices", "lce_backward_slice", "lce_set_wave_sync",
-            "lce_get_wave_sync")
+            "lce_get_wave_sync", "lce_slice_exp_workspace_size",
+            "lce_forward_slice_exp", "lce_backward_slice_exp")
 
 KERNEL_KINDS = 21
 
@@ -119,6 +120,16 @@ def load(build_if_missing: bool = False):
                                            i64, i64, i64, p, i64, p, p, p, sz,
                                            p]
         lib.lce_backward_slice.restype = i32
+        lib.lce_slice_exp_workspace_size.argtypes = [i64, i64, i64, i32]
+        lib.lce_slice_exp_workspace_size.restype = sz
+        lib.lce_forward_slice_exp.argtypes = [p, p, i32, p, i64, i64, i64,
+                                              i64, i64, i64, p, p, p, p, sz,
+                                              p]
+        lib.lce_forward_slice_exp.restype = i32
+        lib.lce_backward_slice_exp.argtypes = [p, p, i32, p, p, i64, i64, i64,
+                                               i64, i64, i64, p, p, p, p, sz,
+                                               p]
+        lib.lce_backward_slice_exp.restype = i32
         lib.lce_mlp_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.lce_mlp_workspace_size.restype = sz
         lib.lce_mlp_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p,
@@ -380,6 +391,61 @@ def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
                                 workspace.data_ptr(), workspace.numel(),
                                 _stream_ptr(dev))
     _check(st, "lce_backward_slice")
+    return dH, dW
+
+
+def slice_exp_workspace(L: int, H: int, Vs: int, dtype, device):
+    """The workspace forward_slice_exp fills and backward_slice_exp reads."""
+    n = load().lce_slice_exp_workspace_size(
+        L, H, Vs, LCE_F32 if dtype == torch.float32 else LCE_BF16)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def forward_slice_exp(h, W_slice, labels, v0: int, V_total: int, workspace,
+                      ignore_index: int = IGNORE_INDEX, out=None):
+    """forward_slice that also keeps the slice's tile exponentials in
+    `workspace` (from slice_exp_workspace) for backward_slice_exp."""
+    lib = load()
+    _check_inputs(h, W_slice, labels)
+    L, H = h.shape
+    Vs = W_slice.shape[0]
+    if out is None:
+        out = torch.empty(3, L, dtype=torch.float32, device=h.device)
+    m, s, zy = out[0], out[1], out[2]
+    st = lib.lce_forward_slice_exp(h.data_ptr(), W_slice.data_ptr(),
+                                   _dtype_code(h), labels.data_ptr(), L, H,
+                                   Vs, v0, V_total, ignore_index,
+                                   m.data_ptr(), s.data_ptr(), zy.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel(),
+                                   _stream_ptr(h.device))
+    _check(st, "lce_forward_slice_exp")
+    return m, s, zy
+
+
+def backward_slice_exp(h, W_slice, labels, lse, dloss, v0: int, V_total: int,
+                       workspace, ignore_index: int = IGNORE_INDEX):
+    """The slice's backward from the exponentials forward_slice_exp kept:
+    returns (dH_part [L,H] float32, dW_slice [Vs,H] float32)."""
+    lib = load()
+    _check_inputs(h, W_slice, labels)
+    L, H = h.shape
+    Vs = W_slice.shape[0]
+    dev = h.device
+    if lse.dtype != torch.float32 or lse.shape != (L,) or not lse.is_cuda:
+        raise ValueError("lse must be a CUDA float32 [L] tensor")
+    dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
+    dH = torch.empty(L, H, dtype=torch.float32, device=dev)
+    dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
+    st = lib.lce_backward_slice_exp(h.data_ptr(), W_slice.data_ptr(),
+                                    _dtype_code(h), labels.data_ptr(),
+                                    lse.data_ptr(), L, H, Vs, v0, V_total,
+                                    ignore_index, dloss.data_ptr(),
+                                    dH.data_ptr(), dW.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel(),
+                                    _stream_ptr(dev))
+    _check(st, "lce_backward_slice_exp")
     return dH, dW
 
 

@@ -1004,6 +1004,177 @@ lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
   return LCE_OK;
 }
 
+size_t lce_slice_exp_workspace_size(int64_t L, int64_t H, int64_t Vs,
+                                    lce_dtype dt) {
+  if (!sizes_ok(L, H, Vs) || (dt != LCE_BF16 && dt != LCE_F32)) return 0;
+  return ws_layout(L, H, Vs, dt, L).total;
+}
+
+lce_status lce_forward_slice_exp(const void* h, const void* W, lce_dtype dt,
+                                 const int64_t* labels, int64_t L, int64_t H,
+                                 int64_t Vs, int64_t v0, int64_t V_total,
+                                 int64_t ignore_index, float* m, float* s_out,
+                                 float* zy, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!h || !W || !labels || !m || !s_out || !zy || !ws)
+    return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
+    return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(m) & 3u) ||
+      (reinterpret_cast<uintptr_t>(s_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(zy) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, Vs, dt, L);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, Vs, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid,
+                           dev->err, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+  // every row's logits once: statistics + tile exponentials kept in ws
+  GemmPlan pl;
+  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true, T_FUSED},
+                      *dev, &pl)) != LCE_OK)
+    return st;
+  uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
+  FusedParams p{};
+  p.labels = labels;
+  p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
+  p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  p.zy = reinterpret_cast<float*>(wsb + w.zy);
+  p.E = E;
+  p.ldg = w.ldg;
+  p.tile_max = reinterpret_cast<float*>(wsb + w.tile_max);
+  p.ignore_index = ignore_index;
+  p.v0 = v0;
+  p.v_total = V_total;
+  CUtensorMap te;
+  if ((st = tmap_store_box(&te, E, Vs, L, w.ldg)) != LCE_OK) return st;
+  e = pace(&pl, wsb + w.sync, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pace");
+  {
+    ProfScope ps(LCE_K_GEMM_FUSED, s);
+    e = run_fused(pl, p, te, dev->err, s);
+    ps.done(2.0 * L * Vs * H);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_fused");
+  {
+    ProfScope ps(LCE_K_SLICE_STATS, s);
+    e = launch_slice_stats(p.part_m, p.part_s, pl.g.splits, p.zy, labels, L,
+                           v0, Vs, V_total, ignore_index, m, s_out, zy, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "slice_stats");
+  return LCE_OK;
+}
+
+lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
+                                  const int64_t* labels, const float* lse,
+                                  int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                                  int64_t V_total, int64_t ignore_index,
+                                  const float* dloss, float* dH_part,
+                                  float* dW, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!h || !W || !labels || !lse || !dloss || !dH_part || !dW || !ws)
+    return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
+  if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
+    return LCE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
+      !aligned16(dH_part) || !aligned16(dW) ||
+      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dloss) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(L, H, Vs, dt, L);
+  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void *hb = nullptr, *Wb = nullptr;
+  if ((st = operands(h, W, dt, L, H, Vs, w, wsb, s, &hb, &Wb)) != LCE_OK)
+    return st;
+  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
+  uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
+  const int num_n = static_cast<int>(ceil_div(Vs, BN));
+  cudaError_t e;
+  {
+    ProfScope ps(LCE_K_COUNT_VALID, s);
+    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid,
+                           dev->err, s);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
+  // the kept exponentials -> softmax - onehot with the merged lse
+  {
+    ProfScope ps(LCE_K_GRAD_FROM_EXP, s);
+    e = launch_grad_from_exp(E, w.ldg,
+                             reinterpret_cast<float*>(wsb + w.tile_max), num_n,
+                             lse, labels, L, Vs, ignore_index, dev->num_sms, s,
+                             v0, V_total);
+    ps.done(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
+  // dH_part = (dloss/N) G W_s: M = L, N = H, K = Vs
+  {
+    GemmPlan pl;
+    if ((st = plan_gemm({L, H, Vs, false, true, E, w.ldg, Wb, H, false, T_DH},
+                        *dev, &pl)) != LCE_OK)
+      return st;
+    StoreParams p{};
+    p.out = dH_part;
+    p.ldo = H;
+    p.out_f32 = 1;
+    p.accumulate = 0;
+    p.dloss = dloss;
+    p.n_valid = n_valid;
+    e = pace(&pl, wsb + w.sync, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pace");
+    ProfScope ps(LCE_K_GEMM_DH, s);
+    e = run_store(pl, false, true, p, dev->err, s);
+    ps.done(2.0 * L * H * Vs);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
+  }
+  // dW_s = (dloss/N) G^T h: M = Vs, N = H, K = L, written once
+  {
+    GemmPlan pl;
+    if ((st = plan_gemm({Vs, H, L, true, true, E, w.ldg, hb, H, false, T_DW},
+                        *dev, &pl)) != LCE_OK)
+      return st;
+    StoreParams p{};
+    p.out = dW;
+    p.ldo = H;
+    p.out_f32 = 1;
+    p.accumulate = 0;
+    p.dloss = dloss;
+    p.n_valid = n_valid;
+    e = pace(&pl, wsb + w.sync, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pace");
+    ProfScope ps(LCE_K_GEMM_DW, s);
+    e = run_store(pl, true, true, p, dev->err, s);
+    ps.done(2.0 * Vs * H * L);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_dW");
+  }
+  return LCE_OK;
+}
+
 size_t lce_combine_workspace_size(int64_t L) {
   if (L < 1) return 0;
   return 256 + static_cast<size_t>(ceil_div(L, COMBINE_ROWS)) * 8;

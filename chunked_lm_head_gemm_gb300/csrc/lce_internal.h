@@ -249,11 +249,14 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
                                cudaStream_t s);
 // In place over one row chunk: E[i][j] = 2^(u - tile max) becomes
 // G = 2^(tile max - lse_i log2 e) E - [j == y_i] (bf16), 0 on ignored rows.
+// For a vocabulary slice (v0, v_total as LseParams) the onehot sits at
+// column y_i - v0 and validity is judged against v_total.
 cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* tile_max, int64_t num_n,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
-                                 int num_sms, cudaStream_t s);
+                                 int num_sms, cudaStream_t s,
+                                 int64_t v0 = 0, int64_t v_total = 0);
 // dH *= dloss[0] (bf16 or fp32) and dW *= dloss[0], skipped when dloss is 1.
 cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
                                int64_t n_dw, const float* dloss,

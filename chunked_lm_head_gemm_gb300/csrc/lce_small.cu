@@ -268,8 +268,10 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
                     const float* __restrict__ tile_max, int64_t num_n,
                     const float* __restrict__ lse,
                     const int64_t* __restrict__ labels, int64_t rows,
-                    int64_t V, int64_t ignore_index) {
+                    int64_t V, int64_t ignore_index, int64_t slice_v0,
+                    int64_t v_total) {
   const int64_t nvec = (V + 7) / 8;
+  const int64_t vt = v_total > 0 ? v_total : V;
   const int64_t total = rows * nvec;
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   int64_t pos = static_cast<int64_t>(blockIdx.x) * per;
@@ -281,13 +283,16 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
     pos += ve - vb;
     const int64_t y = labels[row];
     uint4* er = reinterpret_cast<uint4*>(E + row * ldg);
-    if (!label_valid(y, V, ignore_index)) {
+    if (!label_valid(y, vt, ignore_index)) {
       for (int64_t v = vb + threadIdx.x; v < ve; v += GFE_THREADS)
         er[v] = make_uint4(0u, 0u, 0u, 0u);
       continue;
     }
     const float l2 = lse[row] * LOG2E;
     const float* tm = tile_max + row * num_n;
+    // the label's column in this slice, or far below any column
+    const int64_t yl = y - slice_v0;
+    const int ycol = (yl >= 0 && yl < V) ? static_cast<int>(yl) : -(1 << 30);
     for (int64_t v0 = vb + threadIdx.x; v0 < ve;
          v0 += static_cast<int64_t>(GFE_U) * GFE_THREADS) {
       uint4 in[GFE_U];
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
         if (v < ve) {
           const int64_t j0 = v * 8;
           er[v] = exp_to_grad(in[k], ex2(tm[j0 >> 8] - l2),
-                              static_cast<int>(y - j0));
+                              ycol - static_cast<int>(j0));
         }
       }
     }
@@ -313,7 +318,8 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* tile_max, int64_t num_n,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
-                                 int num_sms, cudaStream_t s) {
+                                 int num_sms, cudaStream_t s, int64_t v0,
+                                 int64_t v_total) {
   const int64_t work = rows * ((V + 7) / 8);
   const int64_t full = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) *
                        GFE_BLOCKS_PER_SM;
@@ -321,7 +327,8 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
   const unsigned grid =
       static_cast<unsigned>(want < full ? (want < 1 ? 1 : want) : full);
   k_grad_from_exp<<<grid, GFE_THREADS, 0, s>>>(E, ldg, tile_max, num_n, lse,
-                                               labels, rows, V, ignore_index);
+                                               labels, rows, V, ignore_index,
+                                               v0, v_total);
   return cudaGetLastError();
 }
 

@@ -76,3 +76,33 @@ def backward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
                                    V_total, ignore_index, chunk_rows,
                                    workspace)
     return sum_partials(dH_part, group), dW
+
+
+def exp_workspace(h: torch.Tensor, W_slice: torch.Tensor) -> torch.Tensor:
+    """Workspace for forward_exp / backward_exp (L x round_up(Vs, 8) bf16
+    exponentials and their tile maxima, plus the usual statistics)."""
+    return B.slice_exp_workspace(h.shape[0], h.shape[1], W_slice.shape[0],
+                                 h.dtype, h.device)
+
+
+def forward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
+                v0: int, V_total: int, workspace: torch.Tensor, group=None,
+                ignore_index: int = B.IGNORE_INDEX):
+    """forward, keeping this slice's exponentials in `workspace` so that
+    backward_exp need not recompute the logits."""
+    m, s, zy = B.forward_slice_exp(h, W_slice, labels, v0, V_total, workspace,
+                                   ignore_index)
+    allst = gather_stats(torch.stack([m, s, zy]), group)
+    return B.combine_slices(allst[:, 0].contiguous(), allst[:, 1].contiguous(),
+                            allst[:, 2].contiguous(), labels, V_total,
+                            ignore_index)
+
+
+def backward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
+                 lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
+                 workspace: torch.Tensor, group=None,
+                 ignore_index: int = B.IGNORE_INDEX):
+    """backward from the exponentials forward_exp kept (same workspace)."""
+    dH_part, dW = B.backward_slice_exp(h, W_slice, labels, lse, dloss, v0,
+                                       V_total, workspace, ignore_index)
+    return sum_partials(dH_part, group), dW

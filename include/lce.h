@@ -225,6 +225,39 @@ lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
                               size_t ws_bytes, void* stream);
 
 /*
+ * The same vocabulary slice without recomputing its logits in the backward
+ * (the recompute-free form of lce_forward_backward, split at the exchange):
+ * lce_forward_slice_exp returns what lce_forward_slice returns and also
+ * keeps, in ws, each row's bf16 exponentials relative to each 256-column
+ * tile's maximum and those maxima; after the caller has merged the slices'
+ * statistics into lse (lce_combine_slices), lce_backward_slice_exp turns
+ * them in place into G_s = dloss/N (softmax - onehot) and computes dH_part
+ * (fp32 [L][H], summed over the slices by the caller) and the slice's dW
+ * (fp32 [Vs][H], written, not accumulated). Executes 6 L H Vs flops per
+ * slice instead of the 8 L H Vs of lce_forward_slice + lce_backward_slice,
+ * for L x round_up(Vs, 8) x 2 bytes of workspace (5 GB for L = 131072 rows
+ * and a 151936 / 8 slice).
+ *   ws  lce_slice_exp_workspace_size(L, H, Vs, dt) bytes, the same buffer
+ *       for both calls and untouched in between; other arguments as
+ *       lce_forward_slice and lce_backward_slice.
+ */
+size_t lce_slice_exp_workspace_size(int64_t L, int64_t H, int64_t Vs,
+                                    lce_dtype dt);
+lce_status lce_forward_slice_exp(const void* h, const void* W, lce_dtype dt,
+                                 const int64_t* labels, int64_t L, int64_t H,
+                                 int64_t Vs, int64_t v0, int64_t V_total,
+                                 int64_t ignore_index, float* m, float* s,
+                                 float* zy, void* ws, size_t ws_bytes,
+                                 void* stream);
+lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
+                                  const int64_t* labels, const float* lse,
+                                  int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                                  int64_t V_total, int64_t ignore_index,
+                                  const float* dloss, float* dH_part,
+                                  float* dW, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/*
  * Count of rows that take part in the loss: n_valid[0] = #{i : labels[i] !=
  * ignore_index and 0 <= labels[i] < V}. A label that is neither raises
  * LCE_ERR_LABEL_RANGE in the device error word and is not counted, as in

@@ -107,6 +107,13 @@ def test_bad_arguments_return_before_any_device_call(lib):
                                   1 << 20, null) == 1
     assert lib.lce_combine_slices(p, p, p, 2, p, 8, 10, -100, p, p, p, 8,
                                   null) == 3
+    assert lib.lce_forward_slice_exp(p, p, 0, p, 8, 8, 8, 4, 10, -100, p, p,
+                                     p, p, 1 << 30, null) == 1
+    assert lib.lce_backward_slice_exp(p, p, 0, p, p, 8, 8, 8, 0, 10, -100, p,
+                                      p, p, p, 16, null) == 3
+    assert lib.lce_slice_exp_workspace_size(0, 8, 8, 0) == 0
+    # the kept exponentials dominate: L x round_up(Vs, 8) x 2 bytes
+    assert lib.lce_slice_exp_workspace_size(1024, 64, 1000, 0) >= 1024 * 1000 * 2
     assert lib.lce_combine_workspace_size(0) == 0
     assert lib.lce_combine_workspace_size(300) == 256 + 2 * 8
     # test hooks

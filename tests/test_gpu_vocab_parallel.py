@@ -48,17 +48,25 @@ def _inputs(name, L, H, V, seed=11):
     return make_inputs(wl, seed=seed, device=require_gpu())
 
 
+@pytest.mark.parametrize("keep", [False, True], ids=["recompute", "keep_exp"])
 @pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
 @pytest.mark.parametrize("name,L,H,V,sizes,chunk", CASES,
                          ids=[c[0] for c in CASES])
-def test_slices_forward_backward(name, L, H, V, sizes, chunk, pair):
+def test_slices_forward_backward(name, L, H, V, sizes, chunk, pair, keep):
     h, W, y = _inputs(name, L, H, V)
     hc, Wc, yc = h.cpu(), W.cpu(), y.cpu()
     dloss = torch.full((), 0.5, device=h.device)
+    # keep: each slice keeps its exponentials in its own workspace
+    wss = [B.slice_exp_workspace(L, H, Vs, h.dtype, h.device) if keep
+           else None for _, Vs in _bounds(sizes)]
     with cta_pair(pair):
         stats = []
-        for v0, Vs in _bounds(sizes):
-            m, s, zy = B.forward_slice(h, W[v0:v0 + Vs], y, v0, V)
+        for k, (v0, Vs) in enumerate(_bounds(sizes)):
+            if keep:
+                m, s, zy = B.forward_slice_exp(h, W[v0:v0 + Vs], y, v0, V,
+                                               wss[k])
+            else:
+                m, s, zy = B.forward_slice(h, W[v0:v0 + Vs], y, v0, V)
             stats.append(torch.stack([m, s, zy]))
             # the slice's own statistics against the oracle on its columns
             f_s, local = _slice_oracle(hc, Wc[v0:v0 + Vs], yc, v0, Vs)
@@ -74,9 +82,14 @@ def test_slices_forward_backward(name, L, H, V, sizes, chunk, pair):
                                      allst[:, 2].contiguous(), y, V)
         dH = torch.zeros(L, H, dtype=torch.float32, device=h.device)
         dWs = []
-        for v0, Vs in _bounds(sizes):
-            dH_part, dW_s = B.backward_slice(h, W[v0:v0 + Vs], y, lse, dloss,
-                                             v0, V, chunk_rows=chunk)
+        for k, (v0, Vs) in enumerate(_bounds(sizes)):
+            if keep:
+                dH_part, dW_s = B.backward_slice_exp(h, W[v0:v0 + Vs], y, lse,
+                                                     dloss, v0, V, wss[k])
+            else:
+                dH_part, dW_s = B.backward_slice(h, W[v0:v0 + Vs], y, lse,
+                                                 dloss, v0, V,
+                                                 chunk_rows=chunk)
             dH += dH_part
             dWs.append(dW_s)
         dW = torch.cat(dWs)
@@ -93,8 +106,9 @@ def test_slices_forward_backward(name, L, H, V, sizes, chunk, pair):
         dH1, dW1 = lce.backward(h, W, y, lse1, dloss, chunk_rows=chunk)
     assert abs(loss.item() - loss1.item()) <= 1e-5 * abs(loss1.item())
     assert torch.max(torch.abs(lse - lse1)).item() <= 1e-4
-    # lse differs in the last bits, which flips a few bf16 roundings of G
-    assert rel_fro(to64(dW), to64(dW1)) <= 1e-3
+    # lse differs in the last bits, which flips a few bf16 roundings of G;
+    # kept exponentials are rounded to bf16 before the rescale
+    assert rel_fro(to64(dW), to64(dW1)) <= (4e-3 if keep else 1e-3)
     # dH1 is rounded to bf16 once; the fp32 sum of partials is not
     assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
 
@@ -133,4 +147,22 @@ def test_module_without_group_is_one_slice():
     assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
     assert torch.max(torch.abs(lse - lse1)).item() <= 1e-5
     assert rel_fro(to64(dW), to64(dW1)) <= 1e-3
+    assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
+
+
+def test_module_keep_exp_matches_recompute():
+    h, W, y = _inputs("mod", 384, 64, 2000)
+    d = torch.full((), 0.75, device=h.device)
+    ws = vp.exp_workspace(h, W[:1000])
+    loss, lse = vp.forward_exp(h, W[:1000], y, 0, 2000, ws)
+    dH, dW = vp.backward_exp(h, W[:1000], y, lse, d, 0, 2000, ws)
+    # the single process holds only the first half of the vocabulary here,
+    # so compare with the recomputing slice calls on the same half
+    m, s, zy = B.forward_slice(h, W[:1000], y, 0, 2000)
+    loss1, lse1 = B.combine_slices(m[None], s[None], zy[None], y, 2000)
+    dH1, dW1 = B.backward_slice(h, W[:1000], y, lse1, d, 0, 2000)
+    assert lce.get_error() == 0
+    assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
+    assert torch.max(torch.abs(lse - lse1)).item() <= 1e-5
+    assert rel_fro(to64(dW), to64(dW1)) <= 4e-3
     assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
