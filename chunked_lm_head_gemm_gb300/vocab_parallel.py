@@ -106,3 +106,52 @@ def backward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
     dH_part, dW = B.backward_slice_exp(h, W_slice, labels, lse, dloss, v0,
                                        V_total, workspace, ignore_index)
     return sum_partials(dH_part, group), dW
+
+
+class VocabParallelCrossEntropy(torch.autograd.Function):
+    """The loss of the whole vocabulary from this process's head slice, as
+    an autograd Function: forward returns the merged loss (the same on every
+    process of the group); backward returns dH summed over the group and
+    this slice's dW. keep_exp=True keeps the slice's exponentials between
+    forward and backward (no recompute, L x Vs x 2 bytes of workspace held
+    until backward); else only lse is kept and the backward recomputes."""
+
+    @staticmethod
+    def forward(ctx, h, W_slice, labels, v0, V_total, group=None,
+                ignore_index=B.IGNORE_INDEX, keep_exp=False):
+        ctx.v0, ctx.V_total, ctx.group = v0, V_total, group
+        ctx.ignore_index, ctx.keep_exp = ignore_index, keep_exp
+        ctx.w_dtype, ctx.h_dtype = W_slice.dtype, h.dtype
+        if keep_exp:
+            ws = exp_workspace(h, W_slice)
+            loss, lse = forward_exp(h, W_slice, labels, v0, V_total, ws,
+                                    group, ignore_index)
+            ctx.ws = ws
+        else:
+            loss, lse = forward(h, W_slice, labels, v0, V_total, group,
+                                ignore_index)
+            ctx.ws = None
+        ctx.save_for_backward(h, W_slice, labels, lse)
+        return loss
+
+    @staticmethod
+    def backward(ctx, dloss):
+        h, W_slice, labels, lse = ctx.saved_tensors
+        if ctx.keep_exp:
+            dH, dW = backward_exp(h, W_slice, labels, lse, dloss, ctx.v0,
+                                  ctx.V_total, ctx.ws, ctx.group,
+                                  ctx.ignore_index)
+            ctx.ws = None
+        else:
+            dH, dW = backward(h, W_slice, labels, lse, dloss, ctx.v0,
+                              ctx.V_total, ctx.group, ctx.ignore_index)
+        return (dH.to(ctx.h_dtype), dW.to(ctx.w_dtype), None, None, None,
+                None, None, None)
+
+
+def vocab_parallel_cross_entropy(h, W_slice, labels, v0: int, V_total: int,
+                                 group=None,
+                                 ignore_index: int = B.IGNORE_INDEX,
+                                 keep_exp: bool = False):
+    return VocabParallelCrossEntropy.apply(h, W_slice, labels, v0, V_total,
+                                           group, ignore_index, keep_exp)

@@ -166,3 +166,23 @@ def test_module_keep_exp_matches_recompute():
     assert torch.max(torch.abs(lse - lse1)).item() <= 1e-5
     assert rel_fro(to64(dW), to64(dW1)) <= 4e-3
     assert rel_fro(to64(dH), to64(dH1)) <= 4e-3
+
+
+@pytest.mark.parametrize("keep", [False, True], ids=["recompute", "keep_exp"])
+def test_autograd_function_one_slice(keep):
+    """With no group the one slice is the whole vocabulary: the autograd
+    Function's loss and gradients equal the whole-vocabulary calls'."""
+    h, W, y = _inputs("ag", 320, 64, 1500)
+    hl = h.clone().requires_grad_(True)
+    Wl = W.clone().requires_grad_(True)
+    loss = vp.vocab_parallel_cross_entropy(hl, Wl, y, 0, 1500,
+                                           keep_exp=keep)
+    (2.0 * loss).backward()
+    d = torch.full((), 2.0, device=h.device)
+    loss1, lse1 = lce.forward(h, W, y)
+    dH1, dW1 = lce.backward(h, W, y, lse1, d)
+    assert lce.get_error() == 0
+    assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
+    assert hl.grad.dtype == h.dtype and Wl.grad.dtype == W.dtype
+    assert rel_fro(to64(hl.grad), to64(dH1)) <= 8e-3
+    assert rel_fro(to64(Wl.grad), to64(dW1)) <= 8e-3
