@@ -702,7 +702,7 @@ def main():
         del h_host, W_host, dH_host, dW_host, bufs
 
     vocab_par = None
-    if args.vocab_shards > 1:
+    if args.vocab_shards >= 1:
         vocab_par = time_vocab_slice(lce, B, h, W, y, args.vocab_shards,
                                      chunk, args.steps, args.warmup)
 
