@@ -44,3 +44,36 @@ def test_reference_arm_silent_on_other_ranks():
     out = _run({"RANK": "1", "WORLD_SIZE": "2"}, "--config", "tiny",
                "--steps", "1", "--warmup", "0", "--gpus", "2")
     assert out.strip() == ""
+
+
+def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic is reported only for the kernel source
+    the committed capture was taken on (else null)."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    h = bench.source_hash()
+    (prof / "traffic.json").write_text(json.dumps({
+        "gemm_dW": {"qwen3-8b": {"dram_bytes_per_launch": 123.0,
+                                 "source_hash": h}},
+        "gemm_dH": {"qwen3-8b": {"dram_bytes_per_launch": 7.0,
+                                 "source_hash": "0" * 16}}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda: h)
+    assert bench.load_traffic("gemm_dW", "qwen3-8b") == 123.0
+    assert bench.load_traffic("gemm_dH", "qwen3-8b") is None
+    assert bench.load_traffic("gemm_dW", "qwen3-4b") is None
+
+
+def test_oracle_sample_is_bounded():
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunked_lm_head_gemm_gb300.inputs import WORKLOADS
+    wl = WORKLOADS["qwen3-8b"]
+    # rows so that the float64 work takes about `seconds` at `rate`
+    rows = bench.sample_rows_for(20.0, 4.0 * wl.H * wl.V * 3.0, wl)
+    assert rows == 60
+    assert bench.sample_rows_for(1e9, 1e12, wl) == wl.L
+    assert bench.sample_rows_for(1e-9, 1.0, wl) == 1
