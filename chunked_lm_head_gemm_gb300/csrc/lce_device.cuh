@@ -10,7 +10,11 @@
 //   warp 1      MMA issuer (one lane): tcgen05.mma 128x256x16 into one of two
 //               256-column TMEM accumulators (double buffered);
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter of the
-//               accumulator, then the fused loss arithmetic.
+//               accumulator, then the fused loss arithmetic; bf16 chunk
+//               outputs leave through shared-memory boxes and TMA stores.
+// A CTA-pair variant (k_gemm_pair, cta_group::2, 256 x 256 tiles, 6-stage
+// ring) shares the roles and epilogues. Producers may pace themselves in
+// waves of output tiles on a workspace counter (GemmGeom::wave_ctr).
 // Every mbarrier wait is bounded in time: on expiry the kernel raises a
 // timeout bit in the error word, the other roles see a shared abort flag,
 // in-flight copies and MMAs are drained (again bounded) and TMEM is freed.
@@ -522,7 +526,8 @@ struct EpiLse : EpiBase {
 };
 
 // Backward recompute: G = exp(z - lse) - [j == y] for rows that take part,
-// 0 for the others, rounded to bf16. The dloss/N scale is applied later, in
+// 0 for the others, rounded to bf16 and written by TMA stores of staged
+// 32 x 32 boxes (EpiBase::store_box). The dloss/N scale is applied later, in
 // fp32, by the dH and dW epilogues.
 struct EpiGrad : EpiBase {
   using Params = GradParams;
@@ -575,8 +580,8 @@ struct EpiGrad : EpiBase {
 
 // Fused forward+backward over one row chunk. Two passes over each tile's
 // TMEM columns: the first finds the tile's row maximum m_t (log2 units) and
-// gathers the label logit; the second writes e = 2^(u - m_t) in bf16 and
-// sums the fp32 values. (m_t, sum) then merge into the row's running
+// gathers the label logit; the second writes e = 2^(u - m_t) in bf16
+// (staged 32 x 32 boxes, TMA stores) and sums the fp32 values. (m_t, sum) then merge into the row's running
 // (max, sum) exactly as in EpiLse, and m_t is stored so that a later pass
 // can turn e into softmax - onehot once the row's lse is known.
 struct EpiFused : EpiBase {
