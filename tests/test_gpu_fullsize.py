@@ -55,6 +55,16 @@ def test_full_size(name):
     ref_loss = ((lse.double() - zy)[valid]).mean().item()
     assert abs(loss.item() - ref_loss) <= 1e-4 * abs(ref_loss)
 
+    # statistical sanity (loose, not parity): with W ~ N(0, w_std^2) drawn
+    # independently of h, a row's logits are ~ N(0, |h_i|^2 w_std^2), so
+    # lse_i ~ ln V + |h_i|^2 w_std^2 / 2 and z_y averages to 0. Not for the
+    # stress rows of the 32B shape, whose logit spread is far from small.
+    if not wl.stress_frac:
+        hn2 = (h.float().pow(2).sum(1).double())[valid]
+        expect = float(np.log(V)) + (hn2 * wl.w_std ** 2 / 2).mean().item()
+        assert abs(loss.item() - expect) <= 0.02 * expect, (loss.item(),
+                                                             expect)
+
     # columns of dW sum to ~0 (rows of softmax - onehot sum to zero)
     colsum = dW.double().sum(0)
     scale = dW.double().abs().sum(0)
