@@ -13,6 +13,11 @@ cross entropy against the labels) and "The massive logits matrix: chunk it"
 The reduction the pages leave open is: mean over rows whose label is neither
 ignore_index nor outside [0, V); 0 when no row is valid.
 
+Loss variants (not on the pages, which define only the plain cross entropy;
+both 0 by default): ``label_smoothing`` eps takes the cross entropy against
+the target (1 - eps) onehot + eps / V, and ``z_loss`` adds z_loss * lse^2
+to each valid row's loss.
+
 Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -59,14 +64,18 @@ def load_library(path: str):
     p, i64, i32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                         ctypes.c_double)
     lib.lce_oracle_forward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
-                                       i32, p, p, p, p]
+                                       f64, f64, i32, p, p, p, p]
     lib.lce_oracle_forward.restype = i32
     lib.lce_oracle_backward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
-                                        f64, i32, p, p, p, i64]
+                                        f64, f64, f64, i32, p, p, p, i64]
     lib.lce_oracle_backward.restype = i32
-    lib.lce_oracle_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64, f64, p,
-                                    i64, i32, p, p, p]
+    lib.lce_oracle_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64, f64,
+                                    f64, f64, p, i64, i32, p, p, p]
     lib.lce_oracle_rows.restype = i32
+    lib.lce_oracle_forward_backward.argtypes = [p, p, i32, p, i64, i64, i64,
+                                                i64, f64, f64, f64, i32, p, p,
+                                                p, p, p, p, p, i64]
+    lib.lce_oracle_forward_backward.restype = i32
     lib.lce_oracle_count_valid.argtypes = [p, i64, i64, i64, p]
     lib.lce_oracle_count_valid.restype = i64
     if hasattr(lib, "mlp_oracle"):
@@ -126,7 +135,8 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)))
 
 
-def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None):
+def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None,
+            label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Returns dict(loss, lse[L], zy[L], n_valid, status) in float64."""
     hn, dt = _as_input(h)
     Wn, dt2 = _as_input(W)
@@ -141,7 +151,9 @@ def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None)
     loss = np.zeros(1, np.float64)
     nv = np.zeros(1, np.int64)
     st = _load().lce_oracle_forward(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
-                                    ignore_index, nthreads or default_threads(),
+                                    ignore_index, float(label_smoothing),
+                                    float(z_loss),
+                                    nthreads or default_threads(),
                                     _ptr(lse), _ptr(zy), _ptr(loss), _ptr(nv))
     if st not in (OK, LABEL_RANGE):
         raise RuntimeError(f"lce_oracle_forward status {st}")
@@ -151,7 +163,8 @@ def forward(h, W, labels, ignore_index: int = -100, nthreads: int | None = None)
 
 def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
              want_dH: bool = True, want_dW: bool = True, vrows=None,
-             nthreads: int | None = None):
+             nthreads: int | None = None, label_smoothing: float = 0.0,
+             z_loss: float = 0.0):
     """Returns dict(dH[L,H] or None, dW or None, status) in float64.
 
     dW is [V,H], or [len(vrows), H] holding rows dW[vrows] when vrows is
@@ -168,7 +181,8 @@ def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
     nvr = V if vr is None else vr.shape[0]
     dW = np.empty((nvr, H), np.float64) if want_dW else None
     st = _load().lce_oracle_backward(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
-                                     ignore_index, float(dloss),
+                                     ignore_index, float(label_smoothing),
+                                     float(z_loss), float(dloss),
                                      nthreads or default_threads(), _ptr(dH),
                                      _ptr(dW), _ptr(vr),
                                      0 if vr is None else nvr)
@@ -178,7 +192,8 @@ def backward(h, W, labels, dloss: float = 1.0, ignore_index: int = -100,
 
 
 def rows(h, W, labels, rows, dloss: float = 1.0, ignore_index: int = -100,
-         want_dH: bool = True, nthreads: int | None = None):
+         want_dH: bool = True, nthreads: int | None = None,
+         label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Selected rows of a problem of any size (N counted over all labels).
 
     Returns dict(lse[n], zy[n], dH[n,H] or None, status) in float64."""
@@ -195,12 +210,47 @@ def rows(h, W, labels, rows, dloss: float = 1.0, ignore_index: int = -100,
     zy = np.empty(n, np.float64)
     dH = np.empty((n, H), np.float64) if want_dH else None
     st = _load().lce_oracle_rows(_ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V,
-                                 ignore_index, float(dloss), _ptr(r), n,
+                                 ignore_index, float(label_smoothing),
+                                 float(z_loss), float(dloss), _ptr(r), n,
                                  nthreads or default_threads(), _ptr(lse),
                                  _ptr(zy), _ptr(dH))
     if st not in (OK, LABEL_RANGE):
         raise RuntimeError(f"lce_oracle_rows status {st}")
     return dict(lse=lse, zy=zy, dH=dH, status=st)
+
+
+def forward_backward(h, W, labels, dloss: float = 1.0,
+                     ignore_index: int = -100, want_dH: bool = True,
+                     want_dW: bool = True, vrows=None,
+                     nthreads: int | None = None,
+                     label_smoothing: float = 0.0, z_loss: float = 0.0):
+    """forward() and backward() of the same problem from one pass over the
+    logits. Returns dict(loss, lse, zy, n_valid, dH, dW, status)."""
+    hn, dt = _as_input(h)
+    Wn, dt2 = _as_input(W)
+    if dt != dt2:
+        raise TypeError("h and W must have the same dtype")
+    y = _labels(labels)
+    L, H = hn.shape
+    V = Wn.shape[0]
+    assert Wn.shape[1] == H and y.shape == (L,)
+    vr = None if vrows is None else np.ascontiguousarray(vrows, dtype=np.int64)
+    lse = np.empty(L, np.float64)
+    zy = np.empty(L, np.float64)
+    loss = np.zeros(1, np.float64)
+    nv = np.zeros(1, np.int64)
+    dH = np.empty((L, H), np.float64) if want_dH else None
+    nvr = V if vr is None else vr.shape[0]
+    dW = np.empty((nvr, H), np.float64) if want_dW else None
+    st = _load().lce_oracle_forward_backward(
+        _ptr(hn), _ptr(Wn), dt, _ptr(y), L, H, V, ignore_index,
+        float(label_smoothing), float(z_loss), float(dloss),
+        nthreads or default_threads(), _ptr(lse), _ptr(zy), _ptr(loss),
+        _ptr(nv), _ptr(dH), _ptr(dW), _ptr(vr), 0 if vr is None else nvr)
+    if st not in (OK, LABEL_RANGE):
+        raise RuntimeError(f"lce_oracle_forward_backward status {st}")
+    return dict(loss=float(loss[0]), lse=lse, zy=zy, n_valid=int(nv[0]),
+                dH=dH, dW=dW, status=st)
 
 
 def count_valid(labels, V: int, ignore_index: int = -100):

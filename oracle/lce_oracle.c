@@ -34,6 +34,16 @@
  * The max shift m_i is the textbook way to evaluate log-sum-exp without
  * overflow; it does not change the value.
  *
+ * Two variants of the per-row loss, neither on the pages (they define only
+ * the plain cross entropy above), selected by eps and zcoef (both 0 gives
+ * the plain loss through the plain code):
+ *   - label smoothing eps: the cross entropy against the smoothed target
+ *     q_j = (1 - eps) [j == y_i] + eps / V instead of the one-hot,
+ *       loss_i = sum_j q_j (lse[i] - z[i][j]);
+ *   - z-loss zcoef: loss_i += zcoef * lse[i]^2.
+ *   Then loss = (1/N) sum_{valid i} loss_i as before, and
+ *   G[i][j] = dloss/N * ( (1 + 2 zcoef lse[i]) exp(z[i][j] - lse[i]) - q_j ).
+ *
  * Inputs are widened to float64 exactly: dtype 0 = bfloat16 (raw 16-bit
  * patterns), 1 = float32, 2 = float64. All arithmetic is float64; the
  * exponential and logarithm are the C library's exp() and log().
@@ -150,8 +160,22 @@ typedef struct {
     double *lse, *zy;
     double *G;    /* nrows x V, only for the backward */
     double gscale; /* dloss / N, 0 when N == 0 */
+    double eps, zcoef; /* loss variant (both 0: plain cross entropy) */
+    double *term;  /* per-row loss of a variant (0 for ignored rows) */
     int status;
 } row_job;
+
+/* One row's loss under the variants: the cross entropy against the smoothed
+ * target q_j = (1 - eps) [j == y] + eps / V, plus zcoef * lse^2. */
+static double row_term(const double *z, int64_t V, int64_t y, double lse,
+                       double eps, double zcoef) {
+    double t = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        double q = (j == y ? 1.0 - eps : 0.0) + eps / (double)V;
+        t += q * (lse - z[j]);
+    }
+    return t + zcoef * lse * lse;
+}
 
 static void *row_worker(void *arg) {
     row_job *jb = (row_job *)arg;
@@ -172,14 +196,25 @@ static void *row_worker(void *arg) {
         int valid = label_is_valid(y, jb->V, jb->ignore_index);
         if (jb->lse) jb->lse[r] = lse;
         if (jb->zy) jb->zy[r] = valid ? z[y] : NAN;
+        if (jb->term)
+            jb->term[r] = valid ? row_term(z, jb->V, y, lse, jb->eps,
+                                           jb->zcoef)
+                                : 0.0;
         if (jb->G) {
             double *g = jb->G + r * jb->V;
             if (!valid || jb->gscale == 0.0) {
                 for (int64_t j = 0; j < jb->V; ++j) g[j] = 0.0;
-            } else {
+            } else if (jb->eps == 0.0 && jb->zcoef == 0.0) {
                 for (int64_t j = 0; j < jb->V; ++j)
                     g[j] = jb->gscale * exp(z[j] - lse);
                 g[y] -= jb->gscale;
+            } else {
+                /* d loss_i / d z_j = (1 + 2 zcoef lse) p_j - q_j */
+                const double zf = 1.0 + 2.0 * jb->zcoef * lse;
+                const double qu = jb->eps / (double)jb->V;
+                for (int64_t j = 0; j < jb->V; ++j)
+                    g[j] = jb->gscale * (zf * exp(z[j] - lse) - qu);
+                g[y] -= jb->gscale * (1.0 - jb->eps);
             }
         }
     }
@@ -231,25 +266,40 @@ static int check_args(const void *h, const void *W, int dtype,
     return ORACLE_OK;
 }
 
+static int check_variant(double eps, double zcoef) {
+    if (!(eps >= 0.0 && eps <= 1.0) || !(zcoef >= 0.0 && zcoef < INFINITY))
+        return ORACLE_BAD_ARG;
+    return ORACLE_OK;
+}
+
+static int is_plain(double eps, double zcoef) {
+    return eps == 0.0 && zcoef == 0.0;
+}
+
 /* ---- public entry points ------------------------------------------------ */
 
 /*
  * Forward: lse[L], zy[L] (logit at the label, NaN for ignored rows),
- * loss = sum_valid(lse - zy) / N (0 when N == 0), n_valid = N.
+ * loss = sum_valid(lse - zy) / N (0 when N == 0), n_valid = N; with a loss
+ * variant (eps or zcoef not 0) the summed per-row loss is row_term's.
  * Returns ORACLE_LABEL_RANGE (results still written, those rows ignored)
  * when some label is neither ignore_index nor in [0, V).
  */
 int lce_oracle_forward(const void *h, const void *W, int dtype,
                        const int64_t *labels, int64_t L, int64_t H, int64_t V,
-                       int64_t ignore_index, int nthreads, double *lse,
-                       double *zy, double *loss, int64_t *n_valid) {
+                       int64_t ignore_index, double eps, double zcoef,
+                       int nthreads, double *lse, double *zy, double *loss,
+                       int64_t *n_valid) {
     int st = check_args(h, W, dtype, labels, L, H, V);
     if (st) return st;
+    if ((st = check_variant(eps, zcoef))) return st;
     int bad = 0;
     int64_t n = count_valid(labels, L, V, ignore_index, &bad);
+    const int plain = is_plain(eps, zcoef);
     double *lse_buf = lse ? lse : (double *)malloc((size_t)L * sizeof(double));
     double *zy_buf = zy ? zy : (double *)malloc((size_t)L * sizeof(double));
-    if (!lse_buf || !zy_buf) {
+    double *term = plain ? NULL : (double *)malloc((size_t)L * sizeof(double));
+    if (!lse_buf || !zy_buf || (!plain && !term)) {
         st = ORACLE_NO_MEMORY;
         goto out;
     }
@@ -264,13 +314,16 @@ int lce_oracle_forward(const void *h, const void *W, int dtype,
     proto.ignore_index = ignore_index;
     proto.lse = lse_buf;
     proto.zy = zy_buf;
+    proto.eps = eps;
+    proto.zcoef = zcoef;
+    proto.term = term;
     st = run_rows(proto, L, nthreads);
     if (st) goto out;
     {
         double total = 0.0;
         for (int64_t i = 0; i < L; ++i)
             if (label_is_valid(labels[i], V, ignore_index))
-                total += lse_buf[i] - zy_buf[i];
+                total += plain ? lse_buf[i] - zy_buf[i] : term[i];
         if (loss) *loss = n > 0 ? total / (double)n : 0.0;
         if (n_valid) *n_valid = n;
     }
@@ -278,6 +331,7 @@ int lce_oracle_forward(const void *h, const void *W, int dtype,
 out:
     if (!lse) free(lse_buf);
     if (!zy) free(zy_buf);
+    free(term);
     return st;
 }
 
@@ -368,11 +422,12 @@ static void run_mm(mm_job proto, int64_t n, int nthreads, void *(*fn)(void *)) {
  */
 int lce_oracle_backward(const void *h, const void *W, int dtype,
                         const int64_t *labels, int64_t L, int64_t H, int64_t V,
-                        int64_t ignore_index, double dloss, int nthreads,
-                        double *dH, double *dW, const int64_t *vrows,
-                        int64_t nvrows) {
+                        int64_t ignore_index, double eps, double zcoef,
+                        double dloss, int nthreads, double *dH, double *dW,
+                        const int64_t *vrows, int64_t nvrows) {
     int st = check_args(h, W, dtype, labels, L, H, V);
     if (st) return st;
+    if ((st = check_variant(eps, zcoef))) return st;
     if (vrows) {
         if (nvrows < 1) return ORACLE_BAD_ARG;
         for (int64_t a = 0; a < nvrows; ++a)
@@ -397,6 +452,8 @@ int lce_oracle_backward(const void *h, const void *W, int dtype,
         proto.V = V;
         proto.ignore_index = ignore_index;
         proto.G = G;
+        proto.eps = eps;
+        proto.zcoef = zcoef;
         proto.gscale = n > 0 ? dloss / (double)n : 0.0;
         st = run_rows(proto, L, nthreads);
         if (st) goto out;
@@ -421,11 +478,12 @@ out:
  */
 int lce_oracle_rows(const void *h, const void *W, int dtype,
                     const int64_t *labels, int64_t L, int64_t H, int64_t V,
-                    int64_t ignore_index, double dloss, const int64_t *rows,
-                    int64_t nrows, int nthreads, double *lse, double *zy,
-                    double *dH_rows) {
+                    int64_t ignore_index, double eps, double zcoef,
+                    double dloss, const int64_t *rows, int64_t nrows,
+                    int nthreads, double *lse, double *zy, double *dH_rows) {
     int st = check_args(h, W, dtype, labels, L, H, V);
     if (st) return st;
+    if ((st = check_variant(eps, zcoef))) return st;
     if (!rows || nrows < 1) return ORACLE_BAD_ARG;
     for (int64_t r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= L) return ORACLE_BAD_ARG;
@@ -451,6 +509,8 @@ int lce_oracle_rows(const void *h, const void *W, int dtype,
         proto.lse = lse;
         proto.zy = zy;
         proto.G = G;
+        proto.eps = eps;
+        proto.zcoef = zcoef;
         proto.gscale = n > 0 ? dloss / (double)n : 0.0;
         st = run_rows(proto, nrows, nthreads);
         if (st) goto out;
@@ -461,6 +521,82 @@ int lce_oracle_rows(const void *h, const void *W, int dtype,
     }
     st = bad ? ORACLE_LABEL_RANGE : ORACLE_OK;
 out:
+    free(G);
+    return st;
+}
+
+/*
+ * Forward and backward of the whole problem from one pass over the logits:
+ * what lce_oracle_forward and lce_oracle_backward return for the same
+ * arguments (any output may be NULL), with each row's logits computed once
+ * instead of twice. Holds G (L x V float64) like lce_oracle_backward.
+ */
+int lce_oracle_forward_backward(const void *h, const void *W, int dtype,
+                                const int64_t *labels, int64_t L, int64_t H,
+                                int64_t V, int64_t ignore_index, double eps,
+                                double zcoef, double dloss, int nthreads,
+                                double *lse, double *zy, double *loss,
+                                int64_t *n_valid, double *dH, double *dW,
+                                const int64_t *vrows, int64_t nvrows) {
+    int st = check_args(h, W, dtype, labels, L, H, V);
+    if (st) return st;
+    if ((st = check_variant(eps, zcoef))) return st;
+    if (vrows) {
+        if (nvrows < 1) return ORACLE_BAD_ARG;
+        for (int64_t a = 0; a < nvrows; ++a)
+            if (vrows[a] < 0 || vrows[a] >= V) return ORACLE_BAD_ARG;
+    }
+    int bad = 0;
+    int64_t n = count_valid(labels, L, V, ignore_index, &bad);
+    const int plain = is_plain(eps, zcoef);
+    double *lse_buf = lse ? lse : (double *)malloc((size_t)L * sizeof(double));
+    double *zy_buf = zy ? zy : (double *)malloc((size_t)L * sizeof(double));
+    double *term = plain ? NULL : (double *)malloc((size_t)L * sizeof(double));
+    double *hd = widen_all(h, dtype, L, H);
+    double *G = (double *)malloc((size_t)(L * V) * sizeof(double));
+    if (!lse_buf || !zy_buf || (!plain && !term) || !hd || !G) {
+        st = ORACLE_NO_MEMORY;
+        goto out;
+    }
+    {
+        row_job proto = {0};
+        proto.h = h;
+        proto.dtype = dtype;
+        proto.W = W;
+        proto.labels = labels;
+        proto.L = L;
+        proto.H = H;
+        proto.V = V;
+        proto.ignore_index = ignore_index;
+        proto.lse = lse_buf;
+        proto.zy = zy_buf;
+        proto.term = term;
+        proto.G = G;
+        proto.eps = eps;
+        proto.zcoef = zcoef;
+        proto.gscale = n > 0 ? dloss / (double)n : 0.0;
+        st = run_rows(proto, L, nthreads);
+        if (st) goto out;
+    }
+    {
+        double total = 0.0;
+        for (int64_t i = 0; i < L; ++i)
+            if (label_is_valid(labels[i], V, ignore_index))
+                total += plain ? lse_buf[i] - zy_buf[i] : term[i];
+        if (loss) *loss = n > 0 ? total / (double)n : 0.0;
+        if (n_valid) *n_valid = n;
+    }
+    {
+        mm_job mp = {G, W, dtype, hd, L, H, V, 0, 0, dH, dW, vrows};
+        if (dH) run_mm(mp, L, nthreads, dH_worker);
+        if (dW) run_mm(mp, vrows ? nvrows : V, nthreads, dW_worker);
+    }
+    st = bad ? ORACLE_LABEL_RANGE : ORACLE_OK;
+out:
+    if (!lse) free(lse_buf);
+    if (!zy) free(zy_buf);
+    free(term);
+    free(hd);
     free(G);
     return st;
 }

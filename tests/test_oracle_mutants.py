@@ -50,6 +50,16 @@ MUTANTS = {
                             "proto.gscale = n > 0 ? dloss / (double)L : 0.0;\n        st = run_rows(proto, L, nthreads);"),
     "ignored_rows_count": ("if (label_is_valid(labels[i], V, ignore_index))\n            ++n;",
                            "if (labels[i] != ignore_index || 1)\n            ++n;"),
+    # the loss variants (label smoothing, z-loss)
+    "smooth_loss_over_V_minus_1": ("double q = (j == y ? 1.0 - eps : 0.0) + eps / (double)V;",
+                                   "double q = (j == y ? 1.0 - eps : 0.0) + eps / (double)(V - 1);"),
+    "smooth_grad_over_V_minus_1": ("const double qu = jb->eps / (double)jb->V;",
+                                   "const double qu = jb->eps / (double)(jb->V - 1);"),
+    "smooth_onehot_not_scaled": ("g[y] -= jb->gscale * (1.0 - jb->eps);",
+                                 "g[y] -= jb->gscale;"),
+    "z_loss_missing_in_loss": ("return t + zcoef * lse * lse;", "return t;"),
+    "z_loss_grad_factor": ("const double zf = 1.0 + 2.0 * jb->zcoef * lse;",
+                           "const double zf = 1.0 + jb->zcoef * lse;"),
 }
 
 PIN_CHECKS = [
@@ -62,6 +72,10 @@ PIN_CHECKS = [
     lambda o: pins.test_v2_is_logistic_loss(o),
     lambda o: pins.test_invariants(o),
     lambda o: pins.test_all_ignored_and_bad_labels(o),
+    lambda o: pins.test_variants_against_torch_f64(o, 37, 19, 53, 2, 0.2,
+                                                   0.05),
+    lambda o: pins.test_variant_finite_differences(o),
+    lambda o: pins.test_variant_w_zero_closed_form(o, 0.3, 1e-3),
 ]
 
 

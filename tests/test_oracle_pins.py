@@ -274,3 +274,170 @@ def test_dW_vocab_subset_matches_whole(oracle_mod):
     sub = oracle_mod.backward(h, W, y, dloss=1.1, want_dH=False,
                               vrows=v)["dW"]
     np.testing.assert_array_equal(sub, full[v])
+
+
+# ---- single pass and loss variants ------------------------------------------
+
+VARIANTS = [(0.1, 0.0), (0.3, 0.0), (1.0, 0.0), (0.0, 1e-2), (0.2, 0.05)]
+
+
+def _torch_variant_ref(h, W, y, eps, zcoef, dloss=1.0):
+    """PyTorch float64: F.cross_entropy with label_smoothing (a library
+    routine) plus zcoef * lse^2 averaged over the rows that take part, and
+    autograd for the gradients."""
+    ht = torch.tensor(np.asarray(h, dtype=np.float64), requires_grad=True)
+    Wt = torch.tensor(np.asarray(W, dtype=np.float64), requires_grad=True)
+    yt = torch.tensor(y)
+    z = ht @ Wt.T
+    loss = torch.nn.functional.cross_entropy(z, yt, ignore_index=-100,
+                                             reduction="mean",
+                                             label_smoothing=eps)
+    valid = yt != -100
+    lse = torch.logsumexp(z, dim=1)
+    if zcoef:
+        loss = loss + zcoef * (lse[valid] ** 2).sum() / valid.sum()
+    (loss * dloss).backward()
+    return loss.item(), lse.detach().numpy(), ht.grad.numpy(), Wt.grad.numpy()
+
+
+@pytest.mark.parametrize("eps,zcoef", VARIANTS)
+@pytest.mark.parametrize("L,H,V,seed", [(3, 2, 5, 1), (37, 19, 53, 2)])
+def test_variants_against_torch_f64(oracle_mod, L, H, V, seed, eps, zcoef):
+    h, W, y = _rand_problem(L, H, V, seed)
+    if (y != -100).sum() == 0:
+        y[0] = 0
+    dloss = 0.7
+    loss, lse, dH, dW = _torch_variant_ref(h, W, y, eps, zcoef, dloss)
+    kw = dict(label_smoothing=eps, z_loss=zcoef)
+    f = oracle_mod.forward(h, W, y, **kw)
+    b = oracle_mod.backward(h, W, y, dloss=dloss, **kw)
+    assert f["loss"] == pytest.approx(loss, rel=1e-12, abs=1e-14)
+    np.testing.assert_allclose(f["lse"], lse, rtol=1e-12)
+    np.testing.assert_allclose(b["dH"], dH, rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(b["dW"], dW, rtol=1e-10, atol=1e-14)
+    r = np.array([0, L - 1])
+    s = oracle_mod.rows(h, W, y, r, dloss=dloss, **kw)
+    np.testing.assert_allclose(s["dH"], dH[r], rtol=1e-10, atol=1e-14)
+
+
+def test_variant_finite_differences(oracle_mod):
+    L, H, V = 8, 4, 16
+    h, W, y = _rand_problem(L, H, V, 19)
+    kw = dict(label_smoothing=0.2, z_loss=0.03)
+    b = oracle_mod.backward(h, W, y, dloss=1.0, **kw)
+    eps = 1e-6
+    rs = np.random.default_rng(6)
+
+    def loss_of(hh, WW):
+        return oracle_mod.forward(hh, WW, y, **kw)["loss"]
+
+    for _ in range(12):
+        i, k = rs.integers(0, L), rs.integers(0, H)
+        hp, hm = h.copy(), h.copy()
+        hp[i, k] += eps
+        hm[i, k] -= eps
+        fd = (loss_of(hp, W) - loss_of(hm, W)) / (2 * eps)
+        assert fd == pytest.approx(b["dH"][i, k], rel=1e-6, abs=1e-9)
+        j, k = rs.integers(0, V), rs.integers(0, H)
+        Wp, Wm = W.copy(), W.copy()
+        Wp[j, k] += eps
+        Wm[j, k] -= eps
+        fd = (loss_of(h, Wp) - loss_of(h, Wm)) / (2 * eps)
+        assert fd == pytest.approx(b["dW"][j, k], rel=1e-6, abs=1e-9)
+
+
+@pytest.mark.parametrize("eps,zcoef", [(0.1, 0.0), (1.0, 0.0), (0.3, 1e-3)])
+def test_variant_w_zero_closed_form(oracle_mod, eps, zcoef):
+    """W = 0: every logit is 0, lse = ln V and the smoothed cross entropy of
+    every row is ln V whatever eps (the target sums to one), so loss =
+    ln V + zcoef (ln V)^2; dH = 0; dW[v] = dloss/N sum_valid ((1 + 2 zcoef
+    ln V)/V - q_v) h_i with q_v = (1 - eps)[v == y_i] + eps/V."""
+    V = 4096
+    g = json.load(open(os.path.join(GOLD, "w_zero.json")))
+    lnV = g["ln_V"][str(V)]
+    L, H = 6, 8
+    rs = np.random.default_rng(8)
+    h = rs.standard_normal((L, H))
+    W = np.zeros((V, H))
+    y = rs.integers(0, V, L).astype(np.int64)
+    y[4] = -100
+    dloss = 0.9
+    kw = dict(label_smoothing=eps, z_loss=zcoef)
+    f = oracle_mod.forward(h, W, y, **kw)
+    assert f["loss"] == pytest.approx(lnV + zcoef * lnV ** 2, rel=1e-13)
+    b = oracle_mod.backward(h, W, y, dloss=dloss, **kw)
+    assert np.all(b["dH"] == 0.0)
+    valid = y != -100
+    n = valid.sum()
+    p = (1.0 + 2.0 * zcoef * lnV) / V
+    expect = np.tile((dloss / n) * (p - eps / V) * h[valid].sum(0), (V, 1))
+    for i in np.nonzero(valid)[0]:
+        expect[y[i]] -= (dloss / n) * (1.0 - eps) * h[i]
+    np.testing.assert_allclose(b["dW"], expect, rtol=1e-11, atol=1e-15)
+
+
+def test_full_smoothing_does_not_depend_on_labels(oracle_mod):
+    """eps = 1: the target is uniform, so which valid label a row has does
+    not matter (only whether it is ignored)."""
+    L, H, V = 30, 6, 25
+    h, W, y = _rand_problem(L, H, V, 43)
+    y2 = y.copy()
+    valid = y != -100
+    y2[valid] = (y[valid] + 7) % V
+    kw = dict(label_smoothing=1.0)
+    f = oracle_mod.forward(h, W, y, **kw)
+    f2 = oracle_mod.forward(h, W, y2, **kw)
+    assert f2["loss"] == pytest.approx(f["loss"], rel=1e-13)
+    b = oracle_mod.backward(h, W, y, **kw)
+    b2 = oracle_mod.backward(h, W, y2, **kw)
+    np.testing.assert_allclose(b2["dW"], b["dW"], rtol=1e-12, atol=1e-16)
+
+
+def test_smoothing_is_shift_invariant_and_z_loss_is_not(oracle_mod):
+    """The smoothed target sums to one, so W -> W + 1 u^T changes neither
+    the smoothed loss nor its gradients; the z-loss term moves with lse,
+    which moves by h.u exactly."""
+    L, H, V = 40, 12, 70
+    h, W, y = _rand_problem(L, H, V, 47)
+    u = np.random.default_rng(9).standard_normal(H)
+    W2 = W + u[None, :]
+    kw = dict(label_smoothing=0.3)
+    f, f2 = (oracle_mod.forward(h, w, y, **kw) for w in (W, W2))
+    assert f2["loss"] == pytest.approx(f["loss"], rel=1e-12)
+    b, b2 = (oracle_mod.backward(h, w, y, **kw) for w in (W, W2))
+    np.testing.assert_allclose(b2["dH"], b["dH"], rtol=1e-9, atol=1e-14)
+    np.testing.assert_allclose(b2["dW"], b["dW"], rtol=1e-9, atol=1e-14)
+    zc = 0.02
+    g, g2 = (oracle_mod.forward(h, w, y, label_smoothing=0.3, z_loss=zc)
+             for w in (W, W2))
+    valid = y != -100
+    s = (h @ u)[valid]
+    lse = f["lse"][valid]
+    moved = zc * np.mean((lse + s) ** 2 - lse ** 2)
+    assert g2["loss"] - g["loss"] == pytest.approx(moved, rel=1e-9)
+
+
+@pytest.mark.parametrize("eps,zcoef", [(0.0, 0.0), (0.2, 0.05)])
+def test_single_pass_matches_forward_and_backward(oracle_mod, eps, zcoef):
+    L, H, V = 33, 10, 47
+    h, W, y = _rand_problem(L, H, V, 53)
+    kw = dict(label_smoothing=eps, z_loss=zcoef)
+    f = oracle_mod.forward(h, W, y, **kw)
+    b = oracle_mod.backward(h, W, y, dloss=1.3, **kw)
+    v = np.array([46, 0, 3])
+    fb = oracle_mod.forward_backward(h, W, y, dloss=1.3, **kw)
+    fbv = oracle_mod.forward_backward(h, W, y, dloss=1.3, vrows=v,
+                                      want_dH=False, **kw)
+    assert fb["loss"] == f["loss"] and fb["n_valid"] == f["n_valid"]
+    assert np.array_equal(fb["lse"], f["lse"])
+    assert np.array_equal(fb["dH"], b["dH"]) and np.array_equal(fb["dW"],
+                                                               b["dW"])
+    assert fbv["dH"] is None and np.array_equal(fbv["dW"], b["dW"][v])
+
+
+def test_variant_arguments_are_checked(oracle_mod):
+    h, W, y = _rand_problem(4, 3, 5, 59)
+    for kw in (dict(label_smoothing=-0.1), dict(label_smoothing=1.5),
+               dict(z_loss=-1.0), dict(z_loss=float("inf"))):
+        with pytest.raises(RuntimeError):
+            oracle_mod.forward(h, W, y, **kw)
