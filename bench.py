@@ -421,6 +421,9 @@ def main():
     ap.add_argument("--config", default="qwen3-8b")
     ap.add_argument("--rows", type=int, default=0,
                     help="override L (a row slice of the workload)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="override V (a reduced vocabulary, for profiling "
+                         "one contraction on a small device footprint)")
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--mode", default="fused", choices=["separate", "fused"])
     ap.add_argument("--only-mode", action="store_true",
@@ -446,6 +449,10 @@ def main():
     wl = WORKLOADS[args.config]
     if args.rows:
         wl = wl.with_rows(args.rows)
+    if args.vocab:
+        import dataclasses
+        wl = dataclasses.replace(wl, V=args.vocab,
+                                 name=f"{wl.name}[V={args.vocab}]")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 

@@ -576,7 +576,12 @@ class LinearCrossEntropy(torch.autograd.Function):
     fused=False: forward saves only lse [L] (4 bytes per row); backward
     recomputes the logits chunk by chunk in the library.
     fused=True: forward computes the loss and the gradients in one call
-    (no recompute) and keeps dH, dW until backward scales them by dloss."""
+    (no recompute) and keeps dH, dW (for dloss = 1) until backward, which
+    returns copies scaled by dloss. The kept tensors are never modified, so
+    a retained graph gives the same gradients again; the cost is memory:
+    dH and dW (L H + 4 V H bytes for bf16 h) stay allocated from the forward
+    until the graph is freed, and backward briefly holds the scaled copies
+    as well."""
 
     @staticmethod
     def forward(ctx, h, W, labels, ignore_index=IGNORE_INDEX, chunk_rows=0,
@@ -597,8 +602,8 @@ class LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dloss):
         if ctx.fused:
-            dH, dW = ctx.saved_tensors
-            scale_gradients(dH, dW, dloss)
+            kept_dH, kept_dW = ctx.saved_tensors
+            dH, dW = scale_gradients(kept_dH.clone(), kept_dW.clone(), dloss)
         else:
             h, W, labels, lse = ctx.saved_tensors
             dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,

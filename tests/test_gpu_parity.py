@@ -21,6 +21,19 @@ def _oracle(h, W, y, dloss=1.0, vrows=None):
     return f, b
 
 
+# oracle results of the row slices, shared by the parametrisations of one
+# slice (both paths, both contraction variants run on the same inputs)
+_SLICE_CACHE = {}
+
+
+def _slice_oracle(key, h, W, y, vrows):
+    if key not in _SLICE_CACHE:
+        fb = oracle.forward_backward(h.cpu(), W.cpu(), y.cpu(), dloss=1.0,
+                                     vrows=vrows)
+        _SLICE_CACHE[key] = (fb, fb)
+    return _SLICE_CACHE[key]
+
+
 @pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
 @pytest.mark.parametrize("mode", MODES)
 def test_tiny_workload(mode, pair):
@@ -138,6 +151,32 @@ def test_autograd_function_matches_explicit_calls(mode):
     assert rel_fro(WW.grad.double().cpu().numpy(), gpu["dW"]) < 4e-3
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_autograd_backward_twice(mode):
+    """A retained graph can be differentiated again with the same result:
+    the fused mode scales copies of the gradients it keeps, never the kept
+    tensors themselves, so a second backward (or a non-unit upstream
+    gradient) does not scale them twice."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = Workload("ag2", 260, 64, 700, "bf16", 1.0, 0.1, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=8, device=dev)
+    hh = h.clone().requires_grad_(True)
+    WW = W.clone().requires_grad_(True)
+    loss = lce.linear_cross_entropy(hh, WW, y, fused=(mode == "fused"))
+    (2.5 * loss).backward(retain_graph=True)
+    gh, gw = hh.grad.clone(), WW.grad.clone()
+    hh.grad = None
+    WW.grad = None
+    (2.5 * loss).backward(retain_graph=True)
+    assert torch.equal(hh.grad, gh) and torch.equal(WW.grad, gw)
+    (2.5 * loss).backward()  # accumulates onto the second pass's gradients
+    assert torch.equal(hh.grad, 2 * gh) and torch.equal(WW.grad, 2 * gw)
+    gpu = run_gpu(h, W, y, dloss=2.5, mode=mode)
+    assert torch.equal(gh.float().cpu(), torch.from_numpy(gpu["dH"]).float())
+
+
 SLICES = [("qwen3-0.6b", 256), ("qwen3-4b", 300), ("qwen3-8b", 256),
           ("qwen3-32b", 256)]
 
@@ -154,9 +193,39 @@ def test_row_slice_of_head_shape(name, rows, mode, pair):
     h, W, y = make_inputs(wl, seed=0, device=dev)
     gpu = run_gpu(h, W, y, dloss=1.0, mode=mode, pair=pair)
     assert gpu["status"] == 0
+    vrows = _touched_vocab_rows(y, wl.V)
+    f, b = _slice_oracle((name, rows), h, W, y, vrows)
+    assert_parity(gpu, f, b, dW_rows=vrows)
+
+
+def _touched_vocab_rows(y, V):
+    """The vocabulary rows the labels touch, 256 seeded others, 0 and V-1."""
     yc = y.cpu().numpy()
     rs = np.random.default_rng(7)
-    vrows = np.unique(np.concatenate([yc[yc >= 0], rs.integers(0, wl.V, 256),
-                                      [0, wl.V - 1]]))
-    f, b = _oracle(h, W, y, vrows=vrows)
+    return np.unique(np.concatenate([yc[yc >= 0], rs.integers(0, V, 256),
+                                     [0, V - 1]]))
+
+
+MULTI = [("qwen3-8b", 1024), ("qwen3-32b", 1024)]
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name,rows", MULTI, ids=[s[0] for s in MULTI])
+def test_multichunk_row_slice_of_head_shape(name, rows, mode, pair):
+    """1024 rows of the 8B and 32B head shapes (full H and V = 151936; the
+    32B slice holds stress rows scaled x20) with a 256-row backward chunk:
+    four chunks, so dW's fp32 read-add-write runs three times at full H and
+    V, and the fused path writes its tile exponentials four times. Loss,
+    every lse, every dH row, and dW on the touched vocabulary rows plus 256
+    seeded others and V-1, against the float64 oracle. The loss is a sum
+    over rows ("Training Beyond 1M Tokens", section "The massive logits
+    matrix: chunk it"), so any chunking must give the oracle's answer."""
+    dev = require_gpu()
+    wl = WORKLOADS[name].with_rows(rows)
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    gpu = run_gpu(h, W, y, dloss=1.0, chunk_rows=256, mode=mode, pair=pair)
+    assert gpu["status"] == 0
+    vrows = _touched_vocab_rows(y, wl.V)
+    f, b = _slice_oracle((name, rows), h, W, y, vrows)
     assert_parity(gpu, f, b, dW_rows=vrows)
