@@ -438,11 +438,24 @@ def main():
                     help="also time one process's share of a P-way "
                          "vocabulary-parallel step (its V/P slice; the "
                          "collectives are not timed)")
+    ap.add_argument("--layout-sweep", default="", metavar="M,N,K",
+                    help="time the library's contraction D = A B on M,N,K in "
+                         "its four operand layouts (A, B K-major or "
+                         "MN-major) and print one JSON line instead of the "
+                         "benchmark")
+    ap.add_argument("--forward-static", action="store_true",
+                    help="time lce_forward_static against lce_forward on "
+                         "the workload (forward only) and print one JSON "
+                         "line instead of the benchmark")
     ap.add_argument("--comparator", type=int, default=0, metavar="ROWS",
                     help="also time the pages' chunked scheme in eager "
                          "PyTorch with ROWS-row chunks (context only)")
     args = ap.parse_args()
 
+    if args.layout_sweep:
+        return layout_sweep(args)
+    if args.forward_static:
+        return forward_static(args)
     if args.workload == "mlp":
         return bench_mlp(args)
     from chunked_lm_head_gemm_gb300.inputs import WORKLOADS
@@ -793,6 +806,120 @@ def main():
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def forward_static(args):
+    """lce_forward_static (fixed scratch inside the library, single-CTA
+    contraction, no wave pacing) against lce_forward (caller workspace,
+    the default contraction variant, paced) on the same inputs, interleaved:
+    median ms per call from CUDA events; one JSON line."""
+    import ctypes
+    import torch
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300.inputs import WORKLOADS, make_inputs
+    wl = WORKLOADS[args.config]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = lce.load()
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    L, H, V = wl.L, wl.H, wl.V
+    ws = lce.alloc_workspace(L, H, V, h.dtype, 0, dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(L, dtype=torch.float32, device=dev)
+
+    def static():
+        st = lib.lce_forward_static(
+            ctypes.c_void_p(h.data_ptr()), ctypes.c_void_p(W.data_ptr()),
+            ctypes.c_void_p(y.data_ptr()), L, H, V, -100,
+            ctypes.c_void_p(loss.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if st != 0:
+            raise RuntimeError(lib.lce_last_cuda_error().decode())
+
+    def workspace():
+        lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
+
+    calls = {"lce_forward_static": static, "lce_forward": workspace}
+    for _ in range(args.warmup):
+        for f in calls.values():
+            f()
+    torch.cuda.synchronize()
+    ms = {k: [] for k in calls}
+    for _ in range(args.steps):
+        for k, f in calls.items():
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            ms[k].append(e0.elapsed_time(e1))
+    if lce.get_error() != 0:
+        raise RuntimeError("device error status in the static-forward timing")
+    flops = 2.0 * L * H * V
+    out = {k: {"ms_median": statistics.median(v),
+               "tflops": flops / statistics.median(v) / 1e9}
+           for k, v in ms.items()}
+    print(json.dumps({"forward_static": out, "workload": wl.name,
+                      "steps": args.steps}), flush=True)
+
+
+def layout_sweep(args):
+    """The contraction D[M,N] = A[M,K] B[K,N] (bf16, fp32 out) through the
+    library's test hook in its four operand layouts, interleaved, on the
+    contraction variant in use: TFLOP/s per layout from CUDA events over
+    --steps launches each, after --warmup; one JSON line."""
+    import torch
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    M, N, K = (int(x) for x in args.layout_sweep.split(","))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lce.load()
+    if args.cta_pair >= 0:
+        B.set_cta_pair(bool(args.cta_pair))
+    g = torch.Generator(device=dev).manual_seed(0)
+    ops = {}
+    for a_mn in (False, True):
+        for b_mn in (False, True):
+            A = torch.randn(*((K, M) if a_mn else (M, K)), generator=g,
+                            device=dev).to(torch.bfloat16)
+            Bm = torch.randn(*((K, N) if b_mn else (N, K)), generator=g,
+                             device=dev).to(torch.bfloat16)
+            ops[(a_mn, b_mn)] = (A, Bm)
+    ms = {k: [] for k in ops}
+    for _ in range(args.warmup):
+        for (a_mn, b_mn), (A, Bm) in ops.items():
+            B.tc_gemm(A, Bm, M, N, K, a_mn, b_mn)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    for _ in range(args.steps):
+        for (a_mn, b_mn), (A, Bm) in ops.items():
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.tc_gemm(A, Bm, M, N, K, a_mn, b_mn)
+            e1.record()
+            torch.cuda.synchronize()
+            ms[(a_mn, b_mn)].append(e0.elapsed_time(e1))
+    clk = clocks.stop()
+    if lce.get_error() != 0:
+        raise RuntimeError("device error status in the layout sweep")
+    flops = 2.0 * M * N * K
+    name = {(False, False): "A K-major, B K-major",
+            (False, True): "A K-major, B MN-major",
+            (True, False): "A MN-major, B K-major",
+            (True, True): "A MN-major, B MN-major"}
+    out = {}
+    for k, v in ms.items():
+        med = statistics.median(v)
+        out[name[k]] = {"ms_median": med, "tflops": flops / med / 1e9}
+    print(json.dumps({"layout_sweep": out, "M": M, "N": N, "K": K,
+                      "steps": args.steps, "cta_pair": B.get_cta_pair(),
+                      "clocks": clk}), flush=True)
 
 
 def bench_mlp(args):

@@ -41,9 +41,17 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_forward_slice", "lce_combine_workspace_size",
             "lce_combine_slices", "lce_backward_slice", "lce_set_wave_sync",
             "lce_get_wave_sync", "lce_slice_exp_workspace_size",
-            "lce_forward_slice_exp", "lce_backward_slice_exp")
+            "lce_forward_slice_exp", "lce_backward_slice_exp",
+            "lce_forward_ex", "lce_backward_ex", "lce_forward_backward_ex",
+            "lce_shard_sums", "lce_combine_shards")
 
-KERNEL_KINDS = 21
+KERNEL_KINDS = 22
+
+
+class LossOpts(ctypes.Structure):
+    """lce_loss_opts: label smoothing in [0, 1] and the z-loss coefficient."""
+    _fields_ = [("label_smoothing", ctypes.c_float),
+                ("z_loss", ctypes.c_float)]
 
 
 class KernelStat(ctypes.Structure):
@@ -104,6 +112,21 @@ def load(build_if_missing: bool = False):
         lib.lce_forward_backward.argtypes = [p, p, i32, p, i64, i64, i64, i64,
                                              i64, p, p, p, p, p, sz, p]
         lib.lce_forward_backward.restype = i32
+        opts = ctypes.POINTER(LossOpts)
+        lib.lce_forward_ex.argtypes = [p, p, i32, p, i64, i64, i64, i64, opts,
+                                       p, p, p, sz, p]
+        lib.lce_forward_ex.restype = i32
+        lib.lce_backward_ex.argtypes = [p, p, i32, p, p, i64, i64, i64, i64,
+                                        opts, p, i64, p, p, p, sz, p]
+        lib.lce_backward_ex.restype = i32
+        lib.lce_forward_backward_ex.argtypes = [p, p, i32, p, i64, i64, i64,
+                                                i64, opts, i64, p, p, p, p, p,
+                                                sz, p]
+        lib.lce_forward_backward_ex.restype = i32
+        lib.lce_shard_sums.argtypes = [p, p, p, p]
+        lib.lce_shard_sums.restype = i32
+        lib.lce_combine_shards.argtypes = [p, p, p, p, p, p]
+        lib.lce_combine_shards.restype = i32
         lib.lce_scale_gradients.argtypes = [p, i32, i64, i64, p, i64, p, p]
         lib.lce_scale_gradients.restype = i32
         lib.lce_count_valid.argtypes = [p, i64, i64, i64, p, p]
@@ -208,10 +231,19 @@ def alloc_workspace(L, H, V, dtype, chunk_rows, device) -> torch.Tensor:
                        dtype=torch.uint8, device=device)
 
 
+def _opts(label_smoothing: float, z_loss: float):
+    """The lce_loss_opts pointer for a loss variant, or None (plain loss)."""
+    if label_smoothing == 0.0 and z_loss == 0.0:
+        return None
+    return ctypes.pointer(LossOpts(float(label_smoothing), float(z_loss)))
+
+
 def forward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
             ignore_index: int = IGNORE_INDEX, workspace=None,
-            loss_out=None, lse_out=None):
-    """Returns (loss [scalar fp32], lse [L] fp32), both on h's device."""
+            loss_out=None, lse_out=None, label_smoothing: float = 0.0,
+            z_loss: float = 0.0):
+    """Returns (loss [scalar fp32], lse [L] fp32), both on h's device.
+    label_smoothing / z_loss select a loss variant (lce_forward_ex)."""
     lib = load()
     _check_inputs(h, W, labels)
     L, H = h.shape
@@ -221,19 +253,31 @@ def forward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
         workspace = alloc_workspace(L, H, V, h.dtype, 0, dev)
     loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float32, device=dev)
     lse = lse_out if lse_out is not None else torch.empty(L, dtype=torch.float32, device=dev)
-    st = lib.lce_forward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
-                         labels.data_ptr(), L, H, V, ignore_index,
-                         loss.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-                         workspace.numel(), _stream_ptr(dev))
-    _check(st, "lce_forward")
+    opts = _opts(label_smoothing, z_loss)
+    if opts is None:
+        st = lib.lce_forward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                             labels.data_ptr(), L, H, V, ignore_index,
+                             loss.data_ptr(), lse.data_ptr(),
+                             workspace.data_ptr(), workspace.numel(),
+                             _stream_ptr(dev))
+        _check(st, "lce_forward")
+    else:
+        st = lib.lce_forward_ex(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                                labels.data_ptr(), L, H, V, ignore_index,
+                                opts, loss.data_ptr(), lse.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(dev))
+        _check(st, "lce_forward_ex")
     return loss, lse
 
 
 def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
              lse: torch.Tensor, dloss: torch.Tensor,
              ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
-             workspace=None, dH_out=None, dW_out=None):
-    """Returns (dH [L,H] of h's dtype, dW [V,H] fp32)."""
+             workspace=None, dH_out=None, dW_out=None,
+             label_smoothing: float = 0.0, z_loss: float = 0.0):
+    """Returns (dH [L,H] of h's dtype, dW [V,H] fp32). The loss variant
+    must be the forward's."""
     lib = load()
     _check_inputs(h, W, labels)
     L, H = h.shape
@@ -246,19 +290,31 @@ def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
         workspace = alloc_workspace(L, H, V, h.dtype, chunk_rows, dev)
     dH = dH_out if dH_out is not None else torch.empty_like(h)
     dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
-    st = lib.lce_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
-                          labels.data_ptr(), lse.data_ptr(), L, H, V,
-                          ignore_index, dloss.data_ptr(), chunk_rows,
-                          dH.data_ptr(), dW.data_ptr(), workspace.data_ptr(),
-                          workspace.numel(), _stream_ptr(dev))
-    _check(st, "lce_backward")
+    opts = _opts(label_smoothing, z_loss)
+    if opts is None:
+        st = lib.lce_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                              labels.data_ptr(), lse.data_ptr(), L, H, V,
+                              ignore_index, dloss.data_ptr(), chunk_rows,
+                              dH.data_ptr(), dW.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(),
+                              _stream_ptr(dev))
+        _check(st, "lce_backward")
+    else:
+        st = lib.lce_backward_ex(h.data_ptr(), W.data_ptr(), _dtype_code(h),
+                                 labels.data_ptr(), lse.data_ptr(), L, H, V,
+                                 ignore_index, opts, dloss.data_ptr(),
+                                 chunk_rows, dH.data_ptr(), dW.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(),
+                                 _stream_ptr(dev))
+        _check(st, "lce_backward_ex")
     return dH, dW
 
 
 def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
                      ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
                      workspace=None, loss_out=None, lse_out=None, dH_out=None,
-                     dW_out=None):
+                     dW_out=None, label_smoothing: float = 0.0,
+                     z_loss: float = 0.0):
     """Loss, lse and the gradients of the loss itself (dloss = 1) in one
     call, without recomputing the logits. Returns (loss, lse, dH, dW)."""
     lib = load()
@@ -272,13 +328,25 @@ def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
     lse = lse_out if lse_out is not None else torch.empty(L, dtype=torch.float32, device=dev)
     dH = dH_out if dH_out is not None else torch.empty_like(h)
     dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
-    st = lib.lce_forward_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
-                                  labels.data_ptr(), L, H, V, ignore_index,
-                                  chunk_rows, loss.data_ptr(), lse.data_ptr(),
-                                  dH.data_ptr(), dW.data_ptr(),
-                                  workspace.data_ptr(), workspace.numel(),
-                                  _stream_ptr(dev))
-    _check(st, "lce_forward_backward")
+    opts = _opts(label_smoothing, z_loss)
+    if opts is None:
+        st = lib.lce_forward_backward(h.data_ptr(), W.data_ptr(),
+                                      _dtype_code(h), labels.data_ptr(), L, H,
+                                      V, ignore_index, chunk_rows,
+                                      loss.data_ptr(), lse.data_ptr(),
+                                      dH.data_ptr(), dW.data_ptr(),
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_ptr(dev))
+        _check(st, "lce_forward_backward")
+    else:
+        st = lib.lce_forward_backward_ex(h.data_ptr(), W.data_ptr(),
+                                         _dtype_code(h), labels.data_ptr(), L,
+                                         H, V, ignore_index, opts, chunk_rows,
+                                         loss.data_ptr(), lse.data_ptr(),
+                                         dH.data_ptr(), dW.data_ptr(),
+                                         workspace.data_ptr(),
+                                         workspace.numel(), _stream_ptr(dev))
+        _check(st, "lce_forward_backward_ex")
     return loss, lse, dH, dW
 
 
@@ -308,6 +376,44 @@ def count_valid(labels: torch.Tensor, V: int,
                                 _stream_ptr(labels.device))
     _check(st, "lce_count_valid")
     return out
+
+
+def shard_sums(loss_local: torch.Tensor, n_local: torch.Tensor,
+               out=None) -> torch.Tensor:
+    """Device float64 [2] = (N_r loss_r, N_r) of one row shard, to be summed
+    over the shards (lce_shard_sums)."""
+    loss_local = loss_local.reshape(1).to(torch.float32).contiguous()
+    n_local = n_local.reshape(1).to(torch.int64).contiguous()
+    dev = loss_local.device
+    if out is None:
+        out = torch.empty(2, dtype=torch.float64, device=dev)
+    st = load().lce_shard_sums(loss_local.data_ptr(), n_local.data_ptr(),
+                               out.data_ptr(), _stream_ptr(dev))
+    _check(st, "lce_shard_sums")
+    return out
+
+
+def combine_shards(sums: torch.Tensor, n_local: torch.Tensor,
+                   dloss: torch.Tensor | None = None):
+    """From the shards' summed (S, N): (loss = S / N, this shard's gradient
+    weight dloss N_r / N), device float32 scalars, 0 when N = 0
+    (lce_combine_shards)."""
+    if sums.dtype != torch.float64 or sums.numel() != 2 or not sums.is_cuda:
+        raise ValueError("sums must be a CUDA float64 tensor of 2 elements")
+    sums = sums.contiguous()
+    dev = sums.device
+    n_local = n_local.reshape(1).to(torch.int64).contiguous()
+    d = None
+    if dloss is not None:
+        d = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    weight = torch.empty((), dtype=torch.float32, device=dev)
+    st = load().lce_combine_shards(sums.data_ptr(), n_local.data_ptr(),
+                                   d.data_ptr() if d is not None else None,
+                                   loss.data_ptr(), weight.data_ptr(),
+                                   _stream_ptr(dev))
+    _check(st, "lce_combine_shards")
+    return loss, weight
 
 
 def forward_slice(h: torch.Tensor, W_slice: torch.Tensor,
@@ -585,17 +691,18 @@ class LinearCrossEntropy(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, h, W, labels, ignore_index=IGNORE_INDEX, chunk_rows=0,
-                fused=False):
+                fused=False, label_smoothing=0.0, z_loss=0.0):
         ctx.ignore_index = ignore_index
         ctx.chunk_rows = chunk_rows
         ctx.fused = fused
         ctx.w_dtype = W.dtype
+        ctx.variant = dict(label_smoothing=label_smoothing, z_loss=z_loss)
         if fused:
             loss, _, dH, dW = forward_backward(h, W, labels, ignore_index,
-                                               chunk_rows)
+                                               chunk_rows, **ctx.variant)
             ctx.save_for_backward(dH, dW)
         else:
-            loss, lse = forward(h, W, labels, ignore_index)
+            loss, lse = forward(h, W, labels, ignore_index, **ctx.variant)
             ctx.save_for_backward(h, W, labels, lse)
         return loss
 
@@ -607,11 +714,14 @@ class LinearCrossEntropy(torch.autograd.Function):
         else:
             h, W, labels, lse = ctx.saved_tensors
             dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,
-                              ctx.chunk_rows)
-        return dH, dW.to(ctx.w_dtype), None, None, None, None
+                              ctx.chunk_rows, **ctx.variant)
+        return dH, dW.to(ctx.w_dtype), None, None, None, None, None, None
 
 
 def linear_cross_entropy(h, W, labels, ignore_index: int = IGNORE_INDEX,
-                         chunk_rows: int = 0, fused: bool = False):
+                         chunk_rows: int = 0, fused: bool = False,
+                         label_smoothing: float = 0.0, z_loss: float = 0.0):
+    """Mean cross entropy of h W^T against labels (autograd). label_smoothing
+    and z_loss select the loss variants of lce_forward_ex."""
     return LinearCrossEntropy.apply(h, W, labels, ignore_index, chunk_rows,
-                                    fused)
+                                    fused, label_smoothing, z_loss)

@@ -10,7 +10,6 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
-#include <numeric>
 #include <string>
 #include <vector>
 
@@ -46,7 +45,7 @@ const char* const kKindNames[LCE_KERNEL_KINDS] = {
     "test_gemm",    "wait_probe",   "gemm_fused",    "grad_from_exp",
     "scale_grads",  "mlp_gate_up",  "mlp_down",      "mlp_da",
     "mlp_dx",       "mlp_dWd",      "mlp_dWgu",      "slice_stats",
-    "combine_slices"};
+    "combine_slices", "shard_combine"};
 
 struct ProfRec {
   int kind;
@@ -233,78 +232,29 @@ lce_status tmap_store_box(CUtensorMap* tm, const void* base, int64_t cols,
                    CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// ---- tuning of the contractions' memory behaviour -----------------------
-// Per contraction kind: the L2 eviction priority of each operand's loads and
-// the tile grouping of tile-per-unit contractions; plus the L2 budget that
-// bounds the live A row panels when choosing column splits. Defaults are the
-// values below; LCE_TUNE="kind.a=H,kind.b=H,kind.g=G,kind.s=S,kind.p=P,
-// l2mb=M,pace_us=P" (kinds lse, grad, fused, dH, dW, test, mlp, mlpgu; H in 0..2;
-// G >= 0; S >= 1, the placement stride GemmGeom::cl_stride; P the least
-// time in us between two wave-pacing waits, GemmGeom::wave_period, < 0 for
-// none; pace_us sets it for every kind) overrides them.
-enum TuneKind {
-  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_MLP_GU, T_KINDS
-};
-struct Tune {
-  int a_hint[T_KINDS];
-  int b_hint[T_KINDS];
-  int group_n[T_KINDS];
-  int cl_stride[T_KINDS];
-  double l2_budget;
-  // wave pacing: at least this long between two waits (0: before every
-  // tile); < 0: no pacing for this kind
-  double pace_ns[T_KINDS];
+// ---- the contractions' tile order and pacing -------------------------------
+enum ContractionKind {
+  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_MLP_GU
 };
 
-const Tune& tune() {
-  static Tune t = [] {
-    Tune v{};
-    v.l2_budget = 48e6;
-    // the MLP contractions run unpaced: paced, the gate/up contraction (its
-    // heavy epilogue) and da lose more to the waits than dx, dWd and dWgu
-    // gain, and the MLP step measured the same either way
-    v.pace_ns[T_MLP] = -1.0;
-    v.pace_ns[T_MLP_GU] = -1.0;
-    const char* env = std::getenv("LCE_TUNE");
-    if (!env) return v;
-    static const char* names[T_KINDS] = {"lse", "grad", "fused", "dH", "dW",
-                                         "test", "mlp", "mlpgu"};
-    std::string spec(env);
-    size_t pos = 0;
-    while (pos < spec.size()) {
-      size_t end = spec.find(',', pos);
-      if (end == std::string::npos) end = spec.size();
-      const std::string item = spec.substr(pos, end - pos);
-      pos = end + 1;
-      const size_t eq = item.find('=');
-      if (eq == std::string::npos) continue;
-      const std::string key = item.substr(0, eq);
-      const double val = std::atof(item.c_str() + eq + 1);
-      if (key == "l2mb") {
-        if (val > 0) v.l2_budget = val * 1e6;
-        continue;
-      }
-      if (key == "pace_us") {
-        for (int k = 0; k < T_KINDS; ++k) v.pace_ns[k] = val * 1e3;
-        continue;
-      }
-      const size_t dot = key.find('.');
-      if (dot == std::string::npos) continue;
-      const std::string kind = key.substr(0, dot), field = key.substr(dot + 1);
-      for (int k = 0; k < T_KINDS; ++k) {
-        if (kind != names[k]) continue;
-        const int iv = static_cast<int>(val);
-        if (field == "a" && iv >= 0 && iv <= 2) v.a_hint[k] = iv;
-        if (field == "b" && iv >= 0 && iv <= 2) v.b_hint[k] = iv;
-        if (field == "g" && iv >= 0) v.group_n[k] = iv;
-        if (field == "s" && iv >= 1) v.cl_stride[k] = iv;
-        if (field == "p") v.pace_ns[k] = val * 1e3;
-      }
-    }
-    return v;
-  }();
-  return t;
-}
+// The vocabulary sweeps (forward logits and their recompute) take enough
+// column-tile runs per row block that at most this many bytes of A row
+// panels are live at once; they stay in L2 while every CTA sweeps W.
+constexpr double kL2PanelBudget = 48e6;
+
+// dH and dW walk their output tiles in groups of kGroupN column tiles, the
+// row blocks varying inside a group, so a wave of 76 pair tiles spans about
+// 9.5 row blocks x 8 column panels instead of 4.75 x 16 and reads fewer
+// distinct operand panels from DRAM. On the 8B shard this cut each launch's
+// DRAM reads from 30.3 to 25.5 GB (dH) and from 32.2 to 27.3 GB (dW), and
+// the step by 0.5%. The tile order changes no result: every tile is
+// computed by the same arithmetic wherever it sits in the order.
+constexpr int kGroupN = 8;
+
+// Wave pacing applies to every contraction but the gated MLP's, which
+// measured the same or slower paced: the gate/up contraction (its heavy
+// epilogue) and da lose more to the waits than dx, dWd and dWgu gain.
+bool paced_kind(int kind) { return kind != T_MLP && kind != T_MLP_GU; }
 
 // Wave pacing of the contractions (GemmGeom::wave_ctr): on unless
 // LCE_WAVE_SYNC=0 or lce_set_wave_sync(0).
@@ -331,7 +281,7 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 void choose_splits(int num_m, int num_n, int nsm, int64_t K, int* splits,
                    int* tps, int rows_per_unit = BM) {
   const double panel = static_cast<double>(rows_per_unit) * K * 2.0;
-  int s_min = static_cast<int>(std::ceil(nsm * panel / tune().l2_budget));
+  int s_min = static_cast<int>(std::ceil(nsm * panel / kL2PanelBudget));
   const int s_max = std::max(1, std::min(kMaxSplits, num_n));
   s_min = std::max(1, std::min(s_min, s_max));
   const double work = static_cast<double>(num_m) * num_n;
@@ -370,9 +320,6 @@ GemmGeom make_geom(int64_t M, int64_t N, int64_t K, int splits, int tps,
   g.num_units = g.num_m * splits;
   g.timeout_ns = wait_timeout_ns();
   g.group_n = 0;
-  g.a_hint = g.b_hint = 0;
-  g.cl_stride = 1;
-  g.wave_period = 1;
   return g;
 }
 
@@ -390,7 +337,7 @@ struct GemmOperands {
   const void* b;
   int64_t b_ld;
   bool sweep;          // sweep all column tiles per row block (choose splits)
-  int kind;            // TuneKind
+  int kind;            // ContractionKind
   // B from two maps (GemmGeom::b_dual): 1 = along N (b2 has b's shape;
   // tiles of 128 output columns), 2 = along K (b covers k < k_split, b2
   // the rest; both have b's row stride)
@@ -401,7 +348,7 @@ struct GemmOperands {
 
 struct GemmPlan {
   bool pair;
-  int kind;  // TuneKind
+  int kind;  // ContractionKind
   GemmGeom g;
   CUtensorMap ta, tb, tb2;
   int grid;
@@ -420,10 +367,7 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   if (o.sweep) choose_splits(num_m, num_n, slots, o.K, &splits, &tps, rows_unit);
   pl->g = make_geom(o.M, o.N, o.K, splits, tps, rows_unit);
   pl->g.num_n = num_n;
-  const Tune& tn = tune();
-  pl->g.a_hint = tn.a_hint[o.kind];
-  pl->g.b_hint = tn.b_hint[o.kind];
-  if (!o.sweep) pl->g.group_n = tn.group_n[o.kind];
+  if (!o.sweep && (o.kind == T_DH || o.kind == T_DW)) pl->g.group_n = kGroupN;
   pl->g.b_dual = o.b_dual;
   pl->g.k_split_kb = o.b_dual == 2 ? static_cast<int>(o.k_split / BK) : 0;
   lce_status st = o.a_mn ? tmap_mnmajor(&pl->ta, o.a, o.M, o.K, o.a_ld)
@@ -445,28 +389,21 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   if (st != LCE_OK) return st;
   const int units = std::max(1, std::min(pl->g.num_units, slots));
   pl->grid = pl->pair ? 2 * units : units;
-  const int stride = tn.cl_stride[o.kind];
-  if (stride > 1 && std::gcd(stride, units) == 1) pl->g.cl_stride = stride;
   return LCE_OK;
 }
 
 // Turn on wave pacing for one launch: the counter is zeroed on the stream
 // first. A wait runs out after ~two tiles' worth of MMA time at full rate.
 cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
-  if (!wave_sync_on() || !ctr || tune().pace_ns[pl->kind] < 0)
-    return cudaSuccess;
+  if (!wave_sync_on() || !ctr || !paced_kind(pl->kind)) return cudaSuccess;
   const GemmGeom& g = pl->g;
   const int slots = pl->pair ? pl->grid / 2 : pl->grid;
   // the most output tiles any CTA (cluster) walks, as the kernels assign
-  // them (first unit, then every slots-th)
+  // them (unit c, then every slots-th)
   uint32_t most = 0;
   for (int c = 0; c < slots; ++c) {
-    const int first = g.cl_stride > 1
-                          ? static_cast<int>((static_cast<int64_t>(c) *
-                                              g.cl_stride) % slots)
-                          : c;
     uint32_t n = 0;
-    for (int u = first; u < g.num_units; u += slots) {
+    for (int u = c; u < g.num_units; u += slots) {
       if (g.group_n > 0 && g.tiles_per_split == 1) {
         n += 1;
       } else {
@@ -481,8 +418,6 @@ cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
   const double per_slot = 1.5e15 / (pl->pair ? 76 : 152);
   const double tile_ns = tile_flops / per_slot * 1e9;
   const double ns = 2.0 * tile_ns;
-  pl->g.wave_period = static_cast<uint32_t>(
-      std::max(1.0, std::floor(tune().pace_ns[pl->kind] / tile_ns)));
   pl->g.wave_ctr = static_cast<unsigned*>(ctr);
   pl->g.wave_wait_ns = static_cast<uint32_t>(
       std::min(2.0e6, std::max(2.0e4, ns)));
@@ -518,8 +453,8 @@ cudaError_t run_store(const GemmPlan& pl, bool a_mn, bool b_mn,
 }
 
 struct WsLayout {
-  size_t n_valid, block_sums, part_m, part_s, zy, h16, w16, G, tile_max,
-      total;
+  size_t n_valid, block_sums, part_m, part_s, part_z, zy, h16, w16, G,
+      tile_max, total;
   size_t fwd_total;  // what the forward-only calls use: everything before G
   size_t sync;       // wave-pacing counter of the gradient contractions
   int64_t chunk, ldg;
@@ -618,6 +553,7 @@ WsLayout ws_layout(int64_t L, int64_t H, int64_t V, lce_dtype dt,
   w.block_sums = take(nb * 8);
   w.part_m = take(static_cast<size_t>(kMaxSplits) * L * 4);
   w.part_s = take(static_cast<size_t>(kMaxSplits) * L * 4);
+  w.part_z = take(static_cast<size_t>(kMaxSplits) * L * 4);
   w.zy = take(L * 4);
   if (dt == LCE_F32) {
     w.h16 = take(static_cast<size_t>(L) * H * 2);
@@ -663,6 +599,30 @@ lce_status operands(const void* h, const void* W, lce_dtype dt, int64_t L,
   *hb = h16;
   *Wb = w16;
   return LCE_OK;
+}
+
+// The loss variant of an optional lce_loss_opts: eps in [0, 1], zcoef >= 0,
+// both finite; NULL is the plain loss.
+struct Variant {
+  float eps = 0.f, zcoef = 0.f;
+  bool smooth() const { return eps != 0.f; }
+  VariantGrad grad(int64_t V) const {
+    VariantGrad v{2.f * zcoef, 1.f - eps, 0.f};
+    if (eps != 0.f)
+      v.eps_v = static_cast<float>(static_cast<double>(eps) /
+                                   static_cast<double>(V));
+    return v;
+  }
+};
+
+bool read_variant(const lce_loss_opts* o, Variant* v) {
+  *v = Variant{};
+  if (!o) return true;
+  if (!(o->label_smoothing >= 0.f && o->label_smoothing <= 1.f)) return false;
+  if (!(o->z_loss >= 0.f && o->z_loss <= 3.0e38f)) return false;
+  v->eps = o->label_smoothing;
+  v->zcoef = o->z_loss;
+  return true;
 }
 
 }  // namespace
@@ -724,6 +684,17 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
                        const int64_t* labels, int64_t L, int64_t H, int64_t V,
                        int64_t ignore_index, float* loss, float* lse, void* ws,
                        size_t ws_bytes, void* stream) {
+  return lce_forward_ex(h, W, dt, labels, L, H, V, ignore_index, nullptr, loss,
+                        lse, ws, ws_bytes, stream);
+}
+
+lce_status lce_forward_ex(const void* h, const void* W, lce_dtype dt,
+                          const int64_t* labels, int64_t L, int64_t H,
+                          int64_t V, int64_t ignore_index,
+                          const lce_loss_opts* opts, float* loss, float* lse,
+                          void* ws, size_t ws_bytes, void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   if (!h || !W || !labels || !loss || !lse || !ws) return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, V)) return LCE_ERR_INVALID_ARG;
@@ -764,6 +735,7 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
   p.zy = reinterpret_cast<float*>(wsb + w.zy);
   p.ignore_index = ignore_index;
+  p.part_z = var.smooth() ? reinterpret_cast<float*>(wsb + w.part_z) : nullptr;
   e = pace(&pl, wsb + w.sync, s);
   if (e != cudaSuccess) return cuda_fail(e, "pace");
   {
@@ -778,7 +750,8 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
   {
     ProfScope ps(LCE_K_LSE_COMBINE, s);
     e = launch_lse_combine(p.part_m, p.part_s, g.splits, p.zy, labels, L, V,
-                           ignore_index, lse, block_sums, &nblocks, s);
+                           ignore_index, lse, block_sums, &nblocks, s,
+                           p.part_z, var.eps, var.zcoef);
     ps.done(0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "lse_combine");
@@ -804,7 +777,8 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
                          int64_t H, int64_t V, int64_t v0, int64_t V_total,
                          int64_t ignore_index, const float* dloss,
                          int64_t chunk_rows, void* dH, bool dh_f32, float* dW,
-                         void* ws, size_t ws_bytes, void* stream) {
+                         void* ws, size_t ws_bytes, void* stream,
+                         const VariantGrad& var) {
   if (!h || !W || !labels || !lse || !dloss || !dH || !dW || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
@@ -856,6 +830,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       p.ignore_index = ignore_index;
       p.v0 = v0;
       p.v_total = V_total;
+      p.var = var;
       e = pace(&pl, wsb + w.sync, s);
       if (e != cudaSuccess) return cuda_fail(e, "pace");
       CUtensorMap tg;
@@ -919,8 +894,22 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
                         int64_t H, int64_t V, int64_t ignore_index,
                         const float* dloss, int64_t chunk_rows, void* dH,
                         float* dW, void* ws, size_t ws_bytes, void* stream) {
+  return lce_backward_ex(h, W, dt, labels, lse, L, H, V, ignore_index,
+                         nullptr, dloss, chunk_rows, dH, dW, ws, ws_bytes,
+                         stream);
+}
+
+lce_status lce_backward_ex(const void* h, const void* W, lce_dtype dt,
+                           const int64_t* labels, const float* lse, int64_t L,
+                           int64_t H, int64_t V, int64_t ignore_index,
+                           const lce_loss_opts* opts, const float* dloss,
+                           int64_t chunk_rows, void* dH, float* dW, void* ws,
+                           size_t ws_bytes, void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   return backward_impl(h, W, dt, labels, lse, L, H, V, 0, V, ignore_index,
-                       dloss, chunk_rows, dH, false, dW, ws, ws_bytes, stream);
+                       dloss, chunk_rows, dH, false, dW, ws, ws_bytes, stream,
+                       var.grad(V));
 }
 
 lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
@@ -934,7 +923,7 @@ lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
     return LCE_ERR_INVALID_ARG;
   return backward_impl(h, W, dt, labels, lse, L, H, Vs, v0, V_total,
                        ignore_index, dloss, chunk_rows, dH_part, true, dW, ws,
-                       ws_bytes, stream);
+                       ws_bytes, stream, Variant{}.grad(V_total));
 }
 
 lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
@@ -1235,6 +1224,21 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
                                 int64_t chunk_rows, float* loss, float* lse,
                                 void* dH, float* dW, void* ws, size_t ws_bytes,
                                 void* stream) {
+  return lce_forward_backward_ex(h, W, dt, labels, L, H, V, ignore_index,
+                                 nullptr, chunk_rows, loss, lse, dH, dW, ws,
+                                 ws_bytes, stream);
+}
+
+lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
+                                   const int64_t* labels, int64_t L, int64_t H,
+                                   int64_t V, int64_t ignore_index,
+                                   const lce_loss_opts* opts,
+                                   int64_t chunk_rows, float* loss, float* lse,
+                                   void* dH, float* dW, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
+  const VariantGrad vg = var.grad(V);
   if (!h || !W || !labels || !loss || !lse || !dH || !dW || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
@@ -1268,6 +1272,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
   float* tile_max = reinterpret_cast<float*>(wsb + w.tile_max);
   float* part_m = reinterpret_cast<float*>(wsb + w.part_m);
   float* part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  float* part_z =
+      var.smooth() ? reinterpret_cast<float*>(wsb + w.part_z) : nullptr;
   float* zy = reinterpret_cast<float*>(wsb + w.zy);
   double* block_sums = reinterpret_cast<double*>(wsb + w.block_sums);
   const size_t dh_elem = dt == LCE_F32 ? 4 : 2;
@@ -1294,6 +1300,7 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       p.ldg = w.ldg;
       p.tile_max = tile_max;
       p.ignore_index = ignore_index;
+      p.part_z = part_z;
       e = pace(&pl, wsb + w.sync, s);
       if (e != cudaSuccess) return cuda_fail(e, "pace");
       CUtensorMap te;
@@ -1309,7 +1316,7 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       ProfScope ps(LCE_K_LSE_COMBINE, s);
       e = launch_lse_combine(part_m, part_s, splits, zy, labels + c0, cr, V,
                              ignore_index, lse + c0, block_sums + block_off,
-                             &nb, s);
+                             &nb, s, part_z, var.eps, var.zcoef);
       ps.done(0);
       if (e != cudaSuccess) return cuda_fail(e, "lse_combine");
       block_off += nb;
@@ -1319,7 +1326,7 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
       ProfScope ps(LCE_K_GRAD_FROM_EXP, s);
       e = launch_grad_from_exp(E, w.ldg, tile_max, num_n, lse + c0,
                                labels + c0, cr, V, ignore_index, dev->num_sms,
-                               s);
+                               s, 0, 0, vg);
       ps.done(0);
       if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
     }
@@ -1414,6 +1421,47 @@ lce_status lce_count_valid(const int64_t* labels, int64_t L, int64_t V,
     ps.done(0);
   }
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "count_valid");
+}
+
+lce_status lce_shard_sums(const float* loss_local, const int64_t* n_local,
+                          double* sums, void* stream) {
+  if (!loss_local || !n_local || !sums) return LCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(loss_local) & 3u) ||
+      (reinterpret_cast<uintptr_t>(n_local) & 7u) ||
+      (reinterpret_cast<uintptr_t>(sums) & 7u))
+    return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(LCE_K_SHARD_COMBINE, s);
+  cudaError_t e = launch_shard_sums(
+      loss_local, reinterpret_cast<const unsigned long long*>(n_local), sums,
+      s);
+  ps.done(0);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "shard_sums");
+}
+
+lce_status lce_combine_shards(const double* sums, const int64_t* n_local,
+                              const float* dloss, float* loss, float* weight,
+                              void* stream) {
+  if (!sums || !n_local || !loss || !weight) return LCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(sums) & 7u) ||
+      (reinterpret_cast<uintptr_t>(n_local) & 7u) ||
+      (reinterpret_cast<uintptr_t>(dloss) & 3u) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u) ||
+      (reinterpret_cast<uintptr_t>(weight) & 3u))
+    return LCE_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  lce_status st = device_info(&dev);
+  if (st != LCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope ps(LCE_K_SHARD_COMBINE, s);
+  cudaError_t e = launch_combine_shards(
+      sums, reinterpret_cast<const unsigned long long*>(n_local), dloss, loss,
+      weight, s);
+  ps.done(0);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "combine_shards");
 }
 
 // ---- sequence-tiled gated MLP ----------------------------------------------

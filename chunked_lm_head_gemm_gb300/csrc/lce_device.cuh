@@ -125,32 +125,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// L2 eviction-priority policies for the hinted loads below.
-__device__ __forceinline__ uint64_t l2_policy(int hint) {
-  uint64_t p = 0;
-  if (hint == 1)
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
-                 : "=l"(p));
-  else if (hint == 2)
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
-                 : "=l"(p));
-  return p;
-}
-
-// As tma_load_2d, with an L2 eviction-priority policy.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
-                                                 const CUtensorMap* tm,
-                                                 int32_t c0, int32_t c1,
-                                                 uint32_t bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar),
-      "l"(policy)
-      : "memory");
-}
-
 // TMA bulk store of one 2D box from this CTA's shared memory to global
 // memory (bulk-group completion), and the group bookkeeping around it.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm,
@@ -183,17 +157,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a),
                "r"(b), "r"(c), "r"(d)
                : "memory");
-}
-
-// One operand box: hinted when the contraction asks for it.
-__device__ __forceinline__ void tma_load_op(uint32_t dst, const CUtensorMap* tm,
-                                            int32_t c0, int32_t c1,
-                                            uint32_t bar, int hint,
-                                            uint64_t policy) {
-  if (hint)
-    tma_load_2d_hint(dst, tm, c0, c1, bar, policy);
-  else
-    tma_load_2d(dst, tm, c0, c1, bar);
 }
 
 // ---------------------------------------------------------------------------
@@ -398,19 +361,6 @@ __device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u,
   return t;
 }
 
-// The first unit of CTA (or cluster) `slot` of `slots`: slot * cl_stride mod
-// slots (a permutation when cl_stride is coprime with slots; the host
-// ensures it), so the units that run at the same time can be placed on
-// other SMs than consecutive slots would give. Off (1) by default: a trial
-// with several strides changed neither the DRAM re-reads nor the time.
-__device__ __forceinline__ int first_unit(const GemmGeom& g, int slot,
-                                          int slots) {
-  return g.cl_stride > 1
-             ? static_cast<int>((static_cast<int64_t>(slot) * g.cl_stride) %
-                                slots)
-             : slot;
-}
-
 // ---------------------------------------------------------------------------
 // epilogues: one thread per accumulator row, 32 columns per TMEM load
 // ---------------------------------------------------------------------------
@@ -462,6 +412,7 @@ struct EpiBase {
 struct EpiLse : EpiBase {
   using Params = LseParams;
   float m2, s;
+  float zs;  // sum of the unit's logits (label smoothing only)
   int64_t row;
   int yv;  // label if it takes part, else -1
   bool row_ok;
@@ -478,6 +429,7 @@ struct EpiLse : EpiBase {
     }
     m2 = -INFINITY;
     s = 0.f;
+    zs = 0.f;
   }
 
   __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
@@ -500,6 +452,13 @@ struct EpiLse : EpiBase {
           if (i == yo) zyv = v[i];
         p.zy[row] = zyv;
       }
+      if (p.part_z != nullptr) {  // warp-uniform
+        float za[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) za[i & 3] += v[i];
+        zs += (za[0] + za[1]) + (za[2] + za[3]);
+      }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -521,14 +480,18 @@ struct EpiLse : EpiBase {
     if (row_ok) {
       p.part_m[static_cast<int64_t>(t.split) * g.M + row] = m2;
       p.part_s[static_cast<int64_t>(t.split) * g.M + row] = s;
+      if (p.part_z != nullptr)
+        p.part_z[static_cast<int64_t>(t.split) * g.M + row] = zs;
     }
   }
 };
 
 // Backward recompute: G = exp(z - lse) - [j == y] for rows that take part,
 // 0 for the others, rounded to bf16 and written by TMA stores of staged
-// 32 x 32 boxes (EpiBase::store_box). The dloss/N scale is applied later, in
-// fp32, by the dH and dW epilogues.
+// 32 x 32 boxes (EpiBase::store_box). With a loss variant, G = zf exp(z -
+// lse) - ome [j == y] - eps_v (VariantGrad); the plain constants {1, 1, 0}
+// leave every value's bits as the plain formula gives them. The dloss/N
+// scale is applied later, in fp32, by the dH and dW epilogues.
 struct EpiGrad : EpiBase {
   using Params = GradParams;
   int64_t row;
@@ -536,6 +499,7 @@ struct EpiGrad : EpiBase {
   bool takes;  // the row takes part in the loss
   int yv;      // label column in this contraction, or -1
   float lse2;
+  float zf;    // 1 + 2 zcoef lse (1 for the plain loss)
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
@@ -544,10 +508,14 @@ struct EpiGrad : EpiBase {
     takes = false;
     yv = -1;
     lse2 = 0.f;
+    zf = 1.f;
     if (row_ok) {
       yv = label_column(p.labels[row], g.N, p.v0, p.v_total, p.ignore_index,
                         &takes);
-      if (takes) lse2 = p.lse[row] * LOG2E;
+      if (takes) {
+        lse2 = p.lse[row] * LOG2E;
+        zf = fmaf(p.var.zloss2, p.lse[row], 1.f);
+      }
     }
   }
 
@@ -564,8 +532,10 @@ struct EpiGrad : EpiBase {
       const int yo = yv - static_cast<int>(j0);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float gi = takes ? ex2(fmaf(v[i], LOG2E, -lse2)) : 0.f;
-        if (i == yo) gi -= 1.f;
+        float gi = takes ? fmaf(ex2(fmaf(v[i], LOG2E, -lse2)), zf,
+                                -p.var.eps_v)
+                         : 0.f;
+        if (i == yo) gi -= p.var.ome;
         v[i] = gi;
       }
       // rows past M and columns past N hold junk that the store drops
@@ -587,6 +557,7 @@ struct EpiGrad : EpiBase {
 struct EpiFused : EpiBase {
   using Params = FusedParams;
   float m2, s;
+  float zs;  // sum of the unit's logits (label smoothing only)
   int64_t row;
   int yv;
   bool row_ok;
@@ -603,6 +574,7 @@ struct EpiFused : EpiBase {
     }
     m2 = -INFINITY;
     s = 0.f;
+    zs = 0.f;
   }
 
   __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
@@ -626,6 +598,13 @@ struct EpiFused : EpiBase {
         for (int i = 0; i < 32; ++i)
           if (i == yo) zyv = v[i];
         if (row_ok) p.zy[row] = zyv;
+      }
+      if (p.part_z != nullptr) {  // warp-uniform
+        float za[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) za[i & 3] += v[i];
+        zs += (za[0] + za[1]) + (za[2] + za[3]);
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -666,6 +645,8 @@ struct EpiFused : EpiBase {
     if (row_ok) {
       p.part_m[static_cast<int64_t>(t.split) * g.M + row] = m2;
       p.part_s[static_cast<int64_t>(t.split) * g.M + row] = s;
+      if (p.part_z != nullptr)
+        p.part_z[static_cast<int64_t>(t.split) * g.M + row] = zs;
     }
   }
 };
@@ -947,16 +928,13 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
                                               const SmemMap& sm,
                                               const WaitCtx& ctx) {
   uint32_t stage = 0, phase = 0, issued = 0;
-  const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
   uint32_t step = 0;  // output tiles whose loads this CTA has issued
-  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units;
-       u += gridDim.x) {
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     const int m0 = t.m_blk * BM;
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
-      if (g.wave_period <= 1 || step % g.wave_period == 0)
-        wave_wait(g, step * gridDim.x);
+      wave_wait(g, step * gridDim.x);
       const int n0 = (t.n_first + tt) * BN;
       for (int kb = 0; kb < g.num_kb; ++kb) {
         if (!mbar_wait(sm.empty(stage), phase ^ 1u, ctx, true)) {
@@ -971,10 +949,9 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
         if (A_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_op(sa + j * 64 * BK * 2, ta, m0 + 64 * j, k0, fb,
-                        g.a_hint, pa);
+            tma_load_2d(sa + j * 64 * BK * 2, ta, m0 + 64 * j, k0, fb);
         } else {
-          tma_load_op(sa, ta, k0, m0, fb, g.a_hint, pa);
+          tma_load_2d(sa, ta, k0, m0, fb);
         }
         // B from the second map past the K split (dual along K)
         const bool second = g.b_dual == 2 && kb >= g.k_split_kb;
@@ -983,15 +960,14 @@ __device__ __forceinline__ void role_producer(const CUtensorMap* ta,
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_op(sb + j * 64 * BK * 2, tbk, n0 + 64 * j, kq, fb,
-                        g.b_hint, pb);
+            tma_load_2d(sb + j * 64 * BK * 2, tbk, n0 + 64 * j, kq, fb);
         } else if (g.b_dual == 1) {
           // dual along N: 128 rows of each map, same rows
           const int nr = (t.n_first + tt) * (BN / 2);
-          tma_load_op(sb, tb, k0, nr, fb, g.b_hint, pb);
-          tma_load_op(sb + (BN / 2) * BK * 2, tb2, k0, nr, fb, g.b_hint, pb);
+          tma_load_2d(sb, tb, k0, nr, fb);
+          tma_load_2d(sb + (BN / 2) * BK * 2, tb2, k0, nr, fb);
         } else {
-          tma_load_op(sb, tbk, kq, n0, fb, g.b_hint, pb);
+          tma_load_2d(sb, tbk, kq, n0, fb);
         }
         ++issued;
         if (++stage == STAGES) {
@@ -1022,7 +998,7 @@ __device__ __forceinline__ void role_mma(const GemmGeom& g, const SmemMap& sm,
   constexpr uint32_t MN_LBO = 64 * BK * 2;  // one 64-wide MN box: 8 KB
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int u = first_unit(g, blockIdx.x, gridDim.x); ok && u < g.num_units; u += gridDim.x) {
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
       if (!mbar_wait(sm.tempty(acc), acc_phase ^ 1u, ctx, true)) {
@@ -1078,7 +1054,7 @@ __device__ __forceinline__ void role_epilogue(const GemmGeom& g,
   Epi epi;
   epi.te = te;
   epi.stage = stage_base + static_cast<uint32_t>(q) * 2u * EPI_BUF_BYTES;
-  for (int u = first_unit(g, blockIdx.x, gridDim.x); u < g.num_units; u += gridDim.x) {
+  for (int u = blockIdx.x; u < g.num_units; u += gridDim.x) {
     const Unit t = decode_unit(g, u);
     epi.begin_unit(p, g, t, r);
     bool ok = true;
@@ -1251,31 +1227,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst,
-                                                      const CUtensorMap* tm,
-                                                      int32_t c0, int32_t c1,
-                                                      uint32_t bar_cluster,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
-      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], "
-      "%5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1),
-      "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_op_pair(uint32_t dst,
-                                                 const CUtensorMap* tm,
-                                                 int32_t c0, int32_t c1,
-                                                 uint32_t bar_cluster,
-                                                 int hint, uint64_t policy) {
-  if (hint)
-    tma_load_2d_pair_hint(dst, tm, c0, c1, bar_cluster, policy);
-  else
-    tma_load_2d_pair(dst, tm, c0, c1, bar_cluster);
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
                                                 uint32_t ncols) {
   asm volatile(
@@ -1364,17 +1315,15 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
                                                    const WaitCtx& ctx) {
   const bool leader = rank == 0;
   const int nclusters = gridDim.x >> 1;
-  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
+  const int cluster = blockIdx.x >> 1;
   uint32_t stage = 0, phase = 0, issued = 0;
-  const uint64_t pa = l2_policy(g.a_hint), pb = l2_policy(g.b_hint);
   bool ok = true;
   uint32_t step = 0;  // output tiles whose loads this CTA has issued
   for (int u = cluster; ok && u < g.num_units; u += nclusters) {
     const Unit t = decode_unit(g, u, 2 * BM, static_cast<int>(rank));
     const int a0 = static_cast<int>(t.row0);  // this CTA's 128 rows of A
     for (int tt = 0; ok && tt < t.n_count; ++tt) {
-      if (leader && (g.wave_period <= 1 || step % g.wave_period == 0))
-        wave_wait(g, step * static_cast<uint32_t>(nclusters));
+      if (leader) wave_wait(g, step * static_cast<uint32_t>(nclusters));
       // this CTA's 128 of the tile's 256 output columns; dual along N: the
       // leader takes the first map's 128 rows, the peer the second's
       const bool dual_n = g.b_dual == 1;
@@ -1394,10 +1343,9 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
         if (A_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_op_pair(sa + j * 64 * BK * 2, ta, a0 + 64 * j, k0, fb,
-                             g.a_hint, pa);
+            tma_load_2d_pair(sa + j * 64 * BK * 2, ta, a0 + 64 * j, k0, fb);
         } else {
-          tma_load_op_pair(sa, ta, k0, a0, fb, g.a_hint, pa);
+          tma_load_2d_pair(sa, ta, k0, a0, fb);
         }
         const bool second = g.b_dual == 2 && kb >= g.k_split_kb;
         const CUtensorMap* tbk = second ? tb2 : tbn;
@@ -1405,10 +1353,9 @@ __device__ __forceinline__ void role_producer_pair(const CUtensorMap* ta,
         if (B_MN) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j)
-            tma_load_op_pair(sb + j * 64 * BK * 2, tbk, b0 + 64 * j, kq, fb,
-                             g.b_hint, pb);
+            tma_load_2d_pair(sb + j * 64 * BK * 2, tbk, b0 + 64 * j, kq, fb);
         } else {
-          tma_load_op_pair(sb, tbk, kq, b0, fb, g.b_hint, pb);
+          tma_load_2d_pair(sb, tbk, kq, b0, fb);
         }
         ++issued;
         if (++stage == STAGES2) {
@@ -1442,7 +1389,7 @@ __device__ __forceinline__ void role_mma_pair(const GemmGeom& g,
   constexpr uint32_t IDESC = idesc_pair_bf16_f32<A_MN, B_MN>();
   constexpr uint32_t MN_LBO = 64 * BK * 2;
   const int nclusters = gridDim.x >> 1;
-  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
+  const int cluster = blockIdx.x >> 1;
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
   for (int u = cluster; ok && u < g.num_units; u += nclusters) {
@@ -1494,7 +1441,7 @@ __device__ __forceinline__ void role_epilogue_pair(
   const int q = warp & 3;
   const int r = q * 32 + lane;
   const int nclusters = gridDim.x >> 1;
-  const int cluster = first_unit(g, blockIdx.x >> 1, nclusters);
+  const int cluster = blockIdx.x >> 1;
   uint32_t acc = 0, acc_phase = 0;
   Epi epi;
   epi.te = te;

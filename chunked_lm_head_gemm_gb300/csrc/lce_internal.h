@@ -49,18 +49,12 @@ struct GemmGeom {
   // block major; g > 0 = groups of g column tiles, row blocks inside a
   // group (a wave then touches fewer column panels).
   int group_n;
-  // L2 eviction priority of each operand's TMA loads: 0 = default,
-  // 1 = evict first (streamed), 2 = evict last (reused).
-  int a_hint, b_hint;
   // B from two tensor maps: 0 = one map; 1 = along N, each 256-row B tile
   // being 128 rows of the first map then the same 128 rows of the second
   // (tiles then cover 128 output columns, num_n = ceil(N / 128)); 2 = along
   // K, k-blocks from k_split_kb on read the second map (at k - k_split_kb).
   int b_dual;
   int k_split_kb;
-  // Placement: CTA (or cluster) i starts at unit (i * cl_stride) mod the
-  // grid's CTAs (clusters); 1 = in order. Coprime with that count.
-  int cl_stride;
   // Wave pacing (nullptr: off): before its s-th output tile (s >= 1) a
   // CTA's (a pair's leader's) producer waits until *wave_ctr >= s * (CTAs or
   // clusters of the grid), i.e. until every CTA has issued the loads of s
@@ -73,7 +67,6 @@ struct GemmGeom {
   unsigned* wave_ctr;
   uint32_t wave_wait_ns;
   uint32_t wave_steps;
-  uint32_t wave_period;  // wait before every wave_period-th tile only (>= 1)
 };
 
 // ---- epilogue parameter blocks ----------------------------------------------
@@ -92,6 +85,19 @@ struct LseParams {
   float* zy;              // [M], logit at the label (rows whose label is here)
   int64_t ignore_index;
   int64_t v0, v_total;
+  float* part_z;          // [splits][M], sum of the logits (label smoothing),
+                          // or NULL
+};
+
+// The loss variants' constants for the gradient logits (all rows that take
+// part): G = zf_i softmax - ome [j == y] - eps_v with zf_i = 1 + zloss2 lse_i,
+// i.e. zloss2 = 2 * z-loss coefficient, ome = 1 - label smoothing, eps_v =
+// label smoothing / V. The plain loss is {0, 1, 0}, whose arithmetic gives
+// the plain gradient's bits exactly.
+struct VariantGrad {
+  float zloss2;
+  float ome;
+  float eps_v;
 };
 
 // Backward recompute tile -> G = softmax - onehot (unscaled), bf16.
@@ -103,6 +109,7 @@ struct GradParams {
   int64_t ldg;
   int64_t ignore_index;
   int64_t v0, v_total;    // vocabulary slice, as LseParams
+  VariantGrad var;        // loss variant ({0, 1, 0}: plain)
 };
 
 // Fused forward+backward, logits of one row chunk -> per-split online
@@ -120,6 +127,7 @@ struct FusedParams {
   float* tile_max;        // [M][num_n], log2 units
   int64_t ignore_index;
   int64_t v0, v_total;    // vocabulary slice, as LseParams
+  float* part_z;          // [splits][M] logit sums, or NULL (as LseParams)
 };
 
 // Gated-MLP gate/up contraction (B dual along N): accumulator columns
@@ -219,12 +227,17 @@ cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
                                int64_t ignore_index,
                                unsigned long long* n_valid, unsigned* err,
                                cudaStream_t s);
+// lse per row from the split partials, and per-256-row float64 sums of the
+// loss terms of the rows that take part: lse - z_y for the plain loss; with
+// a variant (part_z set or zcoef != 0) lse - (1 - eps) z_y - (eps / V)
+// sum_j z_j + zcoef lse^2, the logit sums merged from part_z in split order.
 cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
                                int splits, const float* zy,
                                const int64_t* labels, int64_t L, int64_t V,
                                int64_t ignore_index, float* lse,
                                double* block_sums, int* nblocks_out,
-                               cudaStream_t s);
+                               cudaStream_t s, const float* part_z = nullptr,
+                               float eps = 0.f, float zcoef = 0.f);
 // Vocabulary slice: merge the per-split partials into the slice's per-row
 // max logit m (natural units) and sum of exp(z - m), and the label logit
 // (0 where the label is not in [v0, v0 + Vs)).
@@ -248,7 +261,9 @@ cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
                                cudaStream_t s);
 // In place over one row chunk: E[i][j] = 2^(u - tile max) becomes
-// G = 2^(tile max - lse_i log2 e) E - [j == y_i] (bf16), 0 on ignored rows.
+// G = 2^(tile max - lse_i log2 e) E - [j == y_i] (bf16), 0 on ignored rows;
+// with a loss variant, G = zf_i 2^(tile max - lse_i log2 e) E - ome [j ==
+// y_i] - eps_v (VariantGrad).
 // For a vocabulary slice (v0, v_total as LseParams) the onehot sits at
 // column y_i - v0 and validity is judged against v_total.
 cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
@@ -256,12 +271,22 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
                                  int num_sms, cudaStream_t s,
-                                 int64_t v0 = 0, int64_t v_total = 0);
+                                 int64_t v0 = 0, int64_t v_total = 0,
+                                 VariantGrad var = VariantGrad{0.f, 1.f, 0.f});
 // dH *= dloss[0] (bf16 or fp32) and dW *= dloss[0], skipped when dloss is 1.
 cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
                                int64_t n_dw, const float* dloss,
                                cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned* err, uint64_t timeout_ns,
                               cudaStream_t s);
+// Row-sharded sequences: sums = (N_r loss_r, N_r) in float64; from the
+// shards' summed pair, the sequence's loss and this shard's gradient weight.
+cudaError_t launch_shard_sums(const float* loss_local,
+                              const unsigned long long* n_local, double* sums,
+                              cudaStream_t s);
+cudaError_t launch_combine_shards(const double* sums,
+                                  const unsigned long long* n_local,
+                                  const float* dloss, float* loss,
+                                  float* weight, cudaStream_t s);
 
 }  // namespace lce

@@ -45,8 +45,11 @@ cudaError_t launch_count_valid(const int64_t* labels, int64_t L, int64_t V,
 }
 
 // lse_i = ln 2 * (M + log2 sum_k s_k 2^(m_k - M)), M = max_k m_k, merging the
-// per-split partials in a fixed order; then a fixed-order block sum of
-// (lse_i - z_i,y_i) over rows that take part, in float64.
+// per-split partials in a fixed order; then a fixed-order block sum of the
+// loss terms of the rows that take part, in float64: lse_i - z_i,y_i, or
+// with a loss variant the smoothed cross entropy plus the z-loss,
+// lse_i - (1 - eps) z_i,y_i - (eps / V) sum_j z_ij + zcoef lse_i^2 (the
+// logit sums merged from part_z in split order).
 constexpr int COMBINE_THREADS = COMBINE_ROWS;
 
 __global__ void __launch_bounds__(COMBINE_THREADS)
@@ -55,7 +58,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
                   const float* __restrict__ zy,
                   const int64_t* __restrict__ labels, int64_t L, int64_t V,
                   int64_t ignore_index, float* __restrict__ lse,
-                  double* __restrict__ block_sums) {
+                  double* __restrict__ block_sums,
+                  const float* __restrict__ part_z, float eps, float zcoef) {
   __shared__ double warp_sums[COMBINE_THREADS / 32];
   const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
                     threadIdx.x;
@@ -68,8 +72,20 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
       t += part_s[k * L + i] * exp2f(part_m[k * L + i] - M);
     const float l = (M + log2f(t)) * LN2;
     lse[i] = l;
-    if (label_valid(labels[i], V, ignore_index))
-      term = static_cast<double>(l) - static_cast<double>(zy[i]);
+    if (label_valid(labels[i], V, ignore_index)) {
+      if (part_z == nullptr && zcoef == 0.f) {
+        term = static_cast<double>(l) - static_cast<double>(zy[i]);
+      } else {
+        const double ld = static_cast<double>(l);
+        double zsum = 0.0;
+        if (part_z != nullptr)
+          for (int k = 0; k < splits; ++k) zsum += part_z[k * L + i];
+        const double e = static_cast<double>(eps);
+        term = ld - (1.0 - e) * static_cast<double>(zy[i]) -
+               e / static_cast<double>(V) * zsum +
+               static_cast<double>(zcoef) * ld * ld;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
@@ -87,12 +103,13 @@ cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
                                const int64_t* labels, int64_t L, int64_t V,
                                int64_t ignore_index, float* lse,
                                double* block_sums, int* nblocks_out,
-                               cudaStream_t s) {
+                               cudaStream_t s, const float* part_z, float eps,
+                               float zcoef) {
   const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
   *nblocks_out = nb;
   k_lse_combine<<<nb, COMBINE_THREADS, 0, s>>>(part_m, part_s, splits, zy,
                                                labels, L, V, ignore_index, lse,
-                                               block_sums);
+                                               block_sums, part_z, eps, zcoef);
   return cudaGetLastError();
 }
 
@@ -237,19 +254,22 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n,
 // In place over one row chunk of the fused forward+backward: E holds
 // e = 2^(u - m_t) (bf16), u = z log2 e, m_t the maximum of u over the
 // 256-column tile; with lse2 = lse log2 e the softmax is e 2^(m_t - lse2),
-// so G = e 2^(m_t - lse2) - [j == y] on rows that take part, 0 elsewhere.
+// so G = e 2^(m_t - lse2) - [j == y] on rows that take part, 0 elsewhere;
+// with a loss variant G = zf e 2^(m_t - lse2) - ome [j == y] - eps_v
+// (VariantGrad; zf folded into the scale sc).
 // Works on 16-byte vectors of 8 consecutive columns (8 divides the
 // 256-column tile, so a vector never straddles two tiles). Columns between
 // V and ldg are padding that nothing reads.
-__device__ __forceinline__ uint4 exp_to_grad(uint4 in, float sc, int yo) {
+__device__ __forceinline__ uint4 exp_to_grad(uint4 in, float sc, int yo,
+                                             float ome, float eps_v) {
   const uint32_t w[4] = {in.x, in.y, in.z, in.w};
   uint32_t o[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    float lo = __uint_as_float(w[q] << 16) * sc;
-    float hi = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
-    if (2 * q == yo) lo -= 1.f;
-    if (2 * q + 1 == yo) hi -= 1.f;
+    float lo = fmaf(__uint_as_float(w[q] << 16), sc, -eps_v);
+    float hi = fmaf(__uint_as_float(w[q] & 0xFFFF0000u), sc, -eps_v);
+    if (2 * q == yo) lo -= ome;
+    if (2 * q + 1 == yo) hi -= ome;
     o[q] = pack_bf16x2(lo, hi);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -269,7 +289,7 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
                     const float* __restrict__ lse,
                     const int64_t* __restrict__ labels, int64_t rows,
                     int64_t V, int64_t ignore_index, int64_t slice_v0,
-                    int64_t v_total) {
+                    int64_t v_total, VariantGrad var) {
   const int64_t nvec = (V + 7) / 8;
   const int64_t vt = v_total > 0 ? v_total : V;
   const int64_t total = rows * nvec;
@@ -289,6 +309,7 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
       continue;
     }
     const float l2 = lse[row] * LOG2E;
+    const float zf = fmaf(var.zloss2, lse[row], 1.f);
     const float* tm = tile_max + row * num_n;
     // the label's column in this slice, or far below any column
     const int64_t yl = y - slice_v0;
@@ -306,8 +327,9 @@ __global__ void __launch_bounds__(GFE_THREADS, GFE_BLOCKS_PER_SM)
         const int64_t v = v0 + static_cast<int64_t>(k) * GFE_THREADS;
         if (v < ve) {
           const int64_t j0 = v * 8;
-          er[v] = exp_to_grad(in[k], ex2(tm[j0 >> 8] - l2),
-                              ycol - static_cast<int>(j0));
+          er[v] = exp_to_grad(in[k], ex2(tm[j0 >> 8] - l2) * zf,
+                              ycol - static_cast<int>(j0), var.ome,
+                              var.eps_v);
         }
       }
     }
@@ -319,7 +341,7 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
                                  const float* lse, const int64_t* labels,
                                  int64_t rows, int64_t V, int64_t ignore_index,
                                  int num_sms, cudaStream_t s, int64_t v0,
-                                 int64_t v_total) {
+                                 int64_t v_total, VariantGrad var) {
   const int64_t work = rows * ((V + 7) / 8);
   const int64_t full = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) *
                        GFE_BLOCKS_PER_SM;
@@ -328,7 +350,7 @@ cudaError_t launch_grad_from_exp(uint16_t* E, int64_t ldg,
       static_cast<unsigned>(want < full ? (want < 1 ? 1 : want) : full);
   k_grad_from_exp<<<grid, GFE_THREADS, 0, s>>>(E, ldg, tile_max, num_n, lse,
                                                labels, rows, V, ignore_index,
-                                               v0, v_total);
+                                               v0, v_total, var);
   return cudaGetLastError();
 }
 
@@ -374,6 +396,45 @@ cudaError_t launch_scale_grads(void* dH, int dh_f32, int64_t n_dh, float* dW,
                                int64_t n_dw, const float* dloss,
                                cudaStream_t s) {
   k_scale_grads<<<1024, 256, 0, s>>>(dH, dh_f32, n_dh, dW, n_dw, dloss);
+  return cudaGetLastError();
+}
+
+// Row-sharded sequences: one shard's share of the sequence's loss for the
+// caller's sum over the shards, sums = (N_r loss_r, N_r) in float64; and,
+// from the summed pair (S, N), the sequence's loss S / N and this shard's
+// gradient weight dloss N_r / N, both 0 when N = 0 (a NULL dloss is 1).
+__global__ void k_shard_sums(const float* __restrict__ loss_local,
+                             const unsigned long long* __restrict__ n_local,
+                             double* __restrict__ sums) {
+  const double n = static_cast<double>(*n_local);
+  sums[0] = n * static_cast<double>(*loss_local);
+  sums[1] = n;
+}
+
+__global__ void k_combine_shards(const double* __restrict__ sums,
+                                 const unsigned long long* __restrict__ n_local,
+                                 const float* __restrict__ dloss,
+                                 float* __restrict__ loss,
+                                 float* __restrict__ weight) {
+  const double n = sums[1];
+  const double d = dloss != nullptr ? static_cast<double>(*dloss) : 1.0;
+  *loss = n > 0.0 ? static_cast<float>(sums[0] / n) : 0.f;
+  *weight = n > 0.0 ? static_cast<float>(d * static_cast<double>(*n_local) / n)
+                    : 0.f;
+}
+
+cudaError_t launch_shard_sums(const float* loss_local,
+                              const unsigned long long* n_local, double* sums,
+                              cudaStream_t s) {
+  k_shard_sums<<<1, 1, 0, s>>>(loss_local, n_local, sums);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_shards(const double* sums,
+                                  const unsigned long long* n_local,
+                                  const float* dloss, float* loss,
+                                  float* weight, cudaStream_t s) {
+  k_combine_shards<<<1, 1, 0, s>>>(sums, n_local, dloss, loss, weight);
   return cudaGetLastError();
 }
 

@@ -15,9 +15,11 @@ that comes out scaled by the number of shards when this is missed),
 
 where loss_r, dH'_r, dW'_r are the shard's own mean loss and its gradients.
 The exchange is one all-reduce of two float64 scalars and one sum of the
-V x H fp32 weight gradient. Every loss and gradient value comes from the
-library's kernels; this module only weighs and sums them across the group.
-With no group (or a group of one) it reduces to the single-process call.
+V x H fp32 weight gradient. Every loss and gradient value, and the
+weighting above, comes from the library's kernels (lce_shard_sums,
+lce_combine_shards, lce_scale_gradients); this module only moves data
+between the processes of the group. With no group (or a group of one) it
+reduces to the single-process call.
 """
 from __future__ import annotations
 
@@ -33,23 +35,24 @@ def _world(group) -> int:
     return dist.get_world_size(group)
 
 
-def combine_loss(loss_local: torch.Tensor, n_local: torch.Tensor,
-                 group=None):
-    """(loss, weight) of the whole sequence from one shard's mean loss and
-    valid-row count: loss = sum_r N_r loss_r / sum_r N_r and weight =
-    N_r / sum_r N_r, both 0 when no row of any shard is valid. One
-    all-reduce (sum) of two float64 scalars over `group`; no host sync."""
-    n = n_local.reshape(()).to(torch.float64)
-    t = torch.stack([loss_local.reshape(()).to(torch.float64) * n, n])
+def exchange(sums: torch.Tensor, group=None) -> torch.Tensor:
+    """The shards' (N_r loss_r, N_r) pairs summed in place over `group` (one
+    all-reduce of two float64 values); nothing to do without a group."""
     if _world(group) > 1:
         import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
-    total = t[1]
-    safe = torch.where(total > 0, total, torch.ones_like(total))
-    zero = torch.zeros_like(total)
-    loss = torch.where(total > 0, t[0] / safe, zero)
-    weight = torch.where(total > 0, n / safe, zero)
-    return loss.to(torch.float32), weight
+        dist.all_reduce(sums, op=dist.ReduceOp.SUM, group=group)
+    return sums
+
+
+def combine_loss(loss_local: torch.Tensor, n_local: torch.Tensor,
+                 group=None, dloss: torch.Tensor | None = None):
+    """(loss, weight) of the whole sequence from one shard's mean loss and
+    valid-row count: loss = sum_r N_r loss_r / sum_r N_r and weight =
+    dloss N_r / sum_r N_r (dloss defaults to 1), both 0 when no row of any
+    shard is valid. The arithmetic runs in the library; the exchange is one
+    all-reduce of two float64 scalars over `group`; no host sync."""
+    sums = exchange(B.shard_sums(loss_local, n_local), group)
+    return B.combine_shards(sums, n_local, dloss)
 
 
 def sum_weight_grad(dW: torch.Tensor, group=None) -> torch.Tensor:
@@ -75,11 +78,7 @@ def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
                                              chunk_rows=chunk_rows,
                                              workspace=workspace)
     n_r = B.count_valid(labels, V, ignore_index)
-    loss, weight = combine_loss(loss_r, n_r, group)
-    scale = weight.to(torch.float32)
-    if dloss is not None:
-        scale = scale * dloss.reshape(()).to(device=scale.device,
-                                             dtype=torch.float32)
-    B.scale_gradients(dH, dW, scale)
+    loss, weight = combine_loss(loss_r, n_r, group, dloss)
+    B.scale_gradients(dH, dW, weight)
     sum_weight_grad(dW, group)
     return loss, lse, dH, dW

@@ -161,6 +161,54 @@ lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                void* stream);
 
 /*
+ * Loss variants: label smoothing and z-loss. No counterpart on the pages,
+ * which define only the plain cross entropy ("Training Beyond 1M Tokens",
+ * section "The loss is the first thing to break"); both are common
+ * companions of it in language-model training. For every row that takes
+ * part, with q_j = (1 - label_smoothing) [j == y_i] + label_smoothing / V:
+ *   loss_i = sum_j q_j (lse_i - z_ij) + z_loss * lse_i^2
+ *          = lse_i - (1 - eps) z_{i,y_i} - (eps / V) sum_j z_ij
+ *            + z_loss * lse_i^2                     (eps = label_smoothing)
+ *   loss   = (1/N) sum_{valid i} loss_i               (0 if N = 0)
+ *   G_ij   = dloss/N ((1 + 2 z_loss lse_i) softmax_ij - q_j)
+ * Ignored rows add nothing, as in the plain loss. Fields:
+ *   label_smoothing  in [0, 1]; 0 = the one-hot target
+ *   z_loss           >= 0 and finite; 0 = no z-loss
+ * Other values return LCE_ERR_INVALID_ARG before anything is queued.
+ * A NULL pointer or {0, 0} is the plain loss, computed with exactly the
+ * arithmetic of the calls without options (the same bits). Label smoothing
+ * makes the forward keep, per row and column split, the sum of the logits
+ * as well (a workspace region that lce_workspace_size always counts).
+ */
+typedef struct {
+  float label_smoothing;
+  float z_loss;
+} lce_loss_opts;
+
+/* lce_forward, lce_backward and lce_forward_backward with a loss variant
+ * (opts may be NULL); every other argument as in the call without _ex.
+ * lce_backward_ex must be given the opts of the lce_forward_ex whose lse it
+ * uses (lse itself does not depend on them). */
+lce_status lce_forward_ex(const void* h, const void* W, lce_dtype dt,
+                          const int64_t* labels, int64_t L, int64_t H,
+                          int64_t V, int64_t ignore_index,
+                          const lce_loss_opts* opts, float* loss, float* lse,
+                          void* ws, size_t ws_bytes, void* stream);
+lce_status lce_backward_ex(const void* h, const void* W, lce_dtype dt,
+                           const int64_t* labels, const float* lse, int64_t L,
+                           int64_t H, int64_t V, int64_t ignore_index,
+                           const lce_loss_opts* opts, const float* dloss,
+                           int64_t chunk_rows, void* dH, float* dW, void* ws,
+                           size_t ws_bytes, void* stream);
+lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
+                                   const int64_t* labels, int64_t L, int64_t H,
+                                   int64_t V, int64_t ignore_index,
+                                   const lce_loss_opts* opts,
+                                   int64_t chunk_rows, float* loss, float* lse,
+                                   void* dH, float* dW, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/*
  * Vocabulary-parallel form (several processes each hold a slice of the
  * head's rows, W[v0 .. v0 + Vs) of a vocabulary of V_total, and all of h).
  * "Training Beyond 1M Tokens", section "The massive logits matrix: chunk
@@ -275,6 +323,36 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
 lce_status lce_count_valid(const int64_t* labels, int64_t L, int64_t V,
                            int64_t ignore_index, int64_t* n_valid,
                            void* stream);
+
+/*
+ * The row-sharded sequence's loss and gradient weights, from each shard's
+ * own call. Same source as lce_count_valid; the TRL PR #6845 page ("TRL:
+ * document 1M-token training and add a context-parallelism example"),
+ * table "Assumptions", lists an evaluation loss that comes out scaled by
+ * the number of shards, the kind of mistake a single global N prevents.
+ * With shard r's mean loss loss_r over N_r valid rows (lce_forward or
+ * lce_forward_backward on its rows, N_r from lce_count_valid):
+ *   lce_shard_sums:     sums[0] = N_r loss_r, sums[1] = N_r   (float64)
+ *   (the caller sums `sums` over the shards, e.g. one all-reduce)
+ *   lce_combine_shards: loss   = S / N                  (S, N the summed pair)
+ *                       weight = dloss N_r / N          (dloss NULL: 1)
+ *                       both 0 when N = 0
+ * Shard r's gradients from the call on its rows (those of its own mean
+ * loss) times weight are its share of the sequence's gradients: dH stays on
+ * the shard, dW is the sum over the shards (lce_scale_gradients then one
+ * all-reduce).
+ *   loss_local  device, [1] float32;  n_local device, [1] int64
+ *   sums        device, [2] float64 (out of lce_shard_sums, in of
+ *               lce_combine_shards), 8-byte aligned
+ *   dloss       device, [1] float32 or NULL; loss, weight device [1] float32
+ * Each queues one single-thread kernel on `stream`; argument errors return
+ * before anything is queued.
+ */
+lce_status lce_shard_sums(const float* loss_local, const int64_t* n_local,
+                          double* sums, void* stream);
+lce_status lce_combine_shards(const double* sums, const int64_t* n_local,
+                              const float* dloss, float* loss, float* weight,
+                              void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
@@ -407,7 +485,7 @@ int lce_get_wave_sync(void);
  * per tensor-core contraction, 0 for the other kernels). Host-side state
  * only; events are created on first use and reused.
  */
-#define LCE_KERNEL_KINDS 21
+#define LCE_KERNEL_KINDS 22
 enum {
   LCE_K_COUNT_VALID = 0,
   LCE_K_GEMM_LSE = 1,
@@ -429,7 +507,8 @@ enum {
   LCE_K_MLP_DWD = 17,
   LCE_K_MLP_DWGU = 18,
   LCE_K_SLICE_STATS = 19,
-  LCE_K_COMBINE_SLICES = 20
+  LCE_K_COMBINE_SLICES = 20,
+  LCE_K_SHARD_COMBINE = 21
 };
 
 typedef struct {

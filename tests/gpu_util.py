@@ -61,26 +61,29 @@ class cta_pair:
 
 
 def run_gpu(h, W, y, dloss=1.0, chunk_rows=0, ignore_index=-100,
-            mode="separate", pair=None):
+            mode="separate", pair=None, **variant):
     """Forward + backward through the library; returns host float64 arrays.
 
     mode "separate": lce_forward then lce_backward (logits recomputed);
     mode "fused": lce_forward_backward, then lce_scale_gradients by dloss.
-    pair: True/False selects CTA-pair or single-CTA contractions."""
+    pair: True/False selects CTA-pair or single-CTA contractions.
+    variant: label_smoothing / z_loss (the _ex calls)."""
     with cta_pair(pair):
-        return _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode)
+        return _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode,
+                        variant)
 
 
-def _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode):
+def _run_gpu(h, W, y, dloss, chunk_rows, ignore_index, mode, variant):
     import chunked_lm_head_gemm_gb300 as lce
     d = torch.full((), float(dloss), device=h.device)
     if mode == "fused":
         loss, lse, dH, dW = lce.forward_backward(h, W, y, ignore_index,
-                                                 chunk_rows)
+                                                 chunk_rows, **variant)
         lce.scale_gradients(dH, dW, d)
     else:
-        loss, lse = lce.forward(h, W, y, ignore_index)
-        dH, dW = lce.backward(h, W, y, lse, d, ignore_index, chunk_rows)
+        loss, lse = lce.forward(h, W, y, ignore_index, **variant)
+        dH, dW = lce.backward(h, W, y, lse, d, ignore_index, chunk_rows,
+                              **variant)
     status = lce.get_error()
     return dict(loss=float(loss.item()), lse=to64(lse), dH=to64(dH),
                 dW=to64(dW), status=status)

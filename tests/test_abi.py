@@ -56,10 +56,11 @@ def test_workspace_size(lib):
     c = lib.lce_default_chunk_rows(L, H, V)
     assert c % 128 == 0 and 0 < c <= L
     assert f(L, H, V, 0, 0) >= c * V * 2
-    # plus the forward statistics (16 splits x (max, sum) + the label logit)
-    # and the fused path's per-tile row maxima (chunk x ceil(V/256) floats)
+    # plus the forward statistics (16 splits x (max, sum, logit sum) + the
+    # label logit) and the fused path's per-tile row maxima (chunk x
+    # ceil(V/256) floats)
     tiles = -(-V // 256)
-    assert f(L, H, V, 0, 0) < (c * V * 2 + (16 * 8 + 4 + 1) * L +
+    assert f(L, H, V, 0, 0) < (c * V * 2 + (16 * 12 + 4 + 1) * L +
                                4 * c * tiles + (1 << 20))
     # peak extra memory is O(chunk * V), far below the L x V fp32 logits
     assert f(L, H, V, 0, 0) < L * V * 4 / 8
@@ -116,6 +117,28 @@ def test_bad_arguments_return_before_any_device_call(lib):
     assert lib.lce_slice_exp_workspace_size(1024, 64, 1000, 0) >= 1024 * 1000 * 2
     assert lib.lce_combine_workspace_size(0) == 0
     assert lib.lce_combine_workspace_size(300) == 256 + 2 * 8
+    # loss variants: out-of-range options are refused before anything else
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    for eps, zc in ((-0.1, 0.0), (1.5, 0.0), (0.0, -1.0),
+                    (0.0, float("inf")), (float("nan"), 0.0)):
+        o = ctypes.pointer(B.LossOpts(eps, zc))
+        assert lib.lce_forward_ex(p, p, 0, p, 8, 8, 8, -100, o, p, p, p,
+                                  1 << 30, null) == 1
+        assert lib.lce_backward_ex(p, p, 0, p, p, 8, 8, 8, -100, o, p, 0, p,
+                                   p, p, 1 << 30, null) == 1
+        assert lib.lce_forward_backward_ex(p, p, 0, p, 8, 8, 8, -100, o, 0,
+                                           p, p, p, p, p, 1 << 30, null) == 1
+    ok = ctypes.pointer(B.LossOpts(0.1, 1e-4))
+    assert lib.lce_forward_ex(p, p, 0, p, 8, 8, 8, -100, ok, p, p, p, 16,
+                              null) == 3
+    assert lib.lce_forward_ex(p, p, 0, p, 8, 8, 8, -100, None, p, p, p, 16,
+                              null) == 3
+    # the shard combine: null or misaligned pointers
+    assert lib.lce_shard_sums(null, p, p, null) == 1
+    assert lib.lce_shard_sums(p, p, ctypes.c_void_p(0x1004), null) == 1
+    assert lib.lce_combine_shards(p, p, null, null, p, null) == 1
+    assert lib.lce_combine_shards(p, ctypes.c_void_p(0x1004), null, p, p,
+                                  null) == 1
     # test hooks
     assert lib.lce_test_gemm(null, p, p, 8, 8, 8, 0, 0, null) == 1
     assert lib.lce_test_gemm(p, p, p, 8, 12, 8, 0, 0, null) == 1

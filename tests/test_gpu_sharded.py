@@ -1,9 +1,10 @@
 """Row-sharded loss on the GPU, the shards run one after another on one
-device: each shard's lce_forward_backward and lce_count_valid, weighed by
-N_r / N and summed on the host, must give the whole sequence's loss and
-gradients ("Training Beyond 1M Tokens", section "One GPU is not enough:
-split the sequence across many"). Also the valid-row count against the
-oracle, bit for bit."""
+device: each shard's lce_forward_backward and lce_count_valid, its
+(N_r loss_r, N_r) from lce_shard_sums, the pairs summed (standing in for
+the all-reduce) and weighed by lce_combine_shards, must give the whole
+sequence's loss and gradients ("Training Beyond 1M Tokens", section "One
+GPU is not enough: split the sequence across many"). Also the valid-row
+count against the oracle, bit for bit, and the combine's edge cases."""
 import pytest
 import torch
 
@@ -60,17 +61,20 @@ def test_sequential_shards_equal_whole_sequence(pair):
                 h[r0:r1].contiguous(), W, y[r0:r1].contiguous())
             n_r = B.count_valid(y[r0:r1].contiguous(), WL.V)
             parts.append((loss_r, lse_r, dH_r, dW_r, n_r))
-        # the host-side combine: loss = sum N_r loss_r / N, weight N_r / N
-        n_tot = sum(p[4].to(torch.float64) for p in parts)
-        loss = sum(p[0].to(torch.float64) * p[4].to(torch.float64)
-                   for p in parts) / n_tot
+        # the library's combine: each shard's (N_r loss_r, N_r), their sum
+        # (the all-reduce of a process group), loss and weight per shard
+        total = sum(B.shard_sums(p[0], p[4]) for p in parts)
+        d = torch.full((), dloss, device=dev)
         dW = torch.zeros(WL.V, WL.H, dtype=torch.float32, device=dev)
         dH = []
+        losses = []
         for loss_r, lse_r, dH_r, dW_r, n_r in parts:
-            scale = (n_r.to(torch.float64) / n_tot * dloss).to(torch.float32)
-            lce.scale_gradients(dH_r, dW_r, scale)
+            loss, weight = B.combine_shards(total, n_r, d)
+            losses.append(loss)
+            lce.scale_gradients(dH_r, dW_r, weight)
             dH.append(dH_r)
             dW += dW_r
+        assert all(torch.equal(x, losses[0]) for x in losses)
         dH = torch.cat(dH)
         lse = torch.cat([p[1] for p in parts])
         assert lce.get_error() == 0
@@ -105,3 +109,28 @@ def test_sharded_call_without_group_is_the_single_call():
     assert lce.get_error() == 0
     assert torch.equal(loss, ref[0]) and torch.equal(lse, ref[1])
     assert torch.equal(dH, ref[2]) and torch.equal(dW, ref[3])
+
+
+def test_combine_shards_edge_cases():
+    """N = 0 over all shards gives loss 0 and weight 0; a shard without a
+    valid row gets weight 0; a missing dloss counts as 1; the weights of
+    the shards sum to dloss."""
+    dev = require_gpu()
+    n = [torch.tensor([k], dtype=torch.int64, device=dev) for k in (38, 0,
+                                                                    24)]
+    ls = [torch.tensor(v, dtype=torch.float32, device=dev)
+          for v in (2.0, 0.0, 3.5)]
+    total = sum(B.shard_sums(l, k) for l, k in zip(ls, n))
+    assert total[1].item() == 62.0
+    assert total[0].item() == 38 * 2.0 + 24 * 3.5
+    d = torch.full((), 0.5, device=dev)
+    out = [B.combine_shards(total, k, d) for k in n]
+    assert out[0][0].item() == pytest.approx((76.0 + 84.0) / 62.0, rel=1e-7)
+    assert out[1][1].item() == 0.0
+    assert sum(w.item() for _, w in out) == pytest.approx(0.5, rel=1e-6)
+    assert B.combine_shards(total, n[2])[1].item() == pytest.approx(
+        24 / 62, rel=1e-7)
+    zero = B.shard_sums(ls[1], n[1])
+    loss, weight = B.combine_shards(zero, n[1], d)
+    assert loss.item() == 0.0 and weight.item() == 0.0
+    assert B.get_error() == 0

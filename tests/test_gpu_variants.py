@@ -1,0 +1,135 @@
+"""Label smoothing and z-loss on the GPU against the float64 oracle.
+
+Neither variant is on the pages, which define only the plain cross entropy
+("Training Beyond 1M Tokens", section "The loss is the first thing to
+break"). The reading: label smoothing eps takes each valid row's cross
+entropy against the target (1 - eps) onehot + eps / V; the z-loss adds
+coef * lse^2 per valid row; the mean runs over the valid rows. Both paths
+(recomputing and fused) and both contraction variants, on the small
+workload (fp32 inputs), a ragged multi-tile shape with several backward
+chunks, and a row slice of the 8B head shape (full H and V). With both
+options 0 the _ex calls give the plain calls' bits.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_lm_head_gemm_gb300.inputs import WORKLOADS, Workload, make_inputs
+from tests.gpu_util import (MODES, PAIRS, assert_parity, rel_fro,
+                            require_gpu, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(0.1, 0.0), (0.0, 1e-2), (0.2, 1e-3), (1.0, 0.0)]
+CASES = {
+    "tiny": (WORKLOADS["tiny"], 0),
+    "multi_tile": (Workload("multi_tile", 640, 256, 4100, "bf16", 1.0, 0.05,
+                            "uniform", ignore_frac=0.05), 256),
+    "qwen3-8b[L=256]": (WORKLOADS["qwen3-8b"].with_rows(256), 0),
+}
+_CACHE = {}
+
+
+def _inputs(case, dev):
+    wl, chunk = CASES[case]
+    h, W, y = make_inputs(wl, seed=2, device=dev)
+    return wl, chunk, h, W, y
+
+
+def _oracle(case, eps, zc, h, W, y, vrows):
+    key = (case, eps, zc)
+    if key not in _CACHE:
+        fb = oracle.forward_backward(h.cpu(), W.cpu(), y.cpu(), dloss=1.5,
+                                     vrows=vrows, label_smoothing=eps,
+                                     z_loss=zc)
+        _CACHE[key] = fb
+    return _CACHE[key]
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("eps,zc", VARIANTS,
+                         ids=[f"eps{e}-z{z}" for e, z in VARIANTS])
+@pytest.mark.parametrize("case", list(CASES))
+def test_variant_parity(case, eps, zc, mode, pair):
+    dev = require_gpu()
+    wl, chunk, h, W, y = _inputs(case, dev)
+    gpu = run_gpu(h, W, y, dloss=1.5, chunk_rows=chunk, mode=mode, pair=pair,
+                  label_smoothing=eps, z_loss=zc)
+    assert gpu["status"] == 0
+    vrows = None
+    if wl.V > 10000:
+        yc = y.cpu().numpy()
+        rs = np.random.default_rng(7)
+        vrows = np.unique(np.concatenate(
+            [yc[yc >= 0], rs.integers(0, wl.V, 256), [0, wl.V - 1]]))
+    fb = _oracle(case, eps, zc, h, W, y, vrows)
+    assert_parity(gpu, fb, fb, dW_rows=vrows)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_zero_options_are_the_plain_call(mode):
+    """lce_*_ex with {0, 0} runs the plain arithmetic: identical bits."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    from chunked_lm_head_gemm_gb300 import _binding as B
+    lib = lce.load()
+    wl, chunk, h, W, y = _inputs("multi_tile", dev)
+    L, H = h.shape
+    V = W.shape[0]
+    ws = lce.alloc_workspace(L, H, V, h.dtype, chunk, dev)
+    s = torch.cuda.current_stream().cuda_stream
+    zero = ctypes.pointer(B.LossOpts(0.0, 0.0))
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(L, dtype=torch.float32, device=dev)
+    dH = torch.empty_like(h)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    one = torch.ones(1, device=dev)
+    if mode == "fused":
+        st = lib.lce_forward_backward_ex(
+            h.data_ptr(), W.data_ptr(), 0, y.data_ptr(), L, H, V, -100, zero,
+            chunk, loss.data_ptr(), lse.data_ptr(), dH.data_ptr(),
+            dW.data_ptr(), ws.data_ptr(), ws.numel(), s)
+        assert st == 0
+        ref = lce.forward_backward(h, W, y, chunk_rows=chunk, workspace=ws)
+    else:
+        st = lib.lce_forward_ex(h.data_ptr(), W.data_ptr(), 0, y.data_ptr(),
+                                L, H, V, -100, zero, loss.data_ptr(),
+                                lse.data_ptr(), ws.data_ptr(), ws.numel(), s)
+        assert st == 0
+        st = lib.lce_backward_ex(h.data_ptr(), W.data_ptr(), 0, y.data_ptr(),
+                                 lse.data_ptr(), L, H, V, -100, zero,
+                                 one.data_ptr(), chunk, dH.data_ptr(),
+                                 dW.data_ptr(), ws.data_ptr(), ws.numel(), s)
+        assert st == 0
+        rl, rlse = lce.forward(h, W, y, workspace=ws)
+        rdH, rdW = lce.backward(h, W, y, rlse, one, chunk_rows=chunk,
+                                workspace=ws)
+        ref = (rl, rlse, rdH, rdW)
+    assert lce.get_error() == 0
+    for a, b in zip((loss, lse, dH, dW), ref):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_variant_autograd(mode):
+    """linear_cross_entropy with both options: the same loss and gradients
+    as the explicit calls, and the oracle's."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl, chunk, h, W, y = _inputs("multi_tile", dev)
+    kw = dict(label_smoothing=0.2, z_loss=1e-3)
+    hh = h.clone().requires_grad_(True)
+    WW = W.clone().requires_grad_(True)
+    loss = lce.linear_cross_entropy(hh, WW, y, chunk_rows=chunk,
+                                    fused=(mode == "fused"), **kw)
+    (1.5 * loss).backward()
+    gpu = run_gpu(h, W, y, dloss=1.5, chunk_rows=chunk, mode=mode, **kw)
+    assert loss.item() == gpu["loss"]
+    assert torch.equal(hh.grad.float().cpu(),
+                       torch.from_numpy(gpu["dH"]).float())
+    fb = _oracle("multi_tile", 0.2, 1e-3, h, W, y, None)
+    assert rel_fro(WW.grad.double().cpu().numpy(), fb["dW"]) < 1e-2

@@ -1,11 +1,13 @@
 """Row-sharded loss on CPU: two gloo processes each hold a slice of one
 sequence's rows, compute their shard's mean loss and gradients with the
-float64 oracle (standing in for the GPU library, which needs a device), and
-combine them with chunked_lm_head_gemm_gb300.sharded. The result must equal
-the oracle on the whole sequence: the loss as the mean over ALL valid rows
-(not the mean of the shards' means), each shard's dH rows, and the summed dW
-("Training Beyond 1M Tokens", section "One GPU is not enough: split the
-sequence across many")."""
+float64 oracle (standing in for the GPU library, which needs a device),
+exchange their (N_r loss_r, N_r) pairs and weight gradients with
+chunked_lm_head_gemm_gb300.sharded, and weigh them as the library's
+lce_combine_shards does (that kernel itself is tested on the GPU). The
+result must equal the oracle on the whole sequence: the loss as the mean
+over ALL valid rows (not the mean of the shards' means), each shard's dH
+rows, and the summed dW ("Training Beyond 1M Tokens", section "One GPU is
+not enough: split the sequence across many")."""
 import os
 import socket
 
@@ -49,15 +51,20 @@ def _rank_main(rank, world, port, case, out_dir):
         hs, ys = h[rows], y[rows]
         fw = oracle.forward(hs, W, ys, nthreads=2)
         bw = oracle.backward(hs, W, ys, dloss=1.0, nthreads=2)
-        loss_r = torch.tensor(fw["loss"], dtype=torch.float32)
-        n_r = torch.tensor([fw["n_valid"]], dtype=torch.int64)
-        loss, weight = sharded.combine_loss(loss_r, n_r)
+        # the shard's loss travels as fp32, as the library returns it
+        loss_r = float(np.float32(fw["loss"]))
+        n_r = fw["n_valid"]
+        sums = sharded.exchange(torch.tensor([n_r * loss_r, float(n_r)],
+                                             dtype=torch.float64))
+        total = sums[1].item()
+        loss = sums[0].item() / total if total > 0 else 0.0
+        weight = n_r / total if total > 0 else 0.0
         dloss = 0.75
         dH = torch.from_numpy(bw["dH"]) * (weight * dloss)
         dW = torch.from_numpy(bw["dW"]) * (weight * dloss)
         sharded.sum_weight_grad(dW)
-        np.savez(os.path.join(out_dir, f"rank{rank}.npz"), loss=loss.item(),
-                 loss_r=fw["loss"], weight=weight.item(), dH=dH.numpy(),
+        np.savez(os.path.join(out_dir, f"rank{rank}.npz"), loss=loss,
+                 loss_r=fw["loss"], weight=weight, dH=dH.numpy(),
                  dW=dW.numpy())
     finally:
         dist.destroy_process_group()
@@ -96,10 +103,9 @@ def test_two_rank_gloo_matches_whole_sequence(case, tmp_path, oracle_mod):
         assert not np.any(r[0]["dW"]) and not np.any(r[1]["dH"])
 
 
-def test_single_process_combine_is_identity():
+def test_single_process_exchange_is_identity():
     from chunked_lm_head_gemm_gb300 import sharded
-    loss, weight = sharded.combine_loss(torch.tensor(2.5),
-                                        torch.tensor([17]))
-    assert loss.item() == 2.5 and weight.item() == 1.0
-    loss, weight = sharded.combine_loss(torch.tensor(0.0), torch.tensor([0]))
-    assert loss.item() == 0.0 and weight.item() == 0.0
+    sums = torch.tensor([42.5, 17.0], dtype=torch.float64)
+    assert torch.equal(sharded.exchange(sums.clone()), sums)
+    dW = torch.randn(3, 4)
+    assert torch.equal(sharded.sum_weight_grad(dW.clone()), dW)
