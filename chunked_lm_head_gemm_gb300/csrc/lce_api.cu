@@ -1523,7 +1523,13 @@ lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
   GemmPlan pl;
   lce_status st = plan_gemm(o, dev, &pl);
   if (st != LCE_OK) return st;
-  SwigluParams p{a, g, u, I};
+  SwigluParams p{};
+  if ((st = tmap_store_box(&p.map_a, a, I, cr, I)) != LCE_OK) return st;
+  p.save_gu = g != nullptr && u != nullptr;
+  if (p.save_gu) {
+    if ((st = tmap_store_box(&p.map_g, g, I, cr, I)) != LCE_OK) return st;
+    if ((st = tmap_store_box(&p.map_u, u, I, cr, I)) != LCE_OK) return st;
+  }
   cudaError_t e = pace(&pl, ctr, s);
   if (e != cudaSuccess) return cuda_fail(e, "pace");
   ProfScope ps(LCE_K_MLP_GATE_UP, s);
@@ -1638,7 +1644,13 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       GemmOperands o{cr, I, H, false, true, dyc, H, Wd, I, false, T_MLP};
       GemmPlan pl;
       if ((st = plan_gemm(o, *dev, &pl)) != LCE_OK) return st;
-      SwigluBwdParams p{G, U, I, DGU, 2 * I, I};
+      SwigluBwdParams p{};
+      if ((st = tmap_store_box(&p.map_dgu, DGU, 2 * I, cr, 2 * I)) != LCE_OK)
+        return st;
+      p.g = G;
+      p.u = U;
+      p.ld_gu = I;
+      p.du_off = I;
       cudaError_t e = pace(&pl, wsb + w.sync, s);
       if (e != cudaSuccess) return cuda_fail(e, "pace");
       ProfScope ps(LCE_K_MLP_DA, s);

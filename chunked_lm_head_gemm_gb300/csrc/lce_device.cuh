@@ -381,7 +381,19 @@ struct EpiBase {
   // which drops the rows and columns past the map's extent. Two buffers
   // alternate; a buffer is reused once the store before last has read it.
   __device__ __forceinline__ void store_box(const float (&v)[32], int64_t j0,
-                                            int64_t wrow0) {
+                                            int64_t wrow0,
+                                            const CUtensorMap* map = nullptr) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    store_box_words(w, j0, wrow0, map);
+  }
+
+  // The same box from bf16 pairs already packed (w[i] = columns 2i, 2i + 1
+  // of this lane's row), through `map` (NULL: te).
+  __device__ __forceinline__ void store_box_words(const uint32_t (&w)[16],
+                                                  int64_t j0, int64_t wrow0,
+                                                  const CUtensorMap* map) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t buf = stage + (nstored & 1u) * EPI_BUF_BYTES;
     if (lane == 0 && nstored >= 2) bulk_wait_read1();
@@ -390,15 +402,12 @@ struct EpiBase {
     const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      st_shared_v4(rowa + ((static_cast<uint32_t>(q) ^ sw) << 4),
-                   pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                   pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                   pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      st_shared_v4(rowa + ((static_cast<uint32_t>(q) ^ sw) << 4), w[4 * q],
+                   w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(te, buf, static_cast<int32_t>(j0),
+      tma_store_2d(map ? map : te, buf, static_cast<int32_t>(j0),
                    static_cast<int32_t>(wrow0));
       bulk_commit();
     }
@@ -748,39 +757,23 @@ __device__ __forceinline__ float sigmoid_fast(float t) {
 
 // Gated-MLP gate/up contraction with B dual along N: for the tile's 128
 // output columns, accumulator columns 0..127 are g and 128..255 are u;
-// writes a = silu(g) u (and g, u when asked) in bf16.
+// writes a = silu(g) u (and g, u when asked) in bf16, each 32-column chunk
+// of the warp's 32 rows through a staged box and one TMA store (the store
+// maps drop the rows past M).
 struct EpiSwiGLU : EpiBase {
   using Params = SwigluParams;
   int64_t row;
-  bool row_ok;
 
-  __device__ __forceinline__ void begin_unit(const Params&, const GemmGeom& g,
+  __device__ __forceinline__ void begin_unit(const Params&, const GemmGeom&,
                                              const Unit& t, int r) {
     row = t.row0 + r;
-    row_ok = row < g.M;
-  }
-
-  __device__ __forceinline__ static void store32(uint16_t* dst, const float* v,
-                                                 int nv) {
-    if (nv == 32) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                           pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nv) dst[i] = to_bf16_bits(v[i]);
-    }
   }
 
   __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
                                        const Unit&, int n_blk, uint32_t taddr,
                                        int) {
     const int64_t i0 = static_cast<int64_t>(n_blk) * (BN / 2);
+    const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
       const int64_t j0 = i0 + c * 32;
@@ -788,15 +781,14 @@ struct EpiSwiGLU : EpiBase {
       float gv[32], uv[32];
       tmem_ld32(taddr + c * 32, gv);
       tmem_ld32(taddr + BN / 2 + c * 32, uv);
-      if (!row_ok) continue;
-      const int64_t rem = g.N - j0;
-      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
-      const int64_t off = row * p.ld + j0;
-      if (p.g) store32(p.g + off, gv, nv);
-      if (p.u) store32(p.u + off, uv, nv);
+      if (wrow0 >= g.M) continue;  // warp-uniform: all of the warp's rows
+      if (p.save_gu) {
+        store_box(gv, j0, wrow0, &p.map_g);
+        store_box(uv, j0, wrow0, &p.map_u);
+      }
 #pragma unroll
       for (int i = 0; i < 32; ++i) uv[i] *= gv[i] * sigmoid_fast(gv[i]);
-      store32(p.a + off, uv, nv);
+      store_box(uv, j0, wrow0, &p.map_a);
     }
   }
 
@@ -806,6 +798,9 @@ struct EpiSwiGLU : EpiBase {
 
 // Gated-MLP backward: accumulator = da; dg = da u silu'(g),
 // du = da silu(g), with silu'(t) = s (1 + t (1 - s)), s the logistic.
+// I is a multiple of 64 (checked by the host), so every 32-column chunk is
+// whole; g and u of a chunk are loaded one chunk ahead (per thread, its own
+// row), dg and du leave through staged boxes and TMA stores of [dg | du].
 struct EpiSwiGLUBwd : EpiBase {
   using Params = SwigluBwdParams;
   int64_t row;
@@ -833,66 +828,49 @@ struct EpiSwiGLUBwd : EpiBase {
     }
   }
 
-  // Whole 32-column chunks have their g and u loaded one chunk ahead, so
-  // the loads overlap the previous chunk's arithmetic and TMEM load.
   __device__ __forceinline__ void tile(const Params& p, const GemmGeom& g,
                                        const Unit&, int n_blk, uint32_t taddr,
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+    const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
     GU nxt;
-    if (row_ok && n0 + 32 <= g.N) load_gu(p, n0, nxt);
+    if (row_ok && n0 < g.N) load_gu(p, n0, nxt);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int64_t j0 = n0 + c * 32;
       if (j0 >= g.N) break;
       const GU cur = nxt;
-      const bool full = j0 + 32 <= g.N;
-      if (row_ok && c + 1 < BN / 32 && j0 + 64 <= g.N) load_gu(p, j0 + 32, nxt);
+      if (row_ok && c + 1 < BN / 32 && j0 + 32 < g.N) load_gu(p, j0 + 32, nxt);
       float da[32];
       tmem_ld32(taddr + c * 32, da);
-      if (!row_ok) continue;
-      uint16_t* dgp = p.dgu + row * p.ld_dgu + j0;
-      uint16_t* dup = dgp + p.du_off;
-      if (full) {
+      if (wrow0 >= g.M) continue;  // warp-uniform: all of the warp's rows
+      // rows past M compute from unloaded g, u; their boxes' rows are
+      // dropped by the store map
+      uint32_t og[16], ou[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t gw[4] = {cur.g[q].x, cur.g[q].y, cur.g[q].z, cur.g[q].w};
-          const uint32_t uw[4] = {cur.u[q].x, cur.u[q].y, cur.u[q].z, cur.u[q].w};
-          uint32_t og[4], ou[4];
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t gw[4] = {cur.g[q].x, cur.g[q].y, cur.g[q].z, cur.g[q].w};
+        const uint32_t uw[4] = {cur.u[q].x, cur.u[q].y, cur.u[q].z, cur.u[q].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float dgv[2], duv[2];
+        for (int e = 0; e < 4; ++e) {
+          float dgv[2], duv[2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float gx = __uint_as_float(h ? (gw[e] & 0xFFFF0000u)
-                                                 : (gw[e] << 16));
-              const float ux = __uint_as_float(h ? (uw[e] & 0xFFFF0000u)
-                                                 : (uw[e] << 16));
-              const float sg = sigmoid_fast(gx);
-              const float d = da[8 * q + 2 * e + h];
-              duv[h] = d * gx * sg;
-              dgv[h] = d * ux * sg * (1.f + gx * (1.f - sg));
-            }
-            og[e] = pack_bf16x2(dgv[0], dgv[1]);
-            ou[e] = pack_bf16x2(duv[0], duv[1]);
+          for (int h = 0; h < 2; ++h) {
+            const float gx = __uint_as_float(h ? (gw[e] & 0xFFFF0000u)
+                                               : (gw[e] << 16));
+            const float ux = __uint_as_float(h ? (uw[e] & 0xFFFF0000u)
+                                               : (uw[e] << 16));
+            const float sg = sigmoid_fast(gx);
+            const float d = da[8 * q + 2 * e + h];
+            duv[h] = d * gx * sg;
+            dgv[h] = d * ux * sg * (1.f + gx * (1.f - sg));
           }
-          reinterpret_cast<uint4*>(dgp)[q] = make_uint4(og[0], og[1], og[2], og[3]);
-          reinterpret_cast<uint4*>(dup)[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-        }
-      } else {
-        const int nv = static_cast<int>(g.N - j0);
-        const uint16_t* gp = p.g + row * p.ld_gu + j0;
-        const uint16_t* up = p.u + row * p.ld_gu + j0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (i >= nv) continue;
-          const float gx = __uint_as_float(static_cast<uint32_t>(gp[i]) << 16);
-          const float ux = __uint_as_float(static_cast<uint32_t>(up[i]) << 16);
-          const float sg = sigmoid_fast(gx);
-          dup[i] = to_bf16_bits(da[i] * gx * sg);
-          dgp[i] = to_bf16_bits(da[i] * ux * sg * (1.f + gx * (1.f - sg)));
+          og[4 * q + e] = pack_bf16x2(dgv[0], dgv[1]);
+          ou[4 * q + e] = pack_bf16x2(duv[0], duv[1]);
         }
       }
+      store_box_words(og, j0, wrow0, &p.map_dgu);
+      store_box_words(ou, p.du_off + j0, wrow0, &p.map_dgu);
     }
   }
 
@@ -1087,7 +1065,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap ta,
            const __grid_constant__ CUtensorMap tb,
            const __grid_constant__ CUtensorMap tb2, const GemmGeom g,
-           const typename Epi::Params p, unsigned* err) {
+           const __grid_constant__ typename Epi::Params p, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms: 1 KB aligned
@@ -1480,7 +1458,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap ta,
                 const __grid_constant__ CUtensorMap tb,
                 const __grid_constant__ CUtensorMap tb2, const GemmGeom g,
-                const typename Epi::Params p, unsigned* err) {
+                const __grid_constant__ typename Epi::Params p,
+                unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;

@@ -132,23 +132,24 @@ struct FusedParams {
 
 // Gated-MLP gate/up contraction (B dual along N): accumulator columns
 // 0..127 hold g, 128..255 hold u for output columns [128 n, 128 n + 128);
-// writes a = silu(g) * u and, when the pointers are set, g and u (bf16).
+// writes a = silu(g) * u and, when asked, g and u (bf16), each through its
+// store map (32 x 32 boxes, as the logits epilogues' chunks). The maps
+// reach the kernel inside this block, a __grid_constant__ parameter.
 struct SwigluParams {
-  uint16_t* a;            // [M][ld]
-  uint16_t* g;            // [M][ld] or NULL
-  uint16_t* u;            // [M][ld] or NULL
-  int64_t ld;
+  CUtensorMap map_a;      // store map of a [M][I]
+  CUtensorMap map_g;      // of g [M][I] (used when save_gu)
+  CUtensorMap map_u;      // of u [M][I] (used when save_gu)
+  int save_gu;
 };
 
 // Gated-MLP backward: the accumulator is da = dy Wd; with the saved g, u
 // writes dg = da u silu'(g) at [row][col] and du = da silu(g) at
-// [row][du_off + col] (bf16).
+// [row][du_off + col] (bf16) through one store map of [dg | du].
 struct SwigluBwdParams {
+  CUtensorMap map_dgu;    // store map of dgu [M][2 I]
   const uint16_t* g;      // [M][ld_gu]
   const uint16_t* u;      // [M][ld_gu]
   int64_t ld_gu;
-  uint16_t* dgu;          // [M][ld_dgu]
-  int64_t ld_dgu;
   int64_t du_off;
 };
 
