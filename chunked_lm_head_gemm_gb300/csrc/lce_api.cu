@@ -232,29 +232,22 @@ lce_status tmap_store_box(CUtensorMap* tm, const void* base, int64_t cols,
                    CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// ---- the contractions' tile order and pacing -------------------------------
-enum ContractionKind {
-  T_LSE = 0, T_GRAD, T_FUSED, T_DH, T_DW, T_TEST, T_MLP, T_MLP_GU
-};
-
+// ---- the contractions' tile order --------------------------------------------
 // The vocabulary sweeps (forward logits and their recompute) take enough
 // column-tile runs per row block that at most this many bytes of A row
 // panels are live at once; they stay in L2 while every CTA sweeps W.
 constexpr double kL2PanelBudget = 48e6;
 
-// dH and dW walk their output tiles in groups of kGroupN column tiles, the
-// row blocks varying inside a group, so a wave of 76 pair tiles spans about
-// 9.5 row blocks x 8 column panels instead of 4.75 x 16 and reads fewer
-// distinct operand panels from DRAM. On the 8B shard this cut each launch's
-// DRAM reads from 30.3 to 25.5 GB (dH) and from 32.2 to 27.3 GB (dW), and
-// the step by 0.5%. The tile order changes no result: every tile is
+// Every other contraction (one output tile per work unit) walks its tiles
+// in groups of kGroupN column tiles, the row blocks varying inside a group,
+// so a wave of 76 pair tiles spans about 9.5 row blocks x 8 column panels
+// instead of the row-major order's 76 / num_n row blocks x num_n columns,
+// and reads fewer distinct operand panels from DRAM. On the 8B shard this
+// cut each launch's DRAM reads from 30.3 to 25.5 GB (dH) and from 32.2 to
+// 27.3 GB (dW); on the gated MLP's contractions, with pacing, from ~95 to
+// ~31 GB per row chunk. The tile order changes no result: every tile is
 // computed by the same arithmetic wherever it sits in the order.
 constexpr int kGroupN = 8;
-
-// Wave pacing applies to every contraction but the gated MLP's, which
-// measured the same or slower paced: the gate/up contraction (its heavy
-// epilogue) and da lose more to the waits than dx, dWd and dWgu gain.
-bool paced_kind(int kind) { return kind != T_MLP && kind != T_MLP_GU; }
 
 // Wave pacing of the contractions (GemmGeom::wave_ctr): on unless
 // LCE_WAVE_SYNC=0 or lce_set_wave_sync(0).
@@ -337,7 +330,6 @@ struct GemmOperands {
   const void* b;
   int64_t b_ld;
   bool sweep;          // sweep all column tiles per row block (choose splits)
-  int kind;            // ContractionKind
   // B from two maps (GemmGeom::b_dual): 1 = along N (b2 has b's shape;
   // tiles of 128 output columns), 2 = along K (b covers k < k_split, b2
   // the rest; both have b's row stride)
@@ -348,7 +340,6 @@ struct GemmOperands {
 
 struct GemmPlan {
   bool pair;
-  int kind;  // ContractionKind
   GemmGeom g;
   CUtensorMap ta, tb, tb2;
   int grid;
@@ -357,7 +348,6 @@ struct GemmPlan {
 lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
                      GemmPlan* pl) {
   pl->pair = use_pair() && dev.pair_slots > 0;
-  pl->kind = o.kind;
   const int rows_unit = pl->pair ? 2 * BM : BM;
   const int slots = pl->pair ? dev.pair_slots : dev.num_sms;
   const int num_m = static_cast<int>(ceil_div(o.M, rows_unit));
@@ -367,7 +357,7 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
   if (o.sweep) choose_splits(num_m, num_n, slots, o.K, &splits, &tps, rows_unit);
   pl->g = make_geom(o.M, o.N, o.K, splits, tps, rows_unit);
   pl->g.num_n = num_n;
-  if (!o.sweep && (o.kind == T_DH || o.kind == T_DW)) pl->g.group_n = kGroupN;
+  if (!o.sweep) pl->g.group_n = kGroupN;
   pl->g.b_dual = o.b_dual;
   pl->g.k_split_kb = o.b_dual == 2 ? static_cast<int>(o.k_split / BK) : 0;
   lce_status st = o.a_mn ? tmap_mnmajor(&pl->ta, o.a, o.M, o.K, o.a_ld)
@@ -395,7 +385,7 @@ lce_status plan_gemm(const GemmOperands& o, const DeviceInfo& dev,
 // Turn on wave pacing for one launch: the counter is zeroed on the stream
 // first. A wait runs out after ~two tiles' worth of MMA time at full rate.
 cudaError_t pace(GemmPlan* pl, void* ctr, cudaStream_t s) {
-  if (!wave_sync_on() || !ctr || !paced_kind(pl->kind)) return cudaSuccess;
+  if (!wave_sync_on() || !ctr) return cudaSuccess;
   const GemmGeom& g = pl->g;
   const int slots = pl->pair ? pl->grid / 2 : pl->grid;
   // the most output tiles any CTA (cluster) walks, as the kernels assign
@@ -725,7 +715,7 @@ lce_status lce_forward_ex(const void* h, const void* W, lce_dtype dt,
 
   // logits = h W^T: M = L rows, N = V columns, K = H
   GemmPlan pl;
-  if ((st = plan_gemm({L, V, H, false, false, hb, H, Wb, H, true, T_LSE}, *dev,
+  if ((st = plan_gemm({L, V, H, false, false, hb, H, Wb, H, true}, *dev,
                       &pl)) != LCE_OK)
     return st;
   const GemmGeom& g = pl.g;
@@ -819,7 +809,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
     // (1) recompute z_c = h_c W^T and write G_c = softmax - onehot (bf16)
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true, T_GRAD},
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true},
                           *dev, &pl)) != LCE_OK)
         return st;
       GradParams p{};
@@ -843,7 +833,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
     // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false, T_DH},
+      if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -863,7 +853,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
     // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
     {
       GemmPlan pl;
-      if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false, T_DW},
+      if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -964,7 +954,7 @@ lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
   }
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
   GemmPlan pl;
-  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true, T_LSE},
+  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true},
                       *dev, &pl)) != LCE_OK)
     return st;
   LseParams p{};
@@ -1037,7 +1027,7 @@ lce_status lce_forward_slice_exp(const void* h, const void* W, lce_dtype dt,
   if (e != cudaSuccess) return cuda_fail(e, "count_valid");
   // every row's logits once: statistics + tile exponentials kept in ws
   GemmPlan pl;
-  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true, T_FUSED},
+  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true},
                       *dev, &pl)) != LCE_OK)
     return st;
   uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
@@ -1124,7 +1114,7 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
   // dH_part = (dloss/N) G W_s: M = L, N = H, K = Vs
   {
     GemmPlan pl;
-    if ((st = plan_gemm({L, H, Vs, false, true, E, w.ldg, Wb, H, false, T_DH},
+    if ((st = plan_gemm({L, H, Vs, false, true, E, w.ldg, Wb, H, false},
                         *dev, &pl)) != LCE_OK)
       return st;
     StoreParams p{};
@@ -1144,7 +1134,7 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
   // dW_s = (dloss/N) G^T h: M = Vs, N = H, K = L, written once
   {
     GemmPlan pl;
-    if ((st = plan_gemm({Vs, H, L, true, true, E, w.ldg, hb, H, false, T_DW},
+    if ((st = plan_gemm({Vs, H, L, true, true, E, w.ldg, hb, H, false},
                         *dev, &pl)) != LCE_OK)
       return st;
     StoreParams p{};
@@ -1287,7 +1277,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
     int splits = 1;
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true, T_FUSED},
+      if ((st = plan_gemm({cr, V, H, false, false, hc, H, Wb, H, true},
                           *dev, &pl)) != LCE_OK)
         return st;
       splits = pl.g.splits;
@@ -1333,7 +1323,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
     // (4) dH_c = G_c W / N
     {
       GemmPlan pl;
-      if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false, T_DH},
+      if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -1353,7 +1343,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
     // (5) dW (+)= G_c^T h_c / N
     {
       GemmPlan pl;
-      if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false, T_DW},
+      if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false},
                           *dev, &pl)) != LCE_OK)
         return st;
       StoreParams p{};
@@ -1517,7 +1507,7 @@ lce_status mlp_gate_up(const DeviceInfo& dev, const uint16_t* xc, int64_t cr,
                        const void* Wg, const void* Wu, int64_t H, int64_t I,
                        uint16_t* a, uint16_t* g, uint16_t* u, void* ctr,
                        cudaStream_t s) {
-  GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false, T_MLP_GU};
+  GemmOperands o{cr, I, H, false, false, xc, H, Wg, H, false};
   o.b_dual = 1;
   o.b2 = Wu;
   GemmPlan pl;
@@ -1601,9 +1591,8 @@ lce_status lce_mlp_forward(const void* x, const void* Wg, const void* Wu,
     p.out = static_cast<uint16_t*>(y) + c0 * H;
     p.ldo = H;
     p.out_f32 = 0;
-    if ((st = mlp_store(*dev, {cr, H, I, false, false, A, I, Wd, I, false,
-                               T_MLP},
-                        p, LCE_K_MLP_DOWN,wsb + w.sync, s)) != LCE_OK)
+    if ((st = mlp_store(*dev, {cr, H, I, false, false, A, I, Wd, I, false},
+                        p, LCE_K_MLP_DOWN, wsb + w.sync, s)) != LCE_OK)
       return st;
   }
   return LCE_OK;
@@ -1641,7 +1630,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       return st;
     // (2) da_c = dy_c Wd -> dg_c, du_c into [dg | du]
     {
-      GemmOperands o{cr, I, H, false, true, dyc, H, Wd, I, false, T_MLP};
+      GemmOperands o{cr, I, H, false, true, dyc, H, Wd, I, false};
       GemmPlan pl;
       if ((st = plan_gemm(o, *dev, &pl)) != LCE_OK) return st;
       SwigluBwdParams p{};
@@ -1661,8 +1650,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
     }
     // (3) dx_c = [dg | du] [Wg ; Wu]  (K = 2I, B from two maps along K)
     {
-      GemmOperands o{cr, H, 2 * I, false, true, DGU, 2 * I, Wg, H, false,
-                     T_MLP};
+      GemmOperands o{cr, H, 2 * I, false, true, DGU, 2 * I, Wg, H, false};
       o.b_dual = 2;
       o.b2 = Wu;
       o.k_split = I;
@@ -1680,9 +1668,8 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       p.ldo = I;
       p.out_f32 = 1;
       p.accumulate = c0 > 0;
-      if ((st = mlp_store(*dev, {H, I, cr, true, true, dyc, H, A, I, false,
-                                 T_MLP},
-                          p, LCE_K_MLP_DWD,wsb + w.sync, s)) != LCE_OK)
+      if ((st = mlp_store(*dev, {H, I, cr, true, true, dyc, H, A, I, false},
+                          p, LCE_K_MLP_DWD, wsb + w.sync, s)) != LCE_OK)
         return st;
     }
     // (5) [dWg ; dWu] (+)= [dg | du]^T x_c, rows >= I going to dWu
@@ -1695,8 +1682,8 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       p.out_f32 = 1;
       p.accumulate = c0 > 0;
       if ((st = mlp_store(*dev, {2 * I, H, cr, true, true, DGU, 2 * I, xc, H,
-                                 false, T_MLP},
-                          p, LCE_K_MLP_DWGU,wsb + w.sync, s)) != LCE_OK)
+                                 false},
+                          p, LCE_K_MLP_DWGU, wsb + w.sync, s)) != LCE_OK)
         return st;
     }
   }
@@ -1754,7 +1741,7 @@ lce_status lce_test_gemm(const void* A, const void* B, float* D, int64_t M,
   if (st != LCE_OK) return st;
   GemmPlan pl;
   if ((st = plan_gemm({M, N, K, a_mn != 0, b_mn != 0, A, a_mn ? M : K, B,
-                       b_mn ? N : K, false, T_TEST},
+                       b_mn ? N : K, false},
                       *dev, &pl)) != LCE_OK)
     return st;
   StoreParams p{};

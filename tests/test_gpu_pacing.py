@@ -40,3 +40,28 @@ def test_pacing_does_not_change_results(mode, pair):
     assert lce.get_error() == 0
     for a, b in zip(on, off):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
+def test_pacing_does_not_change_mlp_results(pair):
+    """The gated MLP's contractions are paced too (with every other
+    contraction, their tiles grouped by 8 columns): on and off give the same
+    bits, on a case with several row chunks and many tiles per launch."""
+    dev = require_gpu()
+    from chunked_lm_head_gemm_gb300.inputs import MLP_WORKLOADS, make_mlp_inputs
+    wl = MLP_WORKLOADS["qwen3-0.6b-mlp"].with_rows(2560)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=6, device=dev)
+    before = B.get_wave_sync()
+    out = {}
+    try:
+        with cta_pair(pair):
+            for on in (True, False):
+                B.set_wave_sync(on)
+                y = lce.mlp_forward(x, Wg, Wu, Wd, chunk_rows=1024)
+                out[on] = (y,) + lce.mlp_backward(x, Wg, Wu, Wd, dy,
+                                                  chunk_rows=1024)
+    finally:
+        B.set_wave_sync(before)
+    assert lce.get_error() == 0
+    for a, b in zip(out[True], out[False]):
+        assert torch.equal(a, b)
