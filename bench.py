@@ -211,9 +211,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def _oracle_rate_macs(h, W, y) -> float:
-    """Multiply-adds per second of the oracle forward on a few rows."""
+    """Multiply-adds per second of the oracle forward on one row per host
+    thread (the oracle runs one thread per row, so fewer rows than threads
+    would time only part of the cores)."""
     import oracle
-    n = min(4, h.shape[0])
+    n = min(oracle.default_threads(), h.shape[0])
     t0 = time.perf_counter()
     oracle.forward(h[:n], W, y[:n])
     dt = time.perf_counter() - t0
@@ -265,7 +267,7 @@ def cpu_baseline(wl, h_cpu, W_cpu, y_cpu, target_s: float = 20.0) -> dict:
 def run_reference(args, wl) -> dict:
     import oracle
     oracle.build()
-    probe_rows = 4
+    probe_rows = min(wl.L, oracle.default_threads())
     h, W, y = cpu_inputs(wl, probe_rows)
     rate = _oracle_rate_macs(h, W, y)
     # bounded sample per step: the whole --warmup + --steps run ~2 minutes
