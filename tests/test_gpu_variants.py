@@ -133,3 +133,73 @@ def test_variant_autograd(mode):
                        torch.from_numpy(gpu["dH"]).float())
     fb = _oracle("multi_tile", 0.2, 1e-3, h, W, y, None)
     assert rel_fro(WW.grad.double().cpu().numpy(), fb["dW"]) < 1e-2
+
+
+def test_variants_full_size_sampled_rows():
+    """The 8B shard at full size with label smoothing and the z-loss, in the
+    launch configuration the benchmark times (fused path, default chunk):
+    lse and dH on sampled rows (first, last, an ignored one, random)
+    against the oracle's rows of the whole problem (its N over all
+    labels); the recomputing path within the bound of the fused one."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    from tests.gpu_util import GRAD_RFRO, LSE_ATOL, to64
+    wl = WORKLOADS["qwen3-8b"]
+    h, W, y = make_inputs(wl, seed=0, device=dev)
+    kw = dict(label_smoothing=0.1, z_loss=1e-4)
+    ws = lce.alloc_workspace(wl.L, wl.H, wl.V, h.dtype, 0, dev)
+    loss, lse, dH, dW = lce.forward_backward(h, W, y, workspace=ws, **kw)
+    assert lce.get_error() == 0
+    rs = np.random.default_rng(17)
+    rows = np.unique(np.concatenate([[0, wl.L - 1],
+                                     rs.integers(0, wl.L, 10)]))
+    r = oracle.rows(h.cpu(), W.cpu(), y.cpu(), rows, dloss=1.0, **kw)
+    idx = torch.from_numpy(rows).to(dev)
+    assert np.max(np.abs(to64(lse)[rows] - r["lse"])) <= LSE_ATOL
+    e = rel_fro(to64(dH[idx]), r["dH"])
+    assert e <= GRAD_RFRO, f"sampled dH rows rel Frobenius err {e}"
+    # the loss is plausible: the plain loss plus a positive z-loss term,
+    # minus at most eps times the spread of the logits
+    plain, _ = lce.forward(h, W, y, workspace=ws)
+    zl = kw["z_loss"] * (lse.double()[y >= 0] ** 2).mean().item()
+    assert abs(loss.item() - (plain.item() + zl)) < 0.1 * plain.item()
+    # the recomputing path agrees with the fused one
+    one = torch.ones((), device=dev)
+    loss2, lse2 = lce.forward(h, W, y, workspace=ws, **kw)
+    dH2, dW2 = lce.backward(h, W, y, lse2, one, workspace=ws, **kw)
+    assert lce.get_error() == 0
+    assert abs(loss2.item() - loss.item()) <= 1e-5 * abs(loss.item())
+    assert rel_fro(to64(dH2), to64(dH)) <= GRAD_RFRO
+    assert rel_fro(to64(dW2), to64(dW)) <= GRAD_RFRO
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_variant_edge_cases(mode):
+    """Loss variants on the degenerate cases: every row ignored (loss 0,
+    gradients 0), one class (smoothing changes nothing, the z-loss
+    remains), labels out of range (reported and ignored)."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300._binding as B
+    kw = dict(label_smoothing=0.3, z_loss=0.02)
+    wl = Workload("vallign", 150, 32, 400, "bf16", 1.0, 0.1, "uniform")
+    h, W, y = make_inputs(wl, seed=3, device=dev)
+    y[:] = -100
+    gpu = run_gpu(h, W, y, mode=mode, **kw)
+    assert gpu["status"] == 0 and gpu["loss"] == 0.0
+    assert np.all(gpu["dH"] == 0.0) and np.all(gpu["dW"] == 0.0)
+    for name, L, H, V, seed in (("v1", 70, 16, 1, 2), ("vbad", 260, 32, 500, 4)):
+        wl = Workload(name, L, H, V, "bf16", 1.0, 0.5 if V == 1 else 0.1,
+                      "uniform", ignore_frac=0.1)
+        h, W, y = make_inputs(wl, seed=seed, device=dev)
+        if name == "vbad":
+            y[3] = 500
+            y[77] = -7
+        gpu = run_gpu(h, W, y, dloss=0.8, mode=mode, **kw)
+        fb = oracle.forward_backward(h.cpu(), W.cpu(), y.cpu(), dloss=0.8,
+                                     **kw)
+        if name == "vbad":
+            assert gpu["status"] == B.LCE_ERR_LABEL_RANGE
+            assert fb["status"] == oracle.LABEL_RANGE
+        else:
+            assert gpu["status"] == 0
+        assert_parity(gpu, fb, fb)
