@@ -28,6 +28,9 @@ sample per step) and prints the same line with "impl": "reference".
 lce_mlp_backward) on a Qwen3 MLP shape instead (--config qwen3-8b-mlp ...).
 --gpus N under torchrun: N independent replicas, one per GPU (the library
 has no multi-GPU path), weak scaling, max time over ranks.
+Measurement modes that print their own JSON line instead of the benchmark:
+--layout-sweep M,N,K (the contraction in its four operand layouts) and
+--forward-static (lce_forward_static against lce_forward).
 """
 from __future__ import annotations
 

@@ -591,8 +591,8 @@ lce_status operands(const void* h, const void* W, lce_dtype dt, int64_t L,
   return LCE_OK;
 }
 
-// The loss variant of an optional lce_loss_opts: eps in [0, 1], zcoef >= 0,
-// both finite; NULL is the plain loss.
+// The loss variant of an optional lce_loss_opts: eps in [0, 1], zcoef >= 0
+// with 2 zcoef finite (the gradient's factor); NULL is the plain loss.
 struct Variant {
   float eps = 0.f, zcoef = 0.f;
   bool smooth() const { return eps != 0.f; }
@@ -609,7 +609,7 @@ bool read_variant(const lce_loss_opts* o, Variant* v) {
   *v = Variant{};
   if (!o) return true;
   if (!(o->label_smoothing >= 0.f && o->label_smoothing <= 1.f)) return false;
-  if (!(o->z_loss >= 0.f && o->z_loss <= 3.0e38f)) return false;
+  if (!(o->z_loss >= 0.f) || !std::isfinite(2.f * o->z_loss)) return false;
   v->eps = o->label_smoothing;
   v->zcoef = o->z_loss;
   return true;

@@ -173,7 +173,7 @@ lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
  *   G_ij   = dloss/N ((1 + 2 z_loss lse_i) softmax_ij - q_j)
  * Ignored rows add nothing, as in the plain loss. Fields:
  *   label_smoothing  in [0, 1]; 0 = the one-hot target
- *   z_loss           >= 0 and finite; 0 = no z-loss
+ *   z_loss           >= 0, with 2 * z_loss finite in float; 0 = no z-loss
  * Other values return LCE_ERR_INVALID_ARG before anything is queued.
  * A NULL pointer or {0, 0} is the plain loss, computed with exactly the
  * arithmetic of the calls without options (the same bits). Label smoothing
