@@ -261,6 +261,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane (32x32b.x64), as
+// tmem_ld32: one load for twice the columns, so an epilogue that walks a
+// tile waits for half as many loads.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -446,31 +462,31 @@ struct EpiLse : EpiBase {
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int64_t j0 = n0 + c * 32;
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t j0 = n0 + c * 64;
       if (j0 >= g.N) break;  // same for the whole warp
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+      float v[64];
+      tmem_ld64(taddr + c * 64, v);
       const int64_t rem = g.N - j0;
-      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int nv = rem < 64 ? static_cast<int>(rem) : 64;
       const int yo = yv - static_cast<int>(j0);
-      if (static_cast<unsigned>(yo) < 32u) {
+      if (static_cast<unsigned>(yo) < 64u) {
         float zyv = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i == yo) zyv = v[i];
         p.zy[row] = zyv;
       }
       if (p.part_z != nullptr) {  // warp-uniform
         float za[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i < nv) za[i & 3] += v[i];
         zs += (za[0] + za[1]) + (za[2] + za[3]);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         v[i] = (i < nv) ? v[i] * LOG2E : -INFINITY;
         mx[i & 3] = fmaxf(mx[i & 3], v[i]);
       }
@@ -478,7 +494,7 @@ struct EpiLse : EpiBase {
       const float mn = fmaxf(m2, cmax);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i & 3] += ex2(v[i] - mn);
+      for (int i = 0; i < 64; ++i) acc[i & 3] += ex2(v[i] - mn);
       s = s * ex2(m2 - mn) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       m2 = mn;
     }
@@ -532,24 +548,35 @@ struct EpiGrad : EpiBase {
                                        const Unit&, int n_blk, uint32_t taddr,
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+    // rows past M and columns past N hold junk that the store drops
+    const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int64_t j0 = n0 + c * 32;
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t j0 = n0 + c * 64;
       if (j0 >= g.N) break;
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+      float v[64];
+      tmem_ld64(taddr + c * 64, v);
       const int yo = yv - static_cast<int>(j0);
+      uint32_t w0[16], w1[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float gi = takes ? fmaf(ex2(fmaf(v[i], LOG2E, -lse2)), zf,
-                                -p.var.eps_v)
-                         : 0.f;
-        if (i == yo) gi -= p.var.ome;
-        v[i] = gi;
+      for (int i = 0; i < 64; i += 2) {
+        float gi[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          gi[k] = takes ? fmaf(ex2(fmaf(v[i + k], LOG2E, -lse2)), zf,
+                               -p.var.eps_v)
+                        : 0.f;
+          if (i + k == yo) gi[k] -= p.var.ome;
+        }
+        if (i < 32)
+          w0[i / 2] = pack_bf16x2(gi[0], gi[1]);
+        else
+          w1[(i - 32) / 2] = pack_bf16x2(gi[0], gi[1]);
       }
-      // rows past M and columns past N hold junk that the store drops
-      const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
-      if (wrow0 < g.M) store_box(v, j0, wrow0);  // warp-uniform test
+      if (wrow0 < g.M) {  // warp-uniform test
+        store_box_words(w0, j0, wrow0, nullptr);
+        if (j0 + 32 < g.N) store_box_words(w1, j0 + 32, wrow0, nullptr);
+      }
     }
   }
 
@@ -590,57 +617,67 @@ struct EpiFused : EpiBase {
                                        const Unit&, int n_blk, uint32_t taddr,
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
-    // pass 1: tile maximum, label logit
+    // pass 1: tile maximum, label logit (64 columns per TMEM load)
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int64_t j0 = n0 + c * 32;
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t j0 = n0 + c * 64;
       if (j0 >= g.N) break;
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+      float v[64];
+      tmem_ld64(taddr + c * 64, v);
       const int64_t rem = g.N - j0;
-      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int nv = rem < 64 ? static_cast<int>(rem) : 64;
       const int yo = yv - static_cast<int>(j0);
-      if (static_cast<unsigned>(yo) < 32u) {
+      if (static_cast<unsigned>(yo) < 64u) {
         float zyv = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i == yo) zyv = v[i];
         if (row_ok) p.zy[row] = zyv;
       }
       if (p.part_z != nullptr) {  // warp-uniform
         float za[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i < nv) za[i & 3] += v[i];
         zs += (za[0] + za[1]) + (za[2] + za[3]);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
+      for (int i = 0; i < 64; ++i)
         if (i < nv) mx[i & 3] = fmaxf(mx[i & 3], v[i] * LOG2E);
     }
     const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     // pass 2: exponentials relative to the tile maximum. Each 32-column
-    // chunk of the warp's 32 rows goes through a shared-memory box (row r
-    // at r * 64 bytes, its 16-byte pieces in 64-byte-swizzle order) and out
-    // by one TMA store, which writes whole rows' segments and drops the
-    // rows past M and the columns past N.
+    // half of a 64-column load, for the warp's 32 rows, goes through a
+    // shared-memory box (row r at r * 64 bytes, its 16-byte pieces in
+    // 64-byte-swizzle order) and out by one TMA store, which writes whole
+    // rows' segments and drops the rows past M and the columns past N.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int64_t j0 = n0 + c * 32;
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t j0 = n0 + c * 64;
       if (j0 >= g.N) break;
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+      float v[64];
+      tmem_ld64(taddr + c * 64, v);
       const int64_t rem = g.N - j0;
-      const int nv = rem < 32 ? static_cast<int>(rem) : 32;
+      const int nv = rem < 64 ? static_cast<int>(rem) : 64;
+      uint32_t w0[16], w1[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
-        acc[i & 3] += v[i];
+      for (int i = 0; i < 64; i += 2) {
+        const float e0 = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
+        const float e1 = (i + 1 < nv) ? ex2(fmaf(v[i + 1], LOG2E, -mt)) : 0.f;
+        acc[i & 3] += e0;
+        acc[(i + 1) & 3] += e1;
+        if (i < 32)
+          w0[i / 2] = pack_bf16x2(e0, e1);
+        else
+          w1[(i - 32) / 2] = pack_bf16x2(e0, e1);
       }
-      if (wrow0 < g.M) store_box(v, j0, wrow0);  // warp-uniform test
+      if (wrow0 < g.M) {  // warp-uniform test
+        store_box_words(w0, j0, wrow0, nullptr);
+        if (j0 + 32 < g.N) store_box_words(w1, j0 + 32, wrow0, nullptr);
+      }
     }
     const float st = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     const float mn = fmaxf(m2, mt);
