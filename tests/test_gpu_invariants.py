@@ -10,9 +10,9 @@ chunk it"). Hence:
     dH nor dW (the rows of softmax - onehot sum to zero);
   - permuting the rows permutes lse and dH and leaves the loss and dW
     unchanged;
-  - the rows can be cut into chunks at will: at the full 8B shard length
-    and its default chunk of 24320 rows, dW (accumulated over six chunks)
-    equals the oracle's on every vocabulary row.
+  - the rows can be cut into chunks at will: at every head shape's full
+    length and default chunk, dW (accumulated over all chunks) equals the
+    oracle's on every row of a reduced vocabulary.
 """
 import dataclasses
 
@@ -98,19 +98,28 @@ def test_row_permutation_full_head(mode):
     assert e <= bound, f"dW changed by {e}"
 
 
-def test_full_length_dW_against_oracle():
-    """Every row of the 8B shard (L = 131072, H = 4096, last row ignored)
-    against a reduced vocabulary of 520 ids (two full 256-column tiles and
-    a ragged one), backward in the 8B shard's default 24320-row chunks (five
-    chunks and a 9472-row tail): dW on every vocabulary row, accumulated
-    over six chunks, against the float64 oracle; also the loss, every lse
-    and 64 sampled dH rows. Both paths, default contraction variant."""
+# (head shape, its default backward chunk at the full vocabulary)
+FULL_LENGTH = [("qwen3-0.6b", 24320), ("qwen3-4b", 19456),
+               ("qwen3-8b", 24320), ("qwen3-32b", 19456)]
+
+
+@pytest.mark.parametrize("name,chunk", FULL_LENGTH,
+                         ids=[f[0] for f in FULL_LENGTH])
+def test_full_length_dW_against_oracle(name, chunk):
+    """Every row of a head shape's workload (full L and H, its label
+    recipe: uniform, Zipf at 4B where the most frequent id takes ~18% of
+    the rows, x20 stress rows at 32B) against a reduced vocabulary of 520
+    ids (two full 256-column tiles and a ragged one), backward in the
+    shape's default row chunks at the full vocabulary (the chunking the
+    benchmark runs): dW on every vocabulary row, accumulated over every
+    chunk, against the float64 oracle; also the loss, every lse and 64
+    sampled dH rows. Both paths, default contraction variant."""
     dev = require_gpu()
     import chunked_lm_head_gemm_gb300 as lce
-    wl = dataclasses.replace(WORKLOADS["qwen3-8b"], V=520, name="8b-v520")
+    wl = dataclasses.replace(WORKLOADS[name], V=520, name=f"{name}-v520")
     h, W, y = make_inputs(wl, seed=0, device=dev)
-    chunk = 24320
     L, H, V = wl.L, wl.H, wl.V
+    assert L > chunk  # several chunks
     ws = lce.alloc_workspace(L, H, V, h.dtype, chunk, dev)
     ref = oracle.forward_backward(h.cpu(), W.cpu(), y.cpu(), dloss=1.0,
                                   want_dH=False)
