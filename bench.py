@@ -430,6 +430,12 @@ def main():
                     help="override V (a reduced vocabulary, for profiling "
                          "one contraction on a small device footprint)")
     ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--label-smoothing", type=float, default=0.0,
+                    help="time the loss variant with this label smoothing "
+                         "(lce_*_ex calls; 0 = the plain loss)")
+    ap.add_argument("--z-loss", type=float, default=0.0,
+                    help="time the loss variant with this z-loss "
+                         "coefficient (0 = none)")
     ap.add_argument("--mode", default="fused", choices=["separate", "fused"])
     ap.add_argument("--only-mode", action="store_true",
                     help="time only --mode (profiling runs)")
@@ -509,15 +515,18 @@ def main():
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     dloss = torch.ones(1, dtype=torch.float32, device=dev)
 
+    variant = dict(label_smoothing=args.label_smoothing, z_loss=args.z_loss)
+
     def step_separate():
-        lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
+        lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse,
+                    **variant)
         lce.backward(h, W, y, lse, dloss, chunk_rows=chunk, workspace=ws,
-                     dH_out=dH, dW_out=dW)
+                     dH_out=dH, dW_out=dW, **variant)
 
     def step_fused():
         lce.forward_backward(h, W, y, chunk_rows=chunk, workspace=ws,
                              loss_out=loss, lse_out=lse, dH_out=dH,
-                             dW_out=dW)
+                             dW_out=dW, **variant)
         lce.scale_gradients(dH, dW, dloss)
 
     steps = {"separate": step_separate, "fused": step_fused}
@@ -585,11 +594,12 @@ def main():
         # the separate path's two calls on their own: forward (logits pass,
         # loss) and backward (recompute, dH, dW) from the forward's lse
         def step_fwd():
-            lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse)
+            lce.forward(h, W, y, workspace=ws, loss_out=loss, lse_out=lse,
+                        **variant)
 
         def step_bwd():
             lce.backward(h, W, y, lse, dloss, chunk_rows=chunk, workspace=ws,
-                         dH_out=dH, dW_out=dW)
+                         dH_out=dH, dW_out=dW, **variant)
         for name, fn in (("forward", step_fwd), ("backward", step_bwd)):
             ms, _, _ = timed(fn, False)
             phases[name] = {"ms": ms / args.steps,
@@ -780,6 +790,9 @@ def main():
             "config": {"workload": wl.name, "L": L, "H": H, "V": V,
                        "inputs": wl.dtype, "chunk_rows": chunk,
                        "mode": args.mode,
+                       **({"label_smoothing": args.label_smoothing,
+                           "z_loss": args.z_loss}
+                          if args.label_smoothing or args.z_loss else {}),
                        "cta_pair": B.get_cta_pair(),
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": ("inputs larger than L2, no flush" if flush is None
