@@ -54,7 +54,8 @@ def test_mlp_against_oracle(name, L, H, I, chunk, xs, ws, pair):
 
 
 @pytest.mark.parametrize("pair", PAIRS, ids=lambda v: "pair" if v else "cta")
-@pytest.mark.parametrize("name", ["qwen3-4b-mlp", "qwen3-8b-mlp"])
+@pytest.mark.parametrize("name", ["qwen3-0.6b-mlp", "qwen3-4b-mlp",
+                                  "qwen3-8b-mlp", "qwen3-32b-mlp"])
 def test_mlp_row_slice_of_qwen3_shape(name, pair):
     """256 rows at the Qwen3 MLP widths (H, I), the oracle on all of it."""
     dev = require_gpu()
@@ -62,6 +63,19 @@ def test_mlp_row_slice_of_qwen3_shape(name, pair):
     x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=0, device=dev)
     with cta_pair(pair):
         gpu = _run(x, Wg, Wu, Wd, dy, 0)
+    ref = oracle.mlp(x.cpu(), Wg.cpu(), Wu.cpu(), Wd.cpu(), dy.cpu())
+    _compare(gpu, ref)
+
+
+def test_mlp_multichunk_slice_of_qwen3_8b():
+    """1024 rows at the Qwen3-8B MLP widths in 256-row chunks: the weight
+    gradients' fp32 read-add-write runs three times at full H and I, the
+    intermediates are recomputed per chunk; all five outputs against the
+    oracle."""
+    dev = require_gpu()
+    wl = MLP_WORKLOADS["qwen3-8b-mlp"].with_rows(1024)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=2, device=dev)
+    gpu = _run(x, Wg, Wu, Wd, dy, 256)
     ref = oracle.mlp(x.cpu(), Wg.cpu(), Wu.cpu(), Wd.cpu(), dy.cpu())
     _compare(gpu, ref)
 
