@@ -43,7 +43,9 @@ EXPORTED = ("lce_workspace_size", "lce_default_chunk_rows", "lce_forward",
             "lce_get_wave_sync", "lce_slice_exp_workspace_size",
             "lce_forward_slice_exp", "lce_backward_slice_exp",
             "lce_forward_ex", "lce_backward_ex", "lce_forward_backward_ex",
-            "lce_shard_sums", "lce_combine_shards")
+            "lce_shard_sums", "lce_combine_shards", "lce_forward_slice_ex",
+            "lce_combine_slices_ex", "lce_backward_slice_ex",
+            "lce_forward_slice_exp_ex", "lce_backward_slice_exp_ex")
 
 KERNEL_KINDS = 22
 
@@ -153,6 +155,25 @@ def load(build_if_missing: bool = False):
                                                i64, i64, i64, p, p, p, p, sz,
                                                p]
         lib.lce_backward_slice_exp.restype = i32
+        lib.lce_forward_slice_ex.argtypes = [p, p, i32, p, i64, i64, i64,
+                                             i64, i64, i64, opts, p, p, p, p,
+                                             p, sz, p]
+        lib.lce_forward_slice_ex.restype = i32
+        lib.lce_combine_slices_ex.argtypes = [p, p, p, p, i64, p, i64, i64,
+                                              i64, opts, p, p, p, sz, p]
+        lib.lce_combine_slices_ex.restype = i32
+        lib.lce_backward_slice_ex.argtypes = [p, p, i32, p, p, i64, i64, i64,
+                                              i64, i64, i64, opts, p, i64, p,
+                                              p, p, sz, p]
+        lib.lce_backward_slice_ex.restype = i32
+        lib.lce_forward_slice_exp_ex.argtypes = [p, p, i32, p, i64, i64, i64,
+                                                 i64, i64, i64, opts, p, p, p,
+                                                 p, p, sz, p]
+        lib.lce_forward_slice_exp_ex.restype = i32
+        lib.lce_backward_slice_exp_ex.argtypes = [p, p, i32, p, p, i64, i64,
+                                                  i64, i64, i64, i64, opts, p,
+                                                  p, p, p, sz, p]
+        lib.lce_backward_slice_exp_ex.restype = i32
         lib.lce_mlp_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.lce_mlp_workspace_size.restype = sz
         lib.lce_mlp_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p,
@@ -416,13 +437,27 @@ def combine_shards(sums: torch.Tensor, n_local: torch.Tensor,
     return loss, weight
 
 
+def _slice_out(out, L, label_smoothing, dev):
+    """Rows m, s, zy (and zsum under label smoothing) of a [3 or 4, L]
+    float32 tensor."""
+    rows = 4 if label_smoothing != 0.0 else 3
+    if out is None:
+        out = torch.empty(rows, L, dtype=torch.float32, device=dev)
+    if out.dtype != torch.float32 or out.shape != (rows, L):
+        raise ValueError(f"out must be float32 [{rows}, {L}]")
+    return out, tuple(out[r] for r in range(rows))
+
+
 def forward_slice(h: torch.Tensor, W_slice: torch.Tensor,
                   labels: torch.Tensor, v0: int, V_total: int,
                   ignore_index: int = IGNORE_INDEX, workspace=None,
-                  out=None):
+                  out=None, label_smoothing: float = 0.0,
+                  z_loss: float = 0.0):
     """One vocabulary slice (W_slice = rows v0 .. v0 + Vs - 1 of the head):
     returns (m, s, zy), each float32 [L]: the slice's per-row max logit, sum
-    of exp(z - m), and label logit (0 where the label is elsewhere)."""
+    of exp(z - m), and label logit (0 where the label is elsewhere); under
+    label smoothing also zsum, the slice's per-row sum of logits, as a
+    fourth (lce_forward_slice_ex)."""
     lib = load()
     _check_inputs(h, W_slice, labels)
     L, H = h.shape
@@ -430,30 +465,43 @@ def forward_slice(h: torch.Tensor, W_slice: torch.Tensor,
     dev = h.device
     if workspace is None:
         workspace = alloc_workspace(L, H, Vs, h.dtype, 0, dev)
-    if out is None:
-        out = torch.empty(3, L, dtype=torch.float32, device=dev)
-    m, s, zy = out[0], out[1], out[2]
-    st = lib.lce_forward_slice(h.data_ptr(), W_slice.data_ptr(),
-                               _dtype_code(h), labels.data_ptr(), L, H, Vs,
-                               v0, V_total, ignore_index, m.data_ptr(),
-                               s.data_ptr(), zy.data_ptr(),
-                               workspace.data_ptr(), workspace.numel(),
-                               _stream_ptr(dev))
+    out, rows = _slice_out(out, L, label_smoothing, dev)
+    opts = _opts(label_smoothing, z_loss)
+    if opts is None:
+        st = lib.lce_forward_slice(h.data_ptr(), W_slice.data_ptr(),
+                                   _dtype_code(h), labels.data_ptr(), L, H,
+                                   Vs, v0, V_total, ignore_index,
+                                   rows[0].data_ptr(), rows[1].data_ptr(),
+                                   rows[2].data_ptr(), workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(dev))
+    else:
+        st = lib.lce_forward_slice_ex(
+            h.data_ptr(), W_slice.data_ptr(), _dtype_code(h),
+            labels.data_ptr(), L, H, Vs, v0, V_total, ignore_index, opts,
+            rows[0].data_ptr(), rows[1].data_ptr(), rows[2].data_ptr(),
+            rows[3].data_ptr() if len(rows) == 4 else None,
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(dev))
     _check(st, "lce_forward_slice")
-    return m, s, zy
+    return rows
 
 
 def combine_slices(m: torch.Tensor, s: torch.Tensor, zy: torch.Tensor,
                    labels: torch.Tensor, V_total: int,
-                   ignore_index: int = IGNORE_INDEX, workspace=None):
-    """m, s, zy: float32 [P, L] (every slice's forward_slice output, in the
-    same slice order on every process). Returns (loss, lse [L])."""
+                   ignore_index: int = IGNORE_INDEX, workspace=None,
+                   zsum=None, label_smoothing: float = 0.0,
+                   z_loss: float = 0.0):
+    """m, s, zy (and zsum under label smoothing): float32 [P, L] (every
+    slice's forward_slice output, in the same slice order on every
+    process). Returns (loss, lse [L])."""
     lib = load()
     P, L = m.shape
-    for t in (m, s, zy):
+    ts = (m, s, zy) if zsum is None else (m, s, zy, zsum)
+    for t in ts:
         if t.dtype != torch.float32 or t.shape != (P, L) or not t.is_cuda:
-            raise ValueError("m, s, zy must be CUDA float32 [P, L] tensors")
+            raise ValueError("m, s, zy, zsum must be CUDA float32 [P, L] "
+                             "tensors")
     m, s, zy = m.contiguous(), s.contiguous(), zy.contiguous()
+    zsum = zsum.contiguous() if zsum is not None else None
     labels = labels.contiguous()
     dev = m.device
     if workspace is None:
@@ -461,11 +509,20 @@ def combine_slices(m: torch.Tensor, s: torch.Tensor, zy: torch.Tensor,
                                 dtype=torch.uint8, device=dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     lse = torch.empty(L, dtype=torch.float32, device=dev)
-    st = lib.lce_combine_slices(m.data_ptr(), s.data_ptr(), zy.data_ptr(), P,
-                                labels.data_ptr(), L, V_total, ignore_index,
-                                loss.data_ptr(), lse.data_ptr(),
-                                workspace.data_ptr(), workspace.numel(),
-                                _stream_ptr(dev))
+    opts = _opts(label_smoothing, z_loss)
+    if opts is None:
+        st = lib.lce_combine_slices(m.data_ptr(), s.data_ptr(), zy.data_ptr(),
+                                    P, labels.data_ptr(), L, V_total,
+                                    ignore_index, loss.data_ptr(),
+                                    lse.data_ptr(), workspace.data_ptr(),
+                                    workspace.numel(), _stream_ptr(dev))
+    else:
+        st = lib.lce_combine_slices_ex(
+            m.data_ptr(), s.data_ptr(), zy.data_ptr(),
+            zsum.data_ptr() if zsum is not None else None, P,
+            labels.data_ptr(), L, V_total, ignore_index, opts,
+            loss.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+            workspace.numel(), _stream_ptr(dev))
     _check(st, "lce_combine_slices")
     return loss, lse
 
@@ -474,7 +531,8 @@ def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
                    labels: torch.Tensor, lse: torch.Tensor,
                    dloss: torch.Tensor, v0: int, V_total: int,
                    ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
-                   workspace=None):
+                   workspace=None, label_smoothing: float = 0.0,
+                   z_loss: float = 0.0):
     """One vocabulary slice's backward from the merged lse: returns
     (dH_part [L,H] float32, whose sum over slices is dH; dW_slice [Vs,H])."""
     lib = load()
@@ -489,13 +547,15 @@ def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
         workspace = alloc_workspace(L, H, Vs, h.dtype, chunk_rows, dev)
     dH = torch.empty(L, H, dtype=torch.float32, device=dev)
     dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
-    st = lib.lce_backward_slice(h.data_ptr(), W_slice.data_ptr(),
-                                _dtype_code(h), labels.data_ptr(),
-                                lse.data_ptr(), L, H, Vs, v0, V_total,
-                                ignore_index, dloss.data_ptr(), chunk_rows,
-                                dH.data_ptr(), dW.data_ptr(),
-                                workspace.data_ptr(), workspace.numel(),
-                                _stream_ptr(dev))
+    st = lib.lce_backward_slice_ex(h.data_ptr(), W_slice.data_ptr(),
+                                   _dtype_code(h), labels.data_ptr(),
+                                   lse.data_ptr(), L, H, Vs, v0, V_total,
+                                   ignore_index,
+                                   _opts(label_smoothing, z_loss),
+                                   dloss.data_ptr(), chunk_rows,
+                                   dH.data_ptr(), dW.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel(),
+                                   _stream_ptr(dev))
     _check(st, "lce_backward_slice")
     return dH, dW
 
@@ -510,28 +570,28 @@ def slice_exp_workspace(L: int, H: int, Vs: int, dtype, device):
 
 
 def forward_slice_exp(h, W_slice, labels, v0: int, V_total: int, workspace,
-                      ignore_index: int = IGNORE_INDEX, out=None):
+                      ignore_index: int = IGNORE_INDEX, out=None,
+                      label_smoothing: float = 0.0, z_loss: float = 0.0):
     """forward_slice that also keeps the slice's tile exponentials in
     `workspace` (from slice_exp_workspace) for backward_slice_exp."""
     lib = load()
     _check_inputs(h, W_slice, labels)
     L, H = h.shape
     Vs = W_slice.shape[0]
-    if out is None:
-        out = torch.empty(3, L, dtype=torch.float32, device=h.device)
-    m, s, zy = out[0], out[1], out[2]
-    st = lib.lce_forward_slice_exp(h.data_ptr(), W_slice.data_ptr(),
-                                   _dtype_code(h), labels.data_ptr(), L, H,
-                                   Vs, v0, V_total, ignore_index,
-                                   m.data_ptr(), s.data_ptr(), zy.data_ptr(),
-                                   workspace.data_ptr(), workspace.numel(),
-                                   _stream_ptr(h.device))
+    out, rows = _slice_out(out, L, label_smoothing, h.device)
+    st = lib.lce_forward_slice_exp_ex(
+        h.data_ptr(), W_slice.data_ptr(), _dtype_code(h), labels.data_ptr(),
+        L, H, Vs, v0, V_total, ignore_index, _opts(label_smoothing, z_loss),
+        rows[0].data_ptr(), rows[1].data_ptr(), rows[2].data_ptr(),
+        rows[3].data_ptr() if len(rows) == 4 else None,
+        workspace.data_ptr(), workspace.numel(), _stream_ptr(h.device))
     _check(st, "lce_forward_slice_exp")
-    return m, s, zy
+    return rows
 
 
 def backward_slice_exp(h, W_slice, labels, lse, dloss, v0: int, V_total: int,
-                       workspace, ignore_index: int = IGNORE_INDEX):
+                       workspace, ignore_index: int = IGNORE_INDEX,
+                       label_smoothing: float = 0.0, z_loss: float = 0.0):
     """The slice's backward from the exponentials forward_slice_exp kept:
     returns (dH_part [L,H] float32, dW_slice [Vs,H] float32)."""
     lib = load()
@@ -544,13 +604,15 @@ def backward_slice_exp(h, W_slice, labels, lse, dloss, v0: int, V_total: int,
     dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
     dH = torch.empty(L, H, dtype=torch.float32, device=dev)
     dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
-    st = lib.lce_backward_slice_exp(h.data_ptr(), W_slice.data_ptr(),
-                                    _dtype_code(h), labels.data_ptr(),
-                                    lse.data_ptr(), L, H, Vs, v0, V_total,
-                                    ignore_index, dloss.data_ptr(),
-                                    dH.data_ptr(), dW.data_ptr(),
-                                    workspace.data_ptr(), workspace.numel(),
-                                    _stream_ptr(dev))
+    st = lib.lce_backward_slice_exp_ex(h.data_ptr(), W_slice.data_ptr(),
+                                       _dtype_code(h), labels.data_ptr(),
+                                       lse.data_ptr(), L, H, Vs, v0, V_total,
+                                       ignore_index,
+                                       _opts(label_smoothing, z_loss),
+                                       dloss.data_ptr(), dH.data_ptr(),
+                                       dW.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel(),
+                                       _stream_ptr(dev))
     _check(st, "lce_backward_slice_exp")
     return dH, dW
 

@@ -909,21 +909,49 @@ lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
                               const float* dloss, int64_t chunk_rows,
                               float* dH_part, float* dW, void* ws,
                               size_t ws_bytes, void* stream) {
+  return lce_backward_slice_ex(h, W, dt, labels, lse, L, H, Vs, v0, V_total,
+                               ignore_index, nullptr, dloss, chunk_rows,
+                               dH_part, dW, ws, ws_bytes, stream);
+}
+
+lce_status lce_backward_slice_ex(const void* h, const void* W, lce_dtype dt,
+                                 const int64_t* labels, const float* lse,
+                                 int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                                 int64_t V_total, int64_t ignore_index,
+                                 const lce_loss_opts* opts,
+                                 const float* dloss, int64_t chunk_rows,
+                                 float* dH_part, float* dW, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   if (v0 < 0 || Vs < 1 || V_total < 1 || v0 > V_total - Vs)
     return LCE_ERR_INVALID_ARG;
   return backward_impl(h, W, dt, labels, lse, L, H, Vs, v0, V_total,
                        ignore_index, dloss, chunk_rows, dH_part, true, dW, ws,
-                       ws_bytes, stream, Variant{}.grad(V_total));
+                       ws_bytes, stream, var.grad(V_total));
 }
 
-lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
-                             const int64_t* labels, int64_t L, int64_t H,
-                             int64_t Vs, int64_t v0, int64_t V_total,
-                             int64_t ignore_index, float* m, float* s_out,
-                             float* zy, void* ws, size_t ws_bytes,
-                             void* stream) {
+}  // extern "C"
+
+namespace lce {
+namespace {
+
+// One vocabulary slice's forward statistics: the logits pass with the
+// statistics epilogue, or (keep_exp) with the fused epilogue that also keeps
+// the slice's tile exponentials in ws; then the split partials merged into
+// m, s, zy and, when zsum is given, the slice's logit sums.
+lce_status forward_slice_impl(bool keep_exp, const void* h, const void* W,
+                              lce_dtype dt, const int64_t* labels, int64_t L,
+                              int64_t H, int64_t Vs, int64_t v0,
+                              int64_t V_total, int64_t ignore_index,
+                              const lce_loss_opts* opts, float* m,
+                              float* s_out, float* zy, float* zsum, void* ws,
+                              size_t ws_bytes, void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   if (!h || !W || !labels || !m || !s_out || !zy || !ws)
     return LCE_ERR_INVALID_ARG;
+  if (var.smooth() && !zsum) return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
     return LCE_ERR_INVALID_ARG;
@@ -931,10 +959,11 @@ lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
       (reinterpret_cast<uintptr_t>(labels) & 7u) ||
       (reinterpret_cast<uintptr_t>(m) & 3u) ||
       (reinterpret_cast<uintptr_t>(s_out) & 3u) ||
-      (reinterpret_cast<uintptr_t>(zy) & 3u))
+      (reinterpret_cast<uintptr_t>(zy) & 3u) ||
+      (reinterpret_cast<uintptr_t>(zsum) & 3u))
     return LCE_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(L, H, Vs, dt, 0);
-  if (ws_bytes < w.fwd_total) return LCE_ERR_WORKSPACE;
+  const WsLayout w = ws_layout(L, H, Vs, dt, keep_exp ? L : 0);
+  if (ws_bytes < (keep_exp ? w.total : w.fwd_total)) return LCE_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
   lce_status st = device_info(&dev);
   if (st != LCE_OK) return st;
@@ -957,30 +986,85 @@ lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
   if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true},
                       *dev, &pl)) != LCE_OK)
     return st;
-  LseParams p{};
-  p.labels = labels;
-  p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
-  p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
-  p.zy = reinterpret_cast<float*>(wsb + w.zy);
-  p.ignore_index = ignore_index;
-  p.v0 = v0;
-  p.v_total = V_total;
+  float* part_m = reinterpret_cast<float*>(wsb + w.part_m);
+  float* part_s = reinterpret_cast<float*>(wsb + w.part_s);
+  float* zy_in = reinterpret_cast<float*>(wsb + w.zy);
+  float* part_z = zsum ? reinterpret_cast<float*>(wsb + w.part_z) : nullptr;
   e = pace(&pl, wsb + w.sync, s);
   if (e != cudaSuccess) return cuda_fail(e, "pace");
-  {
+  if (keep_exp) {
+    // every row's logits once: statistics + tile exponentials kept in ws
+    uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
+    FusedParams p{};
+    p.labels = labels;
+    p.part_m = part_m;
+    p.part_s = part_s;
+    p.zy = zy_in;
+    p.part_z = part_z;
+    p.E = E;
+    p.ldg = w.ldg;
+    p.tile_max = reinterpret_cast<float*>(wsb + w.tile_max);
+    p.ignore_index = ignore_index;
+    p.v0 = v0;
+    p.v_total = V_total;
+    CUtensorMap te;
+    if ((st = tmap_store_box(&te, E, Vs, L, w.ldg)) != LCE_OK) return st;
+    ProfScope ps(LCE_K_GEMM_FUSED, s);
+    e = run_fused(pl, p, te, dev->err, s);
+    ps.done(2.0 * L * Vs * H);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_fused");
+  } else {
+    LseParams p{};
+    p.labels = labels;
+    p.part_m = part_m;
+    p.part_s = part_s;
+    p.zy = zy_in;
+    p.part_z = part_z;
+    p.ignore_index = ignore_index;
+    p.v0 = v0;
+    p.v_total = V_total;
     ProfScope ps(LCE_K_GEMM_LSE, s);
     e = run_lse(pl, p, dev->err, s);
     ps.done(2.0 * L * Vs * H);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_lse");
   }
-  if (e != cudaSuccess) return cuda_fail(e, "gemm_lse");
   {
     ProfScope ps(LCE_K_SLICE_STATS, s);
-    e = launch_slice_stats(p.part_m, p.part_s, pl.g.splits, p.zy, labels, L,
-                           v0, Vs, V_total, ignore_index, m, s_out, zy, s);
+    e = launch_slice_stats(part_m, part_s, pl.g.splits, zy_in, labels, L, v0,
+                           Vs, V_total, ignore_index, m, s_out, zy, s, part_z,
+                           zsum);
     ps.done(0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "slice_stats");
   return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+extern "C" {
+
+lce_status lce_forward_slice(const void* h, const void* W, lce_dtype dt,
+                             const int64_t* labels, int64_t L, int64_t H,
+                             int64_t Vs, int64_t v0, int64_t V_total,
+                             int64_t ignore_index, float* m, float* s_out,
+                             float* zy, void* ws, size_t ws_bytes,
+                             void* stream) {
+  return forward_slice_impl(false, h, W, dt, labels, L, H, Vs, v0, V_total,
+                            ignore_index, nullptr, m, s_out, zy, nullptr, ws,
+                            ws_bytes, stream);
+}
+
+lce_status lce_forward_slice_ex(const void* h, const void* W, lce_dtype dt,
+                                const int64_t* labels, int64_t L, int64_t H,
+                                int64_t Vs, int64_t v0, int64_t V_total,
+                                int64_t ignore_index,
+                                const lce_loss_opts* opts, float* m,
+                                float* s_out, float* zy, float* zsum,
+                                void* ws, size_t ws_bytes, void* stream) {
+  return forward_slice_impl(false, h, W, dt, labels, L, H, Vs, v0, V_total,
+                            ignore_index, opts, m, s_out, zy, zsum, ws,
+                            ws_bytes, stream);
 }
 
 size_t lce_slice_exp_workspace_size(int64_t L, int64_t H, int64_t Vs,
@@ -995,71 +1079,22 @@ lce_status lce_forward_slice_exp(const void* h, const void* W, lce_dtype dt,
                                  int64_t ignore_index, float* m, float* s_out,
                                  float* zy, void* ws, size_t ws_bytes,
                                  void* stream) {
-  if (!h || !W || !labels || !m || !s_out || !zy || !ws)
-    return LCE_ERR_INVALID_ARG;
-  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
-  if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
-    return LCE_ERR_INVALID_ARG;
-  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
-      (reinterpret_cast<uintptr_t>(labels) & 7u) ||
-      (reinterpret_cast<uintptr_t>(m) & 3u) ||
-      (reinterpret_cast<uintptr_t>(s_out) & 3u) ||
-      (reinterpret_cast<uintptr_t>(zy) & 3u))
-    return LCE_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(L, H, Vs, dt, L);
-  if (ws_bytes < w.total) return LCE_ERR_WORKSPACE;
-  DeviceInfo* dev = nullptr;
-  lce_status st = device_info(&dev);
-  if (st != LCE_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  const void *hb = nullptr, *Wb = nullptr;
-  if ((st = operands(h, W, dt, L, H, Vs, w, wsb, s, &hb, &Wb)) != LCE_OK)
-    return st;
-  auto* n_valid = reinterpret_cast<unsigned long long*>(wsb + w.n_valid);
-  cudaError_t e;
-  {
-    ProfScope ps(LCE_K_COUNT_VALID, s);
-    e = launch_count_valid(labels, L, V_total, ignore_index, n_valid,
-                           dev->err, s);
-    ps.done(0);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "count_valid");
-  // every row's logits once: statistics + tile exponentials kept in ws
-  GemmPlan pl;
-  if ((st = plan_gemm({L, Vs, H, false, false, hb, H, Wb, H, true},
-                      *dev, &pl)) != LCE_OK)
-    return st;
-  uint16_t* E = reinterpret_cast<uint16_t*>(wsb + w.G);
-  FusedParams p{};
-  p.labels = labels;
-  p.part_m = reinterpret_cast<float*>(wsb + w.part_m);
-  p.part_s = reinterpret_cast<float*>(wsb + w.part_s);
-  p.zy = reinterpret_cast<float*>(wsb + w.zy);
-  p.E = E;
-  p.ldg = w.ldg;
-  p.tile_max = reinterpret_cast<float*>(wsb + w.tile_max);
-  p.ignore_index = ignore_index;
-  p.v0 = v0;
-  p.v_total = V_total;
-  CUtensorMap te;
-  if ((st = tmap_store_box(&te, E, Vs, L, w.ldg)) != LCE_OK) return st;
-  e = pace(&pl, wsb + w.sync, s);
-  if (e != cudaSuccess) return cuda_fail(e, "pace");
-  {
-    ProfScope ps(LCE_K_GEMM_FUSED, s);
-    e = run_fused(pl, p, te, dev->err, s);
-    ps.done(2.0 * L * Vs * H);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "gemm_fused");
-  {
-    ProfScope ps(LCE_K_SLICE_STATS, s);
-    e = launch_slice_stats(p.part_m, p.part_s, pl.g.splits, p.zy, labels, L,
-                           v0, Vs, V_total, ignore_index, m, s_out, zy, s);
-    ps.done(0);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "slice_stats");
-  return LCE_OK;
+  return forward_slice_impl(true, h, W, dt, labels, L, H, Vs, v0, V_total,
+                            ignore_index, nullptr, m, s_out, zy, nullptr, ws,
+                            ws_bytes, stream);
+}
+
+lce_status lce_forward_slice_exp_ex(const void* h, const void* W,
+                                    lce_dtype dt, const int64_t* labels,
+                                    int64_t L, int64_t H, int64_t Vs,
+                                    int64_t v0, int64_t V_total,
+                                    int64_t ignore_index,
+                                    const lce_loss_opts* opts, float* m,
+                                    float* s_out, float* zy, float* zsum,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  return forward_slice_impl(true, h, W, dt, labels, L, H, Vs, v0, V_total,
+                            ignore_index, opts, m, s_out, zy, zsum, ws,
+                            ws_bytes, stream);
 }
 
 lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
@@ -1069,6 +1104,22 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
                                   const float* dloss, float* dH_part,
                                   float* dW, void* ws, size_t ws_bytes,
                                   void* stream) {
+  return lce_backward_slice_exp_ex(h, W, dt, labels, lse, L, H, Vs, v0,
+                                   V_total, ignore_index, nullptr, dloss,
+                                   dH_part, dW, ws, ws_bytes, stream);
+}
+
+lce_status lce_backward_slice_exp_ex(const void* h, const void* W,
+                                     lce_dtype dt, const int64_t* labels,
+                                     const float* lse, int64_t L, int64_t H,
+                                     int64_t Vs, int64_t v0, int64_t V_total,
+                                     int64_t ignore_index,
+                                     const lce_loss_opts* opts,
+                                     const float* dloss, float* dH_part,
+                                     float* dW, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   if (!h || !W || !labels || !lse || !dloss || !dH_part || !dW || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
@@ -1107,7 +1158,7 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
     e = launch_grad_from_exp(E, w.ldg,
                              reinterpret_cast<float*>(wsb + w.tile_max), num_n,
                              lse, labels, L, Vs, ignore_index, dev->num_sms, s,
-                             v0, V_total);
+                             v0, V_total, var.grad(V_total));
     ps.done(0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
@@ -1165,12 +1216,28 @@ lce_status lce_combine_slices(const float* m, const float* s_in,
                               int64_t V_total, int64_t ignore_index,
                               float* loss, float* lse, void* ws,
                               size_t ws_bytes, void* stream) {
+  return lce_combine_slices_ex(m, s_in, zy, nullptr, P, labels, L, V_total,
+                               ignore_index, nullptr, loss, lse, ws, ws_bytes,
+                               stream);
+}
+
+lce_status lce_combine_slices_ex(const float* m, const float* s_in,
+                                 const float* zy, const float* zsum, int64_t P,
+                                 const int64_t* labels, int64_t L,
+                                 int64_t V_total, int64_t ignore_index,
+                                 const lce_loss_opts* opts, float* loss,
+                                 float* lse, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  Variant var;
+  if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   if (!m || !s_in || !zy || !labels || !loss || !lse || !ws || P < 1 ||
       L < 1 || V_total < 1)
     return LCE_ERR_INVALID_ARG;
+  if (var.smooth() && !zsum) return LCE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(m) & 3u) ||
       (reinterpret_cast<uintptr_t>(s_in) & 3u) ||
       (reinterpret_cast<uintptr_t>(zy) & 3u) ||
+      (reinterpret_cast<uintptr_t>(zsum) & 3u) ||
       (reinterpret_cast<uintptr_t>(labels) & 7u) ||
       (reinterpret_cast<uintptr_t>(loss) & 3u) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(ws))
@@ -1194,8 +1261,12 @@ lce_status lce_combine_slices(const float* m, const float* s_in,
   int nb = 0;
   {
     ProfScope ps(LCE_K_COMBINE_SLICES, s);
+    // the logit sums only enter under label smoothing: without it the
+    // terms are the plain loss's, bit for bit, whatever zsum holds
     e = launch_combine_slices(m, s_in, zy, P, labels, L, V_total, ignore_index,
-                              lse, block_sums, &nb, s);
+                              lse, block_sums, &nb, s,
+                              var.smooth() ? zsum : nullptr, var.eps,
+                              var.zcoef);
     ps.done(0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "combine_slices");

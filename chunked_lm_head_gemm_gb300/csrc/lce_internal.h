@@ -241,21 +241,27 @@ cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
                                float eps = 0.f, float zcoef = 0.f);
 // Vocabulary slice: merge the per-split partials into the slice's per-row
 // max logit m (natural units) and sum of exp(z - m), and the label logit
-// (0 where the label is not in [v0, v0 + Vs)).
+// (0 where the label is not in [v0, v0 + Vs)); with part_z, also the
+// slice's per-row logit sum zsum.
 cudaError_t launch_slice_stats(const float* part_m, const float* part_s,
                                int splits, const float* zy_in,
                                const int64_t* labels, int64_t L, int64_t v0,
                                int64_t Vs, int64_t V_total,
                                int64_t ignore_index, float* m, float* s_out,
-                               float* zy, cudaStream_t s);
+                               float* zy, cudaStream_t s,
+                               const float* part_z = nullptr,
+                               float* zsum = nullptr);
 // P slices' statistics ([P][L] each) -> lse and per-256-row loss sums, the
-// slices merged in slice order.
+// slices merged in slice order; a loss variant as launch_lse_combine, the
+// logit sums from the slices' zsum ([P][L]).
 cudaError_t launch_combine_slices(const float* m, const float* s_in,
                                   const float* zy, int64_t P,
                                   const int64_t* labels, int64_t L,
                                   int64_t V_total, int64_t ignore_index,
                                   float* lse, double* block_sums,
-                                  int* nblocks_out, cudaStream_t s);
+                                  int* nblocks_out, cudaStream_t s,
+                                  const float* zsum = nullptr, float eps = 0.f,
+                                  float zcoef = 0.f);
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks,
                                  const unsigned long long* n_valid,
                                  float* loss, cudaStream_t s);

@@ -116,7 +116,9 @@ cudaError_t launch_lse_combine(const float* part_m, const float* part_s,
 // Vocabulary slice [v0, v0 + Vs): per row, the split partials merged in
 // split order into the slice's max logit m = ln 2 * M (natural units) and
 // sum of exp(z - m) = sum_k s_k 2^(m_k - M); the label logit where the label
-// lies in the slice, else 0 (so that summing the slices' values gives it).
+// lies in the slice, else 0 (so that summing the slices' values gives it);
+// when part_z is set, the sum of the slice's logits (the split sums added in
+// split order in float64, then rounded to float).
 __global__ void __launch_bounds__(COMBINE_THREADS)
     k_slice_stats(const float* __restrict__ part_m,
                   const float* __restrict__ part_s, int splits,
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
                   const int64_t* __restrict__ labels, int64_t L, int64_t v0,
                   int64_t Vs, int64_t V_total, int64_t ignore_index,
                   float* __restrict__ m, float* __restrict__ s,
-                  float* __restrict__ zy) {
+                  float* __restrict__ zy, const float* __restrict__ part_z,
+                  float* __restrict__ zsum) {
   const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
                     threadIdx.x;
   if (i >= L) return;
@@ -139,6 +142,11 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
   const bool here = label_valid(y, V_total, ignore_index) && y >= v0 &&
                     y < v0 + Vs;
   zy[i] = here ? zy_in[i] : 0.f;
+  if (part_z != nullptr) {
+    double t = 0.0;
+    for (int k = 0; k < splits; ++k) t += part_z[k * L + i];
+    zsum[i] = static_cast<float>(t);
+  }
 }
 
 cudaError_t launch_slice_stats(const float* part_m, const float* part_s,
@@ -146,25 +154,30 @@ cudaError_t launch_slice_stats(const float* part_m, const float* part_s,
                                const int64_t* labels, int64_t L, int64_t v0,
                                int64_t Vs, int64_t V_total,
                                int64_t ignore_index, float* m, float* s_out,
-                               float* zy, cudaStream_t s) {
+                               float* zy, cudaStream_t s, const float* part_z,
+                               float* zsum) {
   const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
   k_slice_stats<<<nb, COMBINE_THREADS, 0, s>>>(part_m, part_s, splits, zy_in,
                                                labels, L, v0, Vs, V_total,
-                                               ignore_index, m, s_out, zy);
+                                               ignore_index, m, s_out, zy,
+                                               part_z, zsum);
   return cudaGetLastError();
 }
 
 // P vocabulary slices' (m, s, zy), each [P][L]: lse = M + ln sum_r s_r
 // exp(m_r - M) with M = max_r m_r, the label logit = sum_r zy_r, merged in
 // slice order; then per-256-row float64 sums of (lse - z_y) over rows that
-// take part, as k_lse_combine.
+// take part, as k_lse_combine. With a loss variant (zsum set or zcoef != 0)
+// the term is lse - (1 - eps) z_y - (eps / V_total) sum_r zsum_r + zcoef
+// lse^2, the slices' logit sums added in slice order in float64.
 __global__ void __launch_bounds__(COMBINE_THREADS)
     k_combine_slices(const float* __restrict__ m, const float* __restrict__ s,
                      const float* __restrict__ zy, int64_t P,
                      const int64_t* __restrict__ labels, int64_t L,
                      int64_t V_total, int64_t ignore_index,
                      float* __restrict__ lse,
-                     double* __restrict__ block_sums) {
+                     double* __restrict__ block_sums,
+                     const float* __restrict__ zsum, float eps, float zcoef) {
   __shared__ double warp_sums[COMBINE_THREADS / 32];
   const int64_t i = blockIdx.x * static_cast<int64_t>(COMBINE_THREADS) +
                     threadIdx.x;
@@ -179,8 +192,20 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     }
     const float l = M + log2f(t) * LN2;
     lse[i] = l;
-    if (label_valid(labels[i], V_total, ignore_index))
-      term = static_cast<double>(l) - static_cast<double>(z);
+    if (label_valid(labels[i], V_total, ignore_index)) {
+      if (zsum == nullptr && zcoef == 0.f) {
+        term = static_cast<double>(l) - static_cast<double>(z);
+      } else {
+        const double ld = static_cast<double>(l);
+        double zs = 0.0;
+        if (zsum != nullptr)
+          for (int64_t r = 0; r < P; ++r) zs += zsum[r * L + i];
+        const double e = static_cast<double>(eps);
+        term = ld - (1.0 - e) * static_cast<double>(z) -
+               e / static_cast<double>(V_total) * zs +
+               static_cast<double>(zcoef) * ld * ld;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
@@ -198,12 +223,14 @@ cudaError_t launch_combine_slices(const float* m, const float* s_in,
                                   const int64_t* labels, int64_t L,
                                   int64_t V_total, int64_t ignore_index,
                                   float* lse, double* block_sums,
-                                  int* nblocks_out, cudaStream_t s) {
+                                  int* nblocks_out, cudaStream_t s,
+                                  const float* zsum, float eps, float zcoef) {
   const int nb = static_cast<int>((L + COMBINE_THREADS - 1) / COMBINE_THREADS);
   *nblocks_out = nb;
   k_combine_slices<<<nb, COMBINE_THREADS, 0, s>>>(m, s_in, zy, P, labels, L,
                                                   V_total, ignore_index, lse,
-                                                  block_sums);
+                                                  block_sums, zsum, eps,
+                                                  zcoef);
   return cudaGetLastError();
 }
 

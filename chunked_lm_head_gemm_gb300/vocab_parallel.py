@@ -15,6 +15,10 @@ vocabulary instead and each row's log-sum-exp must be merged from the slices:
               columns, dW_r = G_r^T h (stays local), dH_r = G_r W_r
               exchange: all-reduce (sum) of the fp32 dH_r, L H floats
 
+With label smoothing each slice also gives its per-row sum of logits (a
+fourth gathered row), and the merged loss and the slices' G are the
+smoothed cross entropy's; a z-loss needs nothing more than the merged lse.
+
 Every loss and gradient value comes from the library's kernels; this module
 only moves the statistics and partial sums between processes. With no group
 (or a group of one) the one slice is the whole vocabulary.
@@ -34,8 +38,9 @@ def _world(group) -> int:
 
 
 def gather_stats(stats: torch.Tensor, group=None) -> torch.Tensor:
-    """stats [3, L] (m, s, zy of this process's slice) -> [P, 3, L] in rank
-    order, the same on every process."""
+    """stats [R, L] (m, s, zy and, under label smoothing, zsum of this
+    process's slice) -> [P, R, L] in rank order, the same on every
+    process."""
     world = _world(group)
     if world == 1:
         return stats.unsqueeze(0)
@@ -54,27 +59,41 @@ def sum_partials(dH_part: torch.Tensor, group=None) -> torch.Tensor:
     return dH_part
 
 
+def _merge(rows, labels, V_total, group, ignore_index, label_smoothing,
+           z_loss):
+    """This slice's statistics rows -> gathered over the group -> merged
+    (loss, lse) of the whole vocabulary."""
+    allst = gather_stats(torch.stack(rows), group)
+    col = [allst[:, r].contiguous() for r in range(len(rows))]
+    return B.combine_slices(col[0], col[1], col[2], labels, V_total,
+                            ignore_index,
+                            zsum=col[3] if len(col) == 4 else None,
+                            label_smoothing=label_smoothing, z_loss=z_loss)
+
+
 def forward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
             v0: int, V_total: int, group=None,
-            ignore_index: int = B.IGNORE_INDEX, workspace=None):
+            ignore_index: int = B.IGNORE_INDEX, workspace=None,
+            label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Returns (loss, lse [L]) of the whole vocabulary on every process."""
-    m, s, zy = B.forward_slice(h, W_slice, labels, v0, V_total, ignore_index,
-                               workspace)
-    allst = gather_stats(torch.stack([m, s, zy]), group)
-    return B.combine_slices(allst[:, 0].contiguous(), allst[:, 1].contiguous(),
-                            allst[:, 2].contiguous(), labels, V_total,
-                            ignore_index)
+    rows = B.forward_slice(h, W_slice, labels, v0, V_total, ignore_index,
+                           workspace, label_smoothing=label_smoothing,
+                           z_loss=z_loss)
+    return _merge(rows, labels, V_total, group, ignore_index,
+                  label_smoothing, z_loss)
 
 
 def backward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
              lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
              group=None, ignore_index: int = B.IGNORE_INDEX,
-             chunk_rows: int = 0, workspace=None):
+             chunk_rows: int = 0, workspace=None,
+             label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Returns (dH [L,H] float32, summed over the group; dW of this slice
     [Vs,H] float32)."""
     dH_part, dW = B.backward_slice(h, W_slice, labels, lse, dloss, v0,
                                    V_total, ignore_index, chunk_rows,
-                                   workspace)
+                                   workspace, label_smoothing=label_smoothing,
+                                   z_loss=z_loss)
     return sum_partials(dH_part, group), dW
 
 
@@ -87,24 +106,27 @@ def exp_workspace(h: torch.Tensor, W_slice: torch.Tensor) -> torch.Tensor:
 
 def forward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
                 v0: int, V_total: int, workspace: torch.Tensor, group=None,
-                ignore_index: int = B.IGNORE_INDEX):
+                ignore_index: int = B.IGNORE_INDEX,
+                label_smoothing: float = 0.0, z_loss: float = 0.0):
     """forward, keeping this slice's exponentials in `workspace` so that
     backward_exp need not recompute the logits."""
-    m, s, zy = B.forward_slice_exp(h, W_slice, labels, v0, V_total, workspace,
-                                   ignore_index)
-    allst = gather_stats(torch.stack([m, s, zy]), group)
-    return B.combine_slices(allst[:, 0].contiguous(), allst[:, 1].contiguous(),
-                            allst[:, 2].contiguous(), labels, V_total,
-                            ignore_index)
+    rows = B.forward_slice_exp(h, W_slice, labels, v0, V_total, workspace,
+                               ignore_index, label_smoothing=label_smoothing,
+                               z_loss=z_loss)
+    return _merge(rows, labels, V_total, group, ignore_index,
+                  label_smoothing, z_loss)
 
 
 def backward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
                  lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
                  workspace: torch.Tensor, group=None,
-                 ignore_index: int = B.IGNORE_INDEX):
+                 ignore_index: int = B.IGNORE_INDEX,
+                 label_smoothing: float = 0.0, z_loss: float = 0.0):
     """backward from the exponentials forward_exp kept (same workspace)."""
     dH_part, dW = B.backward_slice_exp(h, W_slice, labels, lse, dloss, v0,
-                                       V_total, workspace, ignore_index)
+                                       V_total, workspace, ignore_index,
+                                       label_smoothing=label_smoothing,
+                                       z_loss=z_loss)
     return sum_partials(dH_part, group), dW
 
 
@@ -114,22 +136,26 @@ class VocabParallelCrossEntropy(torch.autograd.Function):
     process of the group); backward returns dH summed over the group and
     this slice's dW. keep_exp=True keeps the slice's exponentials between
     forward and backward (no recompute, L x Vs x 2 bytes of workspace held
-    until backward); else only lse is kept and the backward recomputes."""
+    until backward); else only lse is kept and the backward recomputes.
+    label_smoothing / z_loss select the loss variant (the same on every
+    process)."""
 
     @staticmethod
     def forward(ctx, h, W_slice, labels, v0, V_total, group=None,
-                ignore_index=B.IGNORE_INDEX, keep_exp=False):
+                ignore_index=B.IGNORE_INDEX, keep_exp=False,
+                label_smoothing=0.0, z_loss=0.0):
         ctx.v0, ctx.V_total, ctx.group = v0, V_total, group
         ctx.ignore_index, ctx.keep_exp = ignore_index, keep_exp
         ctx.w_dtype, ctx.h_dtype = W_slice.dtype, h.dtype
+        ctx.variant = dict(label_smoothing=label_smoothing, z_loss=z_loss)
         if keep_exp:
             ws = exp_workspace(h, W_slice)
             loss, lse = forward_exp(h, W_slice, labels, v0, V_total, ws,
-                                    group, ignore_index)
+                                    group, ignore_index, **ctx.variant)
             ctx.ws = ws
         else:
             loss, lse = forward(h, W_slice, labels, v0, V_total, group,
-                                ignore_index)
+                                ignore_index, **ctx.variant)
             ctx.ws = None
         ctx.save_for_backward(h, W_slice, labels, lse)
         return loss
@@ -140,18 +166,22 @@ class VocabParallelCrossEntropy(torch.autograd.Function):
         if ctx.keep_exp:
             dH, dW = backward_exp(h, W_slice, labels, lse, dloss, ctx.v0,
                                   ctx.V_total, ctx.ws, ctx.group,
-                                  ctx.ignore_index)
+                                  ctx.ignore_index, **ctx.variant)
             ctx.ws = None
         else:
             dH, dW = backward(h, W_slice, labels, lse, dloss, ctx.v0,
-                              ctx.V_total, ctx.group, ctx.ignore_index)
+                              ctx.V_total, ctx.group, ctx.ignore_index,
+                              **ctx.variant)
         return (dH.to(ctx.h_dtype), dW.to(ctx.w_dtype), None, None, None,
-                None, None, None)
+                None, None, None, None, None)
 
 
 def vocab_parallel_cross_entropy(h, W_slice, labels, v0: int, V_total: int,
                                  group=None,
                                  ignore_index: int = B.IGNORE_INDEX,
-                                 keep_exp: bool = False):
+                                 keep_exp: bool = False,
+                                 label_smoothing: float = 0.0,
+                                 z_loss: float = 0.0):
     return VocabParallelCrossEntropy.apply(h, W_slice, labels, v0, V_total,
-                                           group, ignore_index, keep_exp)
+                                           group, ignore_index, keep_exp,
+                                           label_smoothing, z_loss)

@@ -306,6 +306,63 @@ lce_status lce_backward_slice_exp(const void* h, const void* W, lce_dtype dt,
                                   void* stream);
 
 /*
+ * The vocabulary-parallel calls with a loss variant (lce_loss_opts; NULL or
+ * {0, 0} is the plain loss, with the same bits as the calls without _ex).
+ * Label smoothing needs each row's sum of logits over the whole vocabulary:
+ *   zsum     device [L] float32 out of the forward calls: sum_j z_ij over the
+ *            slice's columns (the split sums added in float64, rounded to
+ *            float); required when label_smoothing > 0, else may be NULL
+ *            (written whenever given). The caller gathers it with m, s, zy.
+ *   zsum     device [P][L] float32 in to lce_combine_slices_ex, slice r at
+ *            r * L in the order of m, s, zy; required when label_smoothing
+ *            > 0, else ignored (may be NULL).
+ * The merged loss is the variant's of lce_forward_ex over V_total, and the
+ * backward calls give the slice's columns of its G (eps / V_total is the
+ * smoothing mass per column, the z-loss factor uses the merged lse). Every
+ * process must pass the same opts to all of its calls. Missing zsum or
+ * invalid opts return LCE_ERR_INVALID_ARG before anything is queued.
+ */
+lce_status lce_forward_slice_ex(const void* h, const void* W, lce_dtype dt,
+                                const int64_t* labels, int64_t L, int64_t H,
+                                int64_t Vs, int64_t v0, int64_t V_total,
+                                int64_t ignore_index,
+                                const lce_loss_opts* opts, float* m, float* s,
+                                float* zy, float* zsum, void* ws,
+                                size_t ws_bytes, void* stream);
+lce_status lce_combine_slices_ex(const float* m, const float* s,
+                                 const float* zy, const float* zsum, int64_t P,
+                                 const int64_t* labels, int64_t L,
+                                 int64_t V_total, int64_t ignore_index,
+                                 const lce_loss_opts* opts, float* loss,
+                                 float* lse, void* ws, size_t ws_bytes,
+                                 void* stream);
+lce_status lce_backward_slice_ex(const void* h, const void* W, lce_dtype dt,
+                                 const int64_t* labels, const float* lse,
+                                 int64_t L, int64_t H, int64_t Vs, int64_t v0,
+                                 int64_t V_total, int64_t ignore_index,
+                                 const lce_loss_opts* opts,
+                                 const float* dloss, int64_t chunk_rows,
+                                 float* dH_part, float* dW, void* ws,
+                                 size_t ws_bytes, void* stream);
+lce_status lce_forward_slice_exp_ex(const void* h, const void* W,
+                                    lce_dtype dt, const int64_t* labels,
+                                    int64_t L, int64_t H, int64_t Vs,
+                                    int64_t v0, int64_t V_total,
+                                    int64_t ignore_index,
+                                    const lce_loss_opts* opts, float* m,
+                                    float* s, float* zy, float* zsum,
+                                    void* ws, size_t ws_bytes, void* stream);
+lce_status lce_backward_slice_exp_ex(const void* h, const void* W,
+                                     lce_dtype dt, const int64_t* labels,
+                                     const float* lse, int64_t L, int64_t H,
+                                     int64_t Vs, int64_t v0, int64_t V_total,
+                                     int64_t ignore_index,
+                                     const lce_loss_opts* opts,
+                                     const float* dloss, float* dH_part,
+                                     float* dW, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/*
  * Count of rows that take part in the loss: n_valid[0] = #{i : labels[i] !=
  * ignore_index and 0 <= labels[i] < V}. A label that is neither raises
  * LCE_ERR_LABEL_RANGE in the device error word and is not counted, as in

@@ -133,6 +133,45 @@ def test_bad_arguments_return_before_any_device_call(lib):
                               null) == 3
     assert lib.lce_forward_ex(p, p, 0, p, 8, 8, 8, -100, None, p, p, p, 16,
                               null) == 3
+    # loss variants on vocabulary slices: bad options are refused, and the
+    # logit sums are required (and 4-byte aligned) under label smoothing
+    smooth = ctypes.pointer(B.LossOpts(0.1, 0.0))
+    zonly = ctypes.pointer(B.LossOpts(0.0, 1e-4))
+    odd = ctypes.c_void_p(0x1002)
+    for o in (ctypes.pointer(B.LossOpts(-0.1, 0.0)),
+              ctypes.pointer(B.LossOpts(0.0, float("nan")))):
+        assert lib.lce_forward_slice_ex(p, p, 0, p, 8, 8, 8, 0, 10, -100, o,
+                                        p, p, p, p, p, 1 << 30, null) == 1
+        assert lib.lce_forward_slice_exp_ex(p, p, 0, p, 8, 8, 8, 0, 10, -100,
+                                            o, p, p, p, p, p, 1 << 30,
+                                            null) == 1
+        assert lib.lce_combine_slices_ex(p, p, p, p, 2, p, 8, 10, -100, o, p,
+                                         p, p, 1 << 20, null) == 1
+        assert lib.lce_backward_slice_ex(p, p, 0, p, p, 8, 8, 8, 0, 10, -100,
+                                         o, p, 0, p, p, p, 1 << 30,
+                                         null) == 1
+        assert lib.lce_backward_slice_exp_ex(p, p, 0, p, p, 8, 8, 8, 0, 10,
+                                             -100, o, p, p, p, p, 1 << 30,
+                                             null) == 1
+    for f in (lib.lce_forward_slice_ex, lib.lce_forward_slice_exp_ex):
+        assert f(p, p, 0, p, 8, 8, 8, 0, 10, -100, smooth, p, p, p, null, p,
+                 1 << 30, null) == 1
+        assert f(p, p, 0, p, 8, 8, 8, 0, 10, -100, smooth, p, p, p, odd, p,
+                 1 << 30, null) == 1
+        # no smoothing: the sums are optional; a small workspace is next
+        assert f(p, p, 0, p, 8, 8, 8, 0, 10, -100, zonly, p, p, p, null, p,
+                 16, null) == 3
+    assert lib.lce_combine_slices_ex(p, p, p, null, 2, p, 8, 10, -100,
+                                     smooth, p, p, p, 1 << 20, null) == 1
+    assert lib.lce_combine_slices_ex(p, p, p, odd, 2, p, 8, 10, -100,
+                                     smooth, p, p, p, 1 << 20, null) == 1
+    assert lib.lce_combine_slices_ex(p, p, p, null, 2, p, 8, 10, -100,
+                                     zonly, p, p, p, 8, null) == 3
+    assert lib.lce_backward_slice_ex(p, p, 0, p, p, 8, 8, 8, 4, 10, -100,
+                                     smooth, p, 0, p, p, p, 1 << 30,
+                                     null) == 1
+    assert lib.lce_backward_slice_exp_ex(p, p, 0, p, p, 8, 8, 8, 0, 10, -100,
+                                         smooth, p, p, p, p, 16, null) == 3
     # the shard combine: null or misaligned pointers
     assert lib.lce_shard_sums(null, p, p, null) == 1
     assert lib.lce_shard_sums(p, p, ctypes.c_void_p(0x1004), null) == 1

@@ -186,3 +186,124 @@ def test_autograd_function_one_slice(keep):
     assert hl.grad.dtype == h.dtype and Wl.grad.dtype == W.dtype
     assert rel_fro(to64(hl.grad), to64(dH1)) <= 8e-3
     assert rel_fro(to64(Wl.grad), to64(dW1)) <= 8e-3
+
+
+# Loss variants (label smoothing eps, z-loss coefficient) in the
+# vocabulary-parallel form: merged over the slices, the smoothed cross
+# entropy plus the z-loss of the whole vocabulary, against the float64
+# oracle's variant (the reading: target (1 - eps) onehot + eps / V_total,
+# coef * lse^2 per valid row).
+SLICE_VARIANTS = [(0.1, 0.0), (0.0, 1e-2), (0.2, 1e-3)]
+
+
+@pytest.mark.parametrize("keep", [False, True], ids=["recompute", "keep_exp"])
+@pytest.mark.parametrize("eps,zc", SLICE_VARIANTS,
+                         ids=[f"eps{e}-z{z}" for e, z in SLICE_VARIANTS])
+@pytest.mark.parametrize("name,L,H,V,sizes,chunk", CASES[:2],
+                         ids=[c[0] for c in CASES[:2]])
+def test_slices_with_loss_variant(name, L, H, V, sizes, chunk, eps, zc,
+                                  keep):
+    h, W, y = _inputs(name, L, H, V)
+    hc, Wc, yc = h.cpu(), W.cpu(), y.cpu()
+    dloss = torch.full((), 0.5, device=h.device)
+    var = dict(label_smoothing=eps, z_loss=zc)
+    wss = [B.slice_exp_workspace(L, H, Vs, h.dtype, h.device) if keep
+           else None for _, Vs in _bounds(sizes)]
+    stats = []
+    for k, (v0, Vs) in enumerate(_bounds(sizes)):
+        if keep:
+            rows = B.forward_slice_exp(h, W[v0:v0 + Vs], y, v0, V, wss[k],
+                                       **var)
+        else:
+            rows = B.forward_slice(h, W[v0:v0 + Vs], y, v0, V, **var)
+        assert len(rows) == (4 if eps else 3)
+        if eps:
+            # the slice's logit sums against their definition in float64,
+            # sum_j z_ij = sum_j h_i . W_j over the slice's columns
+            z = hc.double() @ Wc[v0:v0 + Vs].double().T
+            err = (rows[3].double().cpu() - z.sum(1)).abs()
+            assert torch.all(err <= 1e-5 * z.abs().sum(1) + 1e-4)
+        stats.append(torch.stack(rows))
+    allst = torch.stack(stats)
+    col = [allst[:, r].contiguous() for r in range(allst.shape[1])]
+    loss, lse = B.combine_slices(col[0], col[1], col[2], y, V,
+                                 zsum=col[3] if eps else None, **var)
+    dH = torch.zeros(L, H, dtype=torch.float32, device=h.device)
+    dWs = []
+    for k, (v0, Vs) in enumerate(_bounds(sizes)):
+        if keep:
+            dH_part, dW_s = B.backward_slice_exp(h, W[v0:v0 + Vs], y, lse,
+                                                 dloss, v0, V, wss[k], **var)
+        else:
+            dH_part, dW_s = B.backward_slice(h, W[v0:v0 + Vs], y, lse, dloss,
+                                             v0, V, chunk_rows=chunk, **var)
+        dH += dH_part
+        dWs.append(dW_s)
+    dW = torch.cat(dWs)
+    assert lce.get_error() == 0
+    fb = oracle.forward_backward(hc, Wc, yc, dloss=0.5, **var)
+    assert abs(loss.item() - fb["loss"]) <= LOSS_RTOL * abs(fb["loss"])
+    assert np.max(np.abs(to64(lse) - fb["lse"])) <= LSE_ATOL
+    assert rel_fro(to64(dH), fb["dH"]) <= GRAD_RFRO
+    assert rel_fro(to64(dW), fb["dW"]) <= GRAD_RFRO
+
+
+def test_slice_ex_calls_with_zero_options_are_the_plain_calls():
+    """The _ex slice calls given {0, 0} (and the logit sums anyway) give
+    the plain calls' bits; the logit sums are written but do not enter."""
+    import ctypes
+    h, W, y = _inputs("zero_opts", 300, 64, 1000)
+    lib = lce.load()
+    zero = ctypes.pointer(B.LossOpts(0.0, 0.0))
+    L, H = h.shape
+    v0, Vs, V = 333, 333, 1000
+    Ws = W[v0:v0 + Vs].contiguous()
+    plain = B.forward_slice(h, Ws, y, v0, V)
+    ws = B.alloc_workspace(L, H, Vs, h.dtype, 0, h.device)
+    out = torch.empty(4, L, dtype=torch.float32, device=h.device)
+    st = lib.lce_forward_slice_ex(
+        h.data_ptr(), Ws.data_ptr(), B.LCE_BF16, y.data_ptr(), L, H, Vs, v0,
+        V, -100, zero, out[0].data_ptr(), out[1].data_ptr(),
+        out[2].data_ptr(), out[3].data_ptr(), ws.data_ptr(), ws.numel(),
+        torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    for a, b in zip(plain, out[:3]):
+        assert torch.equal(a, b)
+    z = h.cpu().double() @ Ws.cpu().double().T
+    err = (out[3].double().cpu() - z.sum(1)).abs()
+    assert torch.all(err <= 1e-5 * z.abs().sum(1) + 1e-4)
+    # combine: the plain call and the _ex call with zsum and {0, 0}
+    loss0, lse0 = B.combine_slices(plain[0][None], plain[1][None],
+                                   plain[2][None], y, V)
+    cws = torch.empty(lib.lce_combine_workspace_size(L), dtype=torch.uint8,
+                      device=h.device)
+    loss1 = torch.empty((), dtype=torch.float32, device=h.device)
+    lse1 = torch.empty(L, dtype=torch.float32, device=h.device)
+    st = lib.lce_combine_slices_ex(
+        out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+        out[3].data_ptr(), 1, y.data_ptr(), L, V, -100, zero,
+        loss1.data_ptr(), lse1.data_ptr(), cws.data_ptr(), cws.numel(),
+        torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    assert torch.equal(loss0, loss1) and torch.equal(lse0, lse1)
+    assert lce.get_error() == 0
+
+
+@pytest.mark.parametrize("keep", [False, True], ids=["recompute", "keep_exp"])
+def test_autograd_function_one_slice_with_variant(keep):
+    """With no group and a loss variant, the autograd Function's loss and
+    gradients equal the whole-vocabulary variant calls'."""
+    h, W, y = _inputs("ag_var", 320, 64, 1500)
+    var = dict(label_smoothing=0.15, z_loss=2e-3)
+    hl = h.clone().requires_grad_(True)
+    Wl = W.clone().requires_grad_(True)
+    loss = vp.vocab_parallel_cross_entropy(hl, Wl, y, 0, 1500,
+                                           keep_exp=keep, **var)
+    (2.0 * loss).backward()
+    d = torch.full((), 2.0, device=h.device)
+    loss1, lse1 = lce.forward(h, W, y, **var)
+    dH1, dW1 = lce.backward(h, W, y, lse1, d, **var)
+    assert lce.get_error() == 0
+    assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
+    assert rel_fro(to64(hl.grad), to64(dH1)) <= 8e-3
+    assert rel_fro(to64(Wl.grad), to64(dW1)) <= 8e-3
