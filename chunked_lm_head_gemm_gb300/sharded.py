@@ -67,16 +67,21 @@ def sum_weight_grad(dW: torch.Tensor, group=None) -> torch.Tensor:
 def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
                      group=None, dloss: torch.Tensor | None = None,
                      ignore_index: int = B.IGNORE_INDEX, chunk_rows: int = 0,
-                     workspace=None):
+                     workspace=None, label_smoothing: float = 0.0,
+                     z_loss: float = 0.0):
     """This shard's rows of one sequence: returns (loss, lse, dH, dW) where
     loss is the whole sequence's mean loss (identical on every process), lse
     and dH are this shard's rows, and dW is the weight gradient of the whole
-    sequence (summed over the group). dloss defaults to 1."""
+    sequence (summed over the group). dloss defaults to 1. A loss variant
+    (label_smoothing, z_loss; the same on every process) is still a mean of
+    per-row terms over the valid rows, so it combines the same way."""
     V = W.shape[0]
     loss_r, lse, dH, dW = B.forward_backward(h, W, labels,
                                              ignore_index=ignore_index,
                                              chunk_rows=chunk_rows,
-                                             workspace=workspace)
+                                             workspace=workspace,
+                                             label_smoothing=label_smoothing,
+                                             z_loss=z_loss)
     n_r = B.count_valid(labels, V, ignore_index)
     loss, weight = combine_loss(loss_r, n_r, group, dloss)
     B.scale_gradients(dH, dW, weight)

@@ -134,3 +134,42 @@ def test_combine_shards_edge_cases():
     loss, weight = B.combine_shards(zero, n[1], d)
     assert loss.item() == 0.0 and weight.item() == 0.0
     assert B.get_error() == 0
+
+
+@pytest.mark.parametrize("eps,zc", [(0.1, 0.0), (0.2, 1e-3)],
+                         ids=["eps0.1", "eps0.2-z0.001"])
+def test_sequential_shards_with_loss_variant(eps, zc):
+    """A loss variant's shards combine as the plain loss's do (the variant
+    is still a mean of per-row terms over the valid rows): the shards'
+    combined loss and gradients against the oracle's variant on the whole
+    sequence."""
+    dev = require_gpu()
+    h, W, y = make_inputs(WL, seed=7, device=dev)
+    var = dict(label_smoothing=eps, z_loss=zc)
+    parts = []
+    for r0, r1 in zip(BOUNDS[:-1], BOUNDS[1:]):
+        loss_r, lse_r, dH_r, dW_r = lce.forward_backward(
+            h[r0:r1].contiguous(), W, y[r0:r1].contiguous(), **var)
+        parts.append((loss_r, dH_r, dW_r,
+                      B.count_valid(y[r0:r1].contiguous(), WL.V)))
+    total = sum(B.shard_sums(p[0], p[3]) for p in parts)
+    d = torch.full((), 0.75, device=dev)
+    dW = torch.zeros(WL.V, WL.H, dtype=torch.float32, device=dev)
+    dH = []
+    for loss_r, dH_r, dW_r, n_r in parts:
+        loss, weight = B.combine_shards(total, n_r, d)
+        lce.scale_gradients(dH_r, dW_r, weight)
+        dH.append(dH_r)
+        dW += dW_r
+    assert lce.get_error() == 0
+    fb = oracle.forward_backward(h.cpu(), W.cpu(), y.cpu(), dloss=0.75,
+                                 **var)
+    assert abs(loss.item() - fb["loss"]) <= LOSS_RTOL * abs(fb["loss"])
+    assert rel_fro(to64(torch.cat(dH)), fb["dH"]) <= GRAD_RFRO
+    assert rel_fro(to64(dW), fb["dW"]) <= GRAD_RFRO
+    # the module's call without a group is the single variant call
+    s = sharded.forward_backward(h, W, y, dloss=d, **var)
+    ref = lce.forward_backward(h, W, y, **var)
+    lce.scale_gradients(ref[2], ref[3], d)
+    assert torch.equal(s[0], ref[0]) and torch.equal(s[2], ref[2])
+    assert torch.equal(s[3], ref[3])
