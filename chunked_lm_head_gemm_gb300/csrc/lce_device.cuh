@@ -143,6 +143,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// Wait until no committed group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Wait until every committed group has completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -277,6 +281,34 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Two fp32 lanes in one 64-bit register pair, for the paired fp32
+// instructions (fma/add .rn.f32x2): each lane rounds exactly as the scalar
+// instruction does, so a paired loop gives the scalar loop's bits.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -381,6 +413,39 @@ __device__ __forceinline__ Unit decode_unit(const GemmGeom& g, int u,
 // epilogues: one thread per accumulator row, 32 columns per TMEM load
 // ---------------------------------------------------------------------------
 
+// Over the first nv (1..64) of one 64-column TMEM load, four interleaved
+// partials each: the largest value, and the sum (label smoothing's logit
+// sums). A whole piece (nv == 64, warp-uniform) runs without column guards.
+__device__ __forceinline__ float piece_max(const float (&v)[64], int nv) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (nv == 64) {
+#pragma unroll
+    for (int i = 0; i < 64; i += 8) {
+      mx[0] = max3(mx[0], v[i], v[i + 1]);
+      mx[1] = max3(mx[1], v[i + 2], v[i + 3]);
+      mx[2] = max3(mx[2], v[i + 4], v[i + 5]);
+      mx[3] = max3(mx[3], v[i + 6], v[i + 7]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i < nv) mx[i & 3] = fmaxf(mx[i & 3], v[i]);
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+__device__ __forceinline__ float piece_sum(const float (&v)[64], int nv) {
+  float za[4] = {0.f, 0.f, 0.f, 0.f};
+  if (nv == 64) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) za[i & 3] += v[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i < nv) za[i & 3] += v[i];
+  }
+  return (za[0] + za[1]) + (za[2] + za[3]);
+}
+
 // What every epilogue may use besides its parameters: the store map and
 // the two shared-memory staging buffers of this warp (EPI_BUF_BYTES each,
 // 1 KB aligned, for 64-byte-swizzled EPI_BOX x EPI_BOX bf16 boxes), and how
@@ -425,6 +490,45 @@ struct EpiBase {
     if (lane == 0) {
       tma_store_2d(map ? map : te, buf, static_cast<int32_t>(j0),
                    static_cast<int32_t>(wrow0));
+      bulk_commit();
+    }
+    ++nstored;
+  }
+
+  // Both 32-column boxes of a 64-column piece at once, columns [j0, j0 +
+  // 32) from w0 and, when `second`, [j0 + 32, j0 + 64) from w1: the two
+  // buffers filled together, one proxy fence, both stores in one group
+  // (half the fences and warp syncs of two store_box_words calls). An
+  // epilogue uses either this or store_box_words, never both, since this
+  // takes both buffers at once.
+  __device__ __forceinline__ void store_box_pair(const uint32_t (&w0)[16],
+                                                 const uint32_t (&w1)[16],
+                                                 int64_t j0, int64_t wrow0,
+                                                 bool second) {
+    const uint32_t lane = threadIdx.x & 31u;
+    if (lane == 0 && nstored > 0) bulk_wait_read0();
+    __syncwarp();
+    const uint32_t rowa = stage + lane * 64u;
+    const uint32_t rowb = rowa + EPI_BUF_BYTES;
+    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(rowa + ((static_cast<uint32_t>(q) ^ sw) << 4), w0[4 * q],
+                   w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
+    if (second) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(rowb + ((static_cast<uint32_t>(q) ^ sw) << 4), w1[4 * q],
+                     w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(te, stage, static_cast<int32_t>(j0),
+                   static_cast<int32_t>(wrow0));
+      if (second)
+        tma_store_2d(te, stage + EPI_BUF_BYTES, static_cast<int32_t>(j0 + 32),
+                     static_cast<int32_t>(wrow0));
       bulk_commit();
     }
     ++nstored;
@@ -477,24 +581,30 @@ struct EpiLse : EpiBase {
           if (i == yo) zyv = v[i];
         p.zy[row] = zyv;
       }
-      if (p.part_z != nullptr) {  // warp-uniform
-        float za[4] = {0.f, 0.f, 0.f, 0.f};
+      if (p.part_z != nullptr) zs += piece_sum(v, nv);  // warp-uniform
+      // max(v) log2 e is max(v log2 e) exactly (rounding is monotone)
+      const float mn = fmaxf(m2, piece_max(v, nv) * LOG2E);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (nv == 64) {  // warp-uniform: a whole piece, no column guards
+        const uint64_t c2 = f2pack(LOG2E, LOG2E), m2n = f2pack(-mn, -mn);
+        uint64_t a01 = f2pack(0.f, 0.f), a23 = a01;  // acc[0..1], acc[2..3]
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          float x0, x1;
+          f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, m2n), x0, x1);
+          const uint64_t e = f2pack(ex2(x0), ex2(x1));
+          if ((i & 2) == 0)
+            a01 = add2(a01, e);
+          else
+            a23 = add2(a23, e);
+        }
+        f2unpack(a01, acc[0], acc[1]);
+        f2unpack(a23, acc[2], acc[3]);
+      } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
-          if (i < nv) za[i & 3] += v[i];
-        zs += (za[0] + za[1]) + (za[2] + za[3]);
+          if (i < nv) acc[i & 3] += ex2(fmaf(v[i], LOG2E, -mn));
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        v[i] = (i < nv) ? v[i] * LOG2E : -INFINITY;
-        mx[i & 3] = fmaxf(mx[i & 3], v[i]);
-      }
-      const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float mn = fmaxf(m2, cmax);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i & 3] += ex2(v[i] - mn);
       s = s * ex2(m2 - mn) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       m2 = mn;
     }
@@ -523,8 +633,9 @@ struct EpiGrad : EpiBase {
   bool row_ok;
   bool takes;  // the row takes part in the loss
   int yv;      // label column in this contraction, or -1
-  float lse2;
-  float zf;    // 1 + 2 zcoef lse (1 for the plain loss)
+  float lse2;  // lse log2 e; +inf for a row that does not take part
+  float zf;    // 1 + 2 zcoef lse (1 for the plain loss); 0 if not taking part
+  float epsr;  // eps_v, or 0 for a row that does not take part
 
   __device__ __forceinline__ void begin_unit(const Params& p, const GemmGeom& g,
                                              const Unit& t, int r) {
@@ -532,15 +643,18 @@ struct EpiGrad : EpiBase {
     row_ok = row < g.M;
     takes = false;
     yv = -1;
-    lse2 = 0.f;
-    zf = 1.f;
-    if (row_ok) {
+    if (row_ok)
       yv = label_column(p.labels[row], g.N, p.v0, p.v_total, p.ignore_index,
                         &takes);
-      if (takes) {
-        lse2 = p.lse[row] * LOG2E;
-        zf = fmaf(p.var.zloss2, p.lse[row], 1.f);
-      }
+    // a row that does not take part gets 2^-inf * 0 - 0 = +0 everywhere
+    // from the same formula as the others, without a select per element
+    lse2 = INFINITY;
+    zf = 0.f;
+    epsr = 0.f;
+    if (takes) {
+      lse2 = p.lse[row] * LOG2E;
+      zf = fmaf(p.var.zloss2, p.lse[row], 1.f);
+      epsr = p.var.eps_v;
     }
   }
 
@@ -558,25 +672,38 @@ struct EpiGrad : EpiBase {
       tmem_ld64(taddr + c * 64, v);
       const int yo = yv - static_cast<int>(j0);
       uint32_t w0[16], w1[16];
+      if (static_cast<unsigned>(yo) >= 64u) {
+        // no label in this piece (all but ~64 / V of the rows' pieces; the
+        // branch is per row, so a warp rarely takes both sides)
+        const uint64_t c2 = f2pack(LOG2E, LOG2E), l2 = f2pack(-lse2, -lse2);
+        const uint64_t z2 = f2pack(zf, zf), e2 = f2pack(-epsr, -epsr);
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        float gi[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          gi[k] = takes ? fmaf(ex2(fmaf(v[i + k], LOG2E, -lse2)), zf,
-                               -p.var.eps_v)
-                        : 0.f;
-          if (i + k == yo) gi[k] -= p.var.ome;
+        for (int i = 0; i < 64; i += 2) {
+          float x0, x1, g0, g1;
+          f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, l2), x0, x1);
+          f2unpack(fma2(f2pack(ex2(x0), ex2(x1)), z2, e2), g0, g1);
+          if (i < 32)
+            w0[i / 2] = pack_bf16x2(g0, g1);
+          else
+            w1[(i - 32) / 2] = pack_bf16x2(g0, g1);
         }
-        if (i < 32)
-          w0[i / 2] = pack_bf16x2(gi[0], gi[1]);
-        else
-          w1[(i - 32) / 2] = pack_bf16x2(gi[0], gi[1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          float gi[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            gi[k] = fmaf(ex2(fmaf(v[i + k], LOG2E, -lse2)), zf, -epsr);
+            if (i + k == yo) gi[k] -= p.var.ome;
+          }
+          if (i < 32)
+            w0[i / 2] = pack_bf16x2(gi[0], gi[1]);
+          else
+            w1[(i - 32) / 2] = pack_bf16x2(gi[0], gi[1]);
+        }
       }
-      if (wrow0 < g.M) {  // warp-uniform test
-        store_box_words(w0, j0, wrow0, nullptr);
-        if (j0 + 32 < g.N) store_box_words(w1, j0 + 32, wrow0, nullptr);
-      }
+      if (wrow0 < g.M)  // warp-uniform test
+        store_box_pair(w0, w1, j0, wrow0, j0 + 32 < g.N);
     }
   }
 
@@ -618,7 +745,7 @@ struct EpiFused : EpiBase {
                                        int) {
     const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
     // pass 1: tile maximum, label logit (64 columns per TMEM load)
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float mx = -INFINITY;
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
       const int64_t j0 = n0 + c * 64;
@@ -635,24 +762,20 @@ struct EpiFused : EpiBase {
           if (i == yo) zyv = v[i];
         if (row_ok) p.zy[row] = zyv;
       }
-      if (p.part_z != nullptr) {  // warp-uniform
-        float za[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i < nv) za[i & 3] += v[i];
-        zs += (za[0] + za[1]) + (za[2] + za[3]);
-      }
-#pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i < nv) mx[i & 3] = fmaxf(mx[i & 3], v[i] * LOG2E);
+      if (p.part_z != nullptr) zs += piece_sum(v, nv);  // warp-uniform
+      mx = fmaxf(mx, piece_max(v, nv));
     }
-    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    // pass 2: exponentials relative to the tile maximum. Each 32-column
-    // half of a 64-column load, for the warp's 32 rows, goes through a
-    // shared-memory box (row r at r * 64 bytes, its 16-byte pieces in
-    // 64-byte-swizzle order) and out by one TMA store, which writes whole
-    // rows' segments and drops the rows past M and the columns past N.
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // max(v) log2 e is max(v log2 e) exactly (rounding is monotone)
+    const float mt = mx * LOG2E;
+    // pass 2: exponentials relative to the tile maximum. The two 32-column
+    // halves of a 64-column load, for the warp's 32 rows, go through two
+    // shared-memory boxes (row r at r * 64 bytes, its 16-byte pieces in
+    // 64-byte-swizzle order) and out by two TMA stores, which write whole
+    // rows' segments and drop the rows past M and the columns past N.
+    // the running sums acc[0..3] in two register pairs: a01 = (acc[0],
+    // acc[1]), a23 = (acc[2], acc[3]); column i adds into acc[i & 3]
+    uint64_t a01 = f2pack(0.f, 0.f), a23 = a01;
+    const uint64_t c2 = f2pack(LOG2E, LOG2E), m2n = f2pack(-mt, -mt);
     const int64_t wrow0 = row - static_cast<int64_t>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
@@ -663,22 +786,43 @@ struct EpiFused : EpiBase {
       const int64_t rem = g.N - j0;
       const int nv = rem < 64 ? static_cast<int>(rem) : 64;
       uint32_t w0[16], w1[16];
+      if (nv == 64) {  // warp-uniform: a whole piece, no column guards
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float e0 = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
-        const float e1 = (i + 1 < nv) ? ex2(fmaf(v[i + 1], LOG2E, -mt)) : 0.f;
-        acc[i & 3] += e0;
-        acc[(i + 1) & 3] += e1;
-        if (i < 32)
-          w0[i / 2] = pack_bf16x2(e0, e1);
-        else
-          w1[(i - 32) / 2] = pack_bf16x2(e0, e1);
+        for (int i = 0; i < 64; i += 2) {
+          float x0, x1;
+          f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, m2n), x0, x1);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          if ((i & 2) == 0)
+            a01 = add2(a01, f2pack(e0, e1));
+          else
+            a23 = add2(a23, f2pack(e0, e1));
+          if (i < 32)
+            w0[i / 2] = pack_bf16x2(e0, e1);
+          else
+            w1[(i - 32) / 2] = pack_bf16x2(e0, e1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = (i < nv) ? ex2(fmaf(v[i], LOG2E, -mt)) : 0.f;
+          const float e1 =
+              (i + 1 < nv) ? ex2(fmaf(v[i + 1], LOG2E, -mt)) : 0.f;
+          if ((i & 2) == 0)
+            a01 = add2(a01, f2pack(e0, e1));
+          else
+            a23 = add2(a23, f2pack(e0, e1));
+          if (i < 32)
+            w0[i / 2] = pack_bf16x2(e0, e1);
+          else
+            w1[(i - 32) / 2] = pack_bf16x2(e0, e1);
+        }
       }
-      if (wrow0 < g.M) {  // warp-uniform test
-        store_box_words(w0, j0, wrow0, nullptr);
-        if (j0 + 32 < g.N) store_box_words(w1, j0 + 32, wrow0, nullptr);
-      }
+      if (wrow0 < g.M)  // warp-uniform test
+        store_box_pair(w0, w1, j0, wrow0, j0 + 32 < g.N);
     }
+    float acc[4];
+    f2unpack(a01, acc[0], acc[1]);
+    f2unpack(a23, acc[2], acc[3]);
     const float st = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     const float mn = fmaxf(m2, mt);
     s = s * ex2(m2 - mn) + st * ex2(mt - mn);
