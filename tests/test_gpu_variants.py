@@ -7,7 +7,8 @@ entropy against the target (1 - eps) onehot + eps / V; the z-loss adds
 coef * lse^2 per valid row; the mean runs over the valid rows. Both paths
 (recomputing and fused) and both contraction variants, on the small
 workload (fp32 inputs), a ragged multi-tile shape with several backward
-chunks, and a row slice of the 8B head shape (full H and V). With both
+chunks, and row slices of the 8B and 32B head shapes (full H and V; the
+32B slice with its x20 stress rows). With both
 options 0 the _ex calls give the plain calls' bits.
 """
 import ctypes
@@ -29,6 +30,9 @@ CASES = {
     "multi_tile": (Workload("multi_tile", 640, 256, 4100, "bf16", 1.0, 0.05,
                             "uniform", ignore_frac=0.05), 256),
     "qwen3-8b[L=256]": (WORKLOADS["qwen3-8b"].with_rows(256), 0),
+    # the widest head, with its x20 stress rows (the largest logits, so the
+    # largest lse in the z-loss term)
+    "qwen3-32b[L=256]": (WORKLOADS["qwen3-32b"].with_rows(256), 0),
 }
 _CACHE = {}
 
@@ -140,7 +144,8 @@ def test_variants_full_size_sampled_rows():
     launch configuration the benchmark times (fused path, default chunk):
     lse and dH on sampled rows (first, last, an ignored one, random)
     against the oracle's rows of the whole problem (its N over all
-    labels); the recomputing path within the bound of the fused one."""
+    labels); the loss against its definition given lse over every row; the
+    recomputing path within the bound of the fused one."""
     dev = require_gpu()
     import chunked_lm_head_gemm_gb300 as lce
     from tests.gpu_util import GRAD_RFRO, LSE_ATOL, to64
@@ -158,10 +163,27 @@ def test_variants_full_size_sampled_rows():
     assert np.max(np.abs(to64(lse)[rows] - r["lse"])) <= LSE_ATOL
     e = rel_fro(to64(dH[idx]), r["dH"])
     assert e <= GRAD_RFRO, f"sampled dH rows rel Frobenius err {e}"
-    # the loss is plausible: the plain loss plus a positive z-loss term,
-    # minus at most eps times the spread of the logits
+    # the loss from its definition given lse, every row: the mean over
+    # valid rows of lse - (1 - eps) z_y - (eps / V) sum_j z_j + coef lse^2,
+    # with z_y = h_i . W_y and sum_j z_j = h_i . (sum_j W_j) in float64
+    eps, zc = kw["label_smoothing"], kw["z_loss"]
+    valid = (y >= 0) & (y < wl.V)
+    idx_v = torch.nonzero(valid).flatten()
+    zy = torch.zeros(wl.L, dtype=torch.float64, device=dev)
+    for s0 in range(0, idx_v.numel(), 8192):
+        ii = idx_v[s0:s0 + 8192]
+        zy[ii] = (h[ii].double() * W[y[ii]].double()).sum(1)
+    wsum = W.double().sum(0)
+    zsum = torch.cat([h[r0:r0 + 8192].double() @ wsum
+                      for r0 in range(0, wl.L, 8192)])
+    l64 = lse.double()
+    term = l64 - (1 - eps) * zy - eps / wl.V * zsum + zc * l64 ** 2
+    ref_loss = term[valid].mean().item()
+    assert abs(loss.item() - ref_loss) <= 1e-4 * abs(ref_loss)
+    # and plausible against the plain loss: plus the z-loss term, minus at
+    # most eps times the spread of the logits
     plain, _ = lce.forward(h, W, y, workspace=ws)
-    zl = kw["z_loss"] * (lse.double()[y >= 0] ** 2).mean().item()
+    zl = zc * (l64[valid] ** 2).mean().item()
     assert abs(loss.item() - (plain.item() + zl)) < 0.1 * plain.item()
     # the recomputing path agrees with the fused one
     one = torch.ones((), device=dev)
