@@ -11,7 +11,9 @@
  * the label-smoothing / z-loss calls, and compares every output with the
  * float64 oracle (oracle/liblce_oracle.so, linked as test infrastructure)
  * on the same bf16 inputs: loss relative error <= 1e-3, lse absolute error
- * <= 2e-3, dH and dW relative Frobenius error <= 1e-2.
+ * <= 2e-3, dH and dW relative Frobenius error <= 1e-2; then the
+ * sequence-tiled MLP (lce_mlp_forward, lce_mlp_backward) against the MLP
+ * oracle, every output within a relative Frobenius error of 1e-2.
  *
  * Exit status 0 when every check passes, 1 otherwise.
  */
@@ -34,6 +36,12 @@ int lce_oracle_forward_backward(const void *h, const void *W, int dtype,
                                 double *lse, double *zy, double *loss,
                                 int64_t *n_valid, double *dH, double *dW,
                                 const int64_t *vrows, int64_t nvrows);
+
+/* The MLP oracle (oracle/mlp_oracle.c): dy widened to float64. */
+int mlp_oracle(const void *x, const void *Wg, const void *Wu, const void *Wd,
+               int dtype, int64_t L, int64_t H, int64_t I, const double *dy,
+               int nthreads, double *y, double *dx, double *dWg, double *dWu,
+               double *dWd);
 
 static int failures = 0;
 
@@ -251,10 +259,122 @@ static int gpu_checks(void) {
   return failures;
 }
 
+/* The sequence-tiled gated MLP: 200 rows in chunks of 128 (a ragged
+ * second chunk), H 64, I 192; y, dx, dWg, dWu, dWd against the oracle,
+ * relative Frobenius error <= 1e-2 each. */
+static int mlp_checks(void) {
+  const int64_t L = 200, H = 64, I = 192, chunk = 128;
+  const size_t nx = (size_t)(L * H), nw = (size_t)(I * H);
+  uint16_t *x = malloc(nx * 2), *wg = malloc(nw * 2), *wu = malloc(nw * 2),
+           *wd = malloc(nw * 2), *dy = malloc(nx * 2), *yb = malloc(nx * 2),
+           *dxb = malloc(nx * 2);
+  float *dwg = malloc(nw * 4), *dwu = malloc(nw * 4), *dwd = malloc(nw * 4);
+  double *dy64 = malloc(nx * 8), *r[5], *g[5];
+  for (int k = 0; k < 5; ++k) {
+    r[k] = malloc((k < 2 ? nx : nw) * 8);
+    g[k] = malloc((k < 2 ? nx : nw) * 8);
+  }
+  if (!x || !wg || !wu || !wd || !dy || !yb || !dxb || !dwg || !dwu || !dwd ||
+      !dy64 || !r[4] || !g[4]) {
+    printf("FAIL host allocation\n");
+    return 1;
+  }
+  for (size_t i = 0; i < nx; ++i) x[i] = to_bf16((float)lcg_normal());
+  for (size_t i = 0; i < nw; ++i) {
+    wg[i] = to_bf16((float)(0.05 * lcg_normal()));
+    wu[i] = to_bf16((float)(0.05 * lcg_normal()));
+    wd[i] = to_bf16((float)(0.05 * lcg_normal()));
+  }
+  for (size_t i = 0; i < nx; ++i) {
+    dy[i] = to_bf16((float)(0.1 * lcg_normal()));
+    dy64[i] = from_bf16(dy[i]);
+  }
+  void *d_x, *d_wg, *d_wu, *d_wd, *d_dy, *d_y, *d_dx, *d_ws;
+  float *d_dwg, *d_dwu, *d_dwd;
+  const size_t ws_bytes = lce_mlp_workspace_size(L, H, I, chunk);
+  check(ws_bytes > 0, "MLP workspace size");
+  CU(cudaMalloc(&d_x, nx * 2));
+  CU(cudaMalloc(&d_wg, nw * 2));
+  CU(cudaMalloc(&d_wu, nw * 2));
+  CU(cudaMalloc(&d_wd, nw * 2));
+  CU(cudaMalloc(&d_dy, nx * 2));
+  CU(cudaMalloc(&d_y, nx * 2));
+  CU(cudaMalloc(&d_dx, nx * 2));
+  CU(cudaMalloc((void **)&d_dwg, nw * 4));
+  CU(cudaMalloc((void **)&d_dwu, nw * 4));
+  CU(cudaMalloc((void **)&d_dwd, nw * 4));
+  CU(cudaMalloc(&d_ws, ws_bytes));
+  CU(cudaMemcpy(d_x, x, nx * 2, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(d_wg, wg, nw * 2, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(d_wu, wu, nw * 2, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(d_wd, wd, nw * 2, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(d_dy, dy, nx * 2, cudaMemcpyHostToDevice));
+  lce_status st = lce_mlp_forward(d_x, d_wg, d_wu, d_wd, L, H, I, chunk, d_y,
+                                  d_ws, ws_bytes, NULL);
+  if (st == LCE_OK)
+    st = lce_mlp_backward(d_x, d_wg, d_wu, d_wd, d_dy, L, H, I, chunk, d_dx,
+                          d_dwg, d_dwu, d_dwd, d_ws, ws_bytes, NULL);
+  check(st == LCE_OK, "MLP forward + backward return LCE_OK");
+  if (st != LCE_OK) return failures;
+  check(lce_get_error(NULL) == LCE_OK, "MLP: device error word clear");
+  CU(cudaMemcpy(yb, d_y, nx * 2, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(dxb, d_dx, nx * 2, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(dwg, d_dwg, nw * 4, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(dwu, d_dwu, nw * 4, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(dwd, d_dwd, nw * 4, cudaMemcpyDeviceToHost));
+  check(mlp_oracle(x, wg, wu, wd, 0, L, H, I, dy64, 4, r[0], r[1], r[2], r[3],
+                   r[4]) == 0,
+        "MLP oracle ran");
+  for (size_t i = 0; i < nx; ++i) {
+    g[0][i] = from_bf16(yb[i]);
+    g[1][i] = from_bf16(dxb[i]);
+  }
+  for (size_t i = 0; i < nw; ++i) {
+    g[2][i] = dwg[i];
+    g[3][i] = dwu[i];
+    g[4][i] = dwd[i];
+  }
+  const char *names[5] = {"MLP y", "MLP dx", "MLP dWg", "MLP dWu", "MLP dWd"};
+  for (int k = 0; k < 5; ++k) {
+    const double e = rel_fro(g[k], r[k], k < 2 ? nx : nw);
+    char what[80];
+    snprintf(what, sizeof what, "%s within 1e-2 (err %.2e)", names[k], e);
+    check(e <= 1e-2, what);
+  }
+  cudaFree(d_x);
+  cudaFree(d_wg);
+  cudaFree(d_wu);
+  cudaFree(d_wd);
+  cudaFree(d_dy);
+  cudaFree(d_y);
+  cudaFree(d_dx);
+  cudaFree(d_dwg);
+  cudaFree(d_dwu);
+  cudaFree(d_dwd);
+  cudaFree(d_ws);
+  free(x);
+  free(wg);
+  free(wu);
+  free(wd);
+  free(dy);
+  free(yb);
+  free(dxb);
+  free(dwg);
+  free(dwu);
+  free(dwd);
+  free(dy64);
+  for (int k = 0; k < 5; ++k) {
+    free(r[k]);
+    free(g[k]);
+  }
+  return failures;
+}
+
 int main(int argc, char **argv) {
   no_gpu_checks();
   if (argc > 1 && strcmp(argv[1], "--gpu") == 0) {
     if (gpu_checks() != 0 && failures == 0) ++failures;
+    if (mlp_checks() != 0 && failures == 0) ++failures;
   }
   printf("%d failure(s)\n", failures);
   return failures ? 1 : 0;
