@@ -469,7 +469,7 @@ lce_status lce_test_wait_timeout(uint64_t timeout_ns, void* stream);
  * replays) race and give wrong results; order them on one stream.
  * It runs the single-CTA contraction without wave pacing, and at most as
  * many column splits as the array holds at this L (15 at L = 131072), so
- * it is somewhat slower than lce_forward: 96.9 against 91.2 ms at
+ * it is somewhat slower than lce_forward: 96.3 against 88.9 ms at
  * L = 131072, H = 4096, V = 151936 on a GB300.
  */
 lce_status lce_forward_static(const void* h, const void* W,
