@@ -14,6 +14,7 @@ include/lce.h; this package is the thin Python binding.
     loss, lse, dH, dW = lce.forward_backward(h, W, labels)  # no recompute
     y = lce.mlp_forward(x, Wg, Wu, Wd)          # sequence-tiled gated MLP
     dx, dWg, dWu, dWd = lce.mlp_backward(x, Wg, Wu, Wd, dy)
+    y = lce.sequence_tiled_mlp(x, Wg, Wu, Wd)   # the same, autograd-aware
     from chunked_lm_head_gemm_gb300 import sharded   # rows split over ranks
     loss, lse, dH, dW = sharded.forward_backward(h, W, labels, group)
     from chunked_lm_head_gemm_gb300 import vocab_parallel as vp  # head split
@@ -22,16 +23,17 @@ include/lce.h; this package is the thin Python binding.
                                group)
 """
 from ._binding import (IGNORE_INDEX, LCEError, LinearCrossEntropy,
-                       alloc_workspace, backward, count_valid,
+                       SequenceTiledMLP, alloc_workspace, backward, count_valid,
                        default_chunk_rows, forward, forward_backward,
                        get_error, library_path, linear_cross_entropy, load,
                        mlp_backward, mlp_forward, mlp_workspace_size,
                        profile_start, profile_stop, scale_gradients,
-                       workspace_size)
+                       sequence_tiled_mlp, workspace_size)
 
-__all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "alloc_workspace",
+__all__ = ["IGNORE_INDEX", "LCEError", "LinearCrossEntropy", "SequenceTiledMLP",
+           "alloc_workspace",
            "backward", "count_valid", "default_chunk_rows", "forward",
            "forward_backward", "get_error", "library_path",
            "linear_cross_entropy", "load", "mlp_backward", "mlp_forward",
            "mlp_workspace_size", "profile_start", "profile_stop",
-           "scale_gradients", "workspace_size"]
+           "scale_gradients", "sequence_tiled_mlp", "workspace_size"]

@@ -780,6 +780,34 @@ class LinearCrossEntropy(torch.autograd.Function):
         return dH, dW.to(ctx.w_dtype), None, None, None, None, None, None
 
 
+class SequenceTiledMLP(torch.autograd.Function):
+    """y = down(silu(gate(x)) * up(x)) over row chunks, as an autograd
+    Function: forward keeps only its inputs (no L x I intermediate outlives
+    a chunk); backward recomputes each chunk's gate/up activations in the
+    library and returns dx (bf16) and the three weight gradients in the
+    weights' dtype. dy is made a contiguous bf16 tensor first."""
+
+    @staticmethod
+    def forward(ctx, x, Wg, Wu, Wd, chunk_rows=0):
+        ctx.chunk_rows = chunk_rows
+        ctx.save_for_backward(x, Wg, Wu, Wd)
+        return mlp_forward(x, Wg, Wu, Wd, chunk_rows)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, Wg, Wu, Wd = ctx.saved_tensors
+        dy = dy.to(torch.bfloat16).contiguous()
+        dx, dWg, dWu, dWd = mlp_backward(x, Wg, Wu, Wd, dy, ctx.chunk_rows)
+        return (dx, dWg.to(Wg.dtype), dWu.to(Wu.dtype), dWd.to(Wd.dtype),
+                None)
+
+
+def sequence_tiled_mlp(x, Wg, Wu, Wd, chunk_rows: int = 0):
+    """The gated MLP down(silu(gate(x)) * up(x)) (nn.Linear weight layouts:
+    Wg, Wu [I, H], Wd [H, I]; bf16) with autograd, over row chunks."""
+    return SequenceTiledMLP.apply(x, Wg, Wu, Wd, chunk_rows)
+
+
 def linear_cross_entropy(h, W, labels, ignore_index: int = IGNORE_INDEX,
                          chunk_rows: int = 0, fused: bool = False,
                          label_smoothing: float = 0.0, z_loss: float = 0.0):

@@ -97,7 +97,35 @@ struct DeviceInfo {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 
+// The driver calls a launch makes (tensor-map encoding) need a CUDA context
+// current on the calling thread. A thread that has made no runtime call yet
+// (for instance an autograd worker whose framework skipped setting the
+// device it already reported) may have none; the runtime would make its
+// device's primary context current at its first call that needs one, so do
+// that here, and only then (a context the caller made current is kept).
+lce_status ensure_context() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (get_current && get_current(&ctx) == CUDA_SUCCESS && ctx) return LCE_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  return e == cudaSuccess ? LCE_OK : cuda_fail(e, "cudaSetDevice");
+}
+
 lce_status device_info(DeviceInfo** out) {
+  const lce_status cs = ensure_context();
+  if (cs != LCE_OK) return cs;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
