@@ -44,7 +44,10 @@
  *   - Results are deterministic: no floating-point atomics; fixed reduction
  *     orders for a fixed shape, dtype and chunk_rows.
  *   - The functions are thread-safe for distinct workspaces; calls that
- *     share a workspace must be ordered on one stream.
+ *     share a workspace must be ordered on one stream. The device is the
+ *     calling thread's current one; a thread with no CUDA context current
+ *     yet gets its current device's primary context made current by the
+ *     first call (a context the caller made current is kept).
  */
 #ifndef LCE_H_
 #define LCE_H_
