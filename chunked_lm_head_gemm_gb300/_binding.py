@@ -296,9 +296,11 @@ def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
              lse: torch.Tensor, dloss: torch.Tensor,
              ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
              workspace=None, dH_out=None, dW_out=None,
-             label_smoothing: float = 0.0, z_loss: float = 0.0):
+             label_smoothing: float = 0.0, z_loss: float = 0.0,
+             compute_dH: bool = True, compute_dW: bool = True):
     """Returns (dH [L,H] of h's dtype, dW [V,H] fp32). The loss variant
-    must be the forward's."""
+    must be the forward's. compute_dH / compute_dW = False skips that
+    gradient's contraction (returned as None; at least one is needed)."""
     lib = load()
     _check_inputs(h, W, labels)
     L, H = h.shape
@@ -309,25 +311,41 @@ def backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
     dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
     if workspace is None:
         workspace = alloc_workspace(L, H, V, h.dtype, chunk_rows, dev)
-    dH = dH_out if dH_out is not None else torch.empty_like(h)
-    dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
+    dH, dW = _grad_outputs(h, V, dH_out, dW_out, compute_dH, compute_dW)
     opts = _opts(label_smoothing, z_loss)
     if opts is None:
         st = lib.lce_backward(h.data_ptr(), W.data_ptr(), _dtype_code(h),
                               labels.data_ptr(), lse.data_ptr(), L, H, V,
                               ignore_index, dloss.data_ptr(), chunk_rows,
-                              dH.data_ptr(), dW.data_ptr(),
-                              workspace.data_ptr(), workspace.numel(),
-                              _stream_ptr(dev))
+                              _ptr(dH), _ptr(dW), workspace.data_ptr(),
+                              workspace.numel(), _stream_ptr(dev))
         _check(st, "lce_backward")
     else:
         st = lib.lce_backward_ex(h.data_ptr(), W.data_ptr(), _dtype_code(h),
                                  labels.data_ptr(), lse.data_ptr(), L, H, V,
                                  ignore_index, opts, dloss.data_ptr(),
-                                 chunk_rows, dH.data_ptr(), dW.data_ptr(),
+                                 chunk_rows, _ptr(dH), _ptr(dW),
                                  workspace.data_ptr(), workspace.numel(),
                                  _stream_ptr(dev))
         _check(st, "lce_backward_ex")
+    return dH, dW
+
+
+def _ptr(t):
+    """A tensor's device pointer, or None (NULL) for an absent one."""
+    return None if t is None else t.data_ptr()
+
+
+def _grad_outputs(h, V, dH_out, dW_out, compute_dH, compute_dW):
+    """The dH [L,H] (h's dtype) and dW [V,H] fp32 outputs, None where the
+    gradient is not wanted."""
+    L, H = h.shape
+    dH = dW = None
+    if compute_dH:
+        dH = dH_out if dH_out is not None else torch.empty_like(h)
+    if compute_dW:
+        dW = dW_out if dW_out is not None else torch.empty(
+            V, H, dtype=torch.float32, device=h.device)
     return dH, dW
 
 
@@ -335,9 +353,11 @@ def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
                      ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
                      workspace=None, loss_out=None, lse_out=None, dH_out=None,
                      dW_out=None, label_smoothing: float = 0.0,
-                     z_loss: float = 0.0):
+                     z_loss: float = 0.0, compute_dH: bool = True,
+                     compute_dW: bool = True):
     """Loss, lse and the gradients of the loss itself (dloss = 1) in one
-    call, without recomputing the logits. Returns (loss, lse, dH, dW)."""
+    call, without recomputing the logits. Returns (loss, lse, dH, dW);
+    compute_dH / compute_dW = False skips that gradient (None)."""
     lib = load()
     _check_inputs(h, W, labels)
     L, H = h.shape
@@ -347,15 +367,14 @@ def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
         workspace = alloc_workspace(L, H, V, h.dtype, chunk_rows, dev)
     loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float32, device=dev)
     lse = lse_out if lse_out is not None else torch.empty(L, dtype=torch.float32, device=dev)
-    dH = dH_out if dH_out is not None else torch.empty_like(h)
-    dW = dW_out if dW_out is not None else torch.empty(V, H, dtype=torch.float32, device=dev)
+    dH, dW = _grad_outputs(h, V, dH_out, dW_out, compute_dH, compute_dW)
     opts = _opts(label_smoothing, z_loss)
     if opts is None:
         st = lib.lce_forward_backward(h.data_ptr(), W.data_ptr(),
                                       _dtype_code(h), labels.data_ptr(), L, H,
                                       V, ignore_index, chunk_rows,
                                       loss.data_ptr(), lse.data_ptr(),
-                                      dH.data_ptr(), dW.data_ptr(),
+                                      _ptr(dH), _ptr(dW),
                                       workspace.data_ptr(), workspace.numel(),
                                       _stream_ptr(dev))
         _check(st, "lce_forward_backward")
@@ -364,21 +383,26 @@ def forward_backward(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor,
                                          _dtype_code(h), labels.data_ptr(), L,
                                          H, V, ignore_index, opts, chunk_rows,
                                          loss.data_ptr(), lse.data_ptr(),
-                                         dH.data_ptr(), dW.data_ptr(),
+                                         _ptr(dH), _ptr(dW),
                                          workspace.data_ptr(),
                                          workspace.numel(), _stream_ptr(dev))
         _check(st, "lce_forward_backward_ex")
     return loss, lse, dH, dW
 
 
-def scale_gradients(dH: torch.Tensor, dW: torch.Tensor, dloss: torch.Tensor):
-    """dH *= dloss and dW *= dloss in place (dloss a device scalar)."""
-    L, H = dH.shape
-    V = dW.shape[0]
-    dloss = dloss.reshape(1).to(device=dH.device, dtype=torch.float32).contiguous()
-    st = load().lce_scale_gradients(dH.data_ptr(), _dtype_code(dH), L, H,
-                                    dW.data_ptr(), V, dloss.data_ptr(),
-                                    _stream_ptr(dH.device))
+def scale_gradients(dH, dW, dloss: torch.Tensor):
+    """dH *= dloss and dW *= dloss in place (dloss a device scalar); either
+    gradient may be None."""
+    ref = dH if dH is not None else dW
+    if ref is None:
+        return dH, dW
+    L, H = dH.shape if dH is not None else (1, dW.shape[1])
+    V = dW.shape[0] if dW is not None else 1
+    code = _dtype_code(dH) if dH is not None else LCE_BF16
+    dloss = dloss.reshape(1).to(device=ref.device,
+                                dtype=torch.float32).contiguous()
+    st = load().lce_scale_gradients(_ptr(dH), code, L, H, _ptr(dW), V,
+                                    dloss.data_ptr(), _stream_ptr(ref.device))
     _check(st, "lce_scale_gradients")
     return dH, dW
 
@@ -759,25 +783,36 @@ class LinearCrossEntropy(torch.autograd.Function):
         ctx.fused = fused
         ctx.w_dtype = W.dtype
         ctx.variant = dict(label_smoothing=label_smoothing, z_loss=z_loss)
-        if fused:
+        # only the gradients autograd asks for are computed (a frozen head:
+        # no dW contraction)
+        ctx.want = dict(compute_dH=ctx.needs_input_grad[0],
+                        compute_dW=ctx.needs_input_grad[1])
+        if fused and any(ctx.want.values()):
             loss, _, dH, dW = forward_backward(h, W, labels, ignore_index,
-                                               chunk_rows, **ctx.variant)
+                                               chunk_rows, **ctx.variant,
+                                               **ctx.want)
             ctx.save_for_backward(dH, dW)
         else:
+            ctx.fused = False
             loss, lse = forward(h, W, labels, ignore_index, **ctx.variant)
             ctx.save_for_backward(h, W, labels, lse)
         return loss
 
     @staticmethod
     def backward(ctx, dloss):
+        if not any(ctx.want.values()):
+            return None, None, None, None, None, None, None, None
         if ctx.fused:
             kept_dH, kept_dW = ctx.saved_tensors
-            dH, dW = scale_gradients(kept_dH.clone(), kept_dW.clone(), dloss)
+            dH, dW = scale_gradients(
+                kept_dH.clone() if kept_dH is not None else None,
+                kept_dW.clone() if kept_dW is not None else None, dloss)
         else:
             h, W, labels, lse = ctx.saved_tensors
             dH, dW = backward(h, W, labels, lse, dloss, ctx.ignore_index,
-                              ctx.chunk_rows, **ctx.variant)
-        return dH, dW.to(ctx.w_dtype), None, None, None, None, None, None
+                              ctx.chunk_rows, **ctx.variant, **ctx.want)
+        return (dH, dW.to(ctx.w_dtype) if dW is not None else None, None,
+                None, None, None, None, None)
 
 
 class SequenceTiledMLP(torch.autograd.Function):

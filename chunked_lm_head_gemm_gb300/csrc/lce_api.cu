@@ -797,7 +797,8 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
                          int64_t chunk_rows, void* dH, bool dh_f32, float* dW,
                          void* ws, size_t ws_bytes, void* stream,
                          const VariantGrad& var) {
-  if (!h || !W || !labels || !lse || !dloss || !dH || !dW || !ws)
+  // dH or dW may be NULL (that gradient is not computed), not both
+  if (!h || !W || !labels || !lse || !dloss || (!dH && !dW) || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, V) || chunk_rows < 0) return LCE_ERR_INVALID_ARG;
@@ -859,7 +860,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       if (e != cudaSuccess) return cuda_fail(e, "gemm_grad");
     }
     // (2) dH_c = (dloss/N) G_c W: M = cr, N = H, K = V
-    {
+    if (dH) {
       GemmPlan pl;
       if ((st = plan_gemm({cr, H, V, false, true, G, w.ldg, Wb, H, false},
                           *dev, &pl)) != LCE_OK)
@@ -879,7 +880,7 @@ lce_status backward_impl(const void* h, const void* W, lce_dtype dt,
       if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
     }
     // (3) dW (+)= (dloss/N) G_c^T h_c: M = V, N = H, K = cr
-    {
+    if (dW) {
       GemmPlan pl;
       if ((st = plan_gemm({V, H, cr, true, true, G, w.ldg, hc, H, false},
                           *dev, &pl)) != LCE_OK)
@@ -1148,7 +1149,8 @@ lce_status lce_backward_slice_exp_ex(const void* h, const void* W,
                                      void* stream) {
   Variant var;
   if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
-  if (!h || !W || !labels || !lse || !dloss || !dH_part || !dW || !ws)
+  // dH_part or dW may be NULL (not computed), not both
+  if (!h || !W || !labels || !lse || !dloss || (!dH_part && !dW) || !ws)
     return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, Vs) || v0 < 0 || V_total < 1 || v0 > V_total - Vs)
@@ -1191,7 +1193,7 @@ lce_status lce_backward_slice_exp_ex(const void* h, const void* W,
   }
   if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
   // dH_part = (dloss/N) G W_s: M = L, N = H, K = Vs
-  {
+  if (dH_part) {
     GemmPlan pl;
     if ((st = plan_gemm({L, H, Vs, false, true, E, w.ldg, Wb, H, false},
                         *dev, &pl)) != LCE_OK)
@@ -1211,7 +1213,7 @@ lce_status lce_backward_slice_exp_ex(const void* h, const void* W,
     if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
   }
   // dW_s = (dloss/N) G^T h: M = Vs, N = H, K = L, written once
-  {
+  if (dW) {
     GemmPlan pl;
     if ((st = plan_gemm({Vs, H, L, true, true, E, w.ldg, hb, H, false},
                         *dev, &pl)) != LCE_OK)
@@ -1328,8 +1330,8 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
   Variant var;
   if (!read_variant(opts, &var)) return LCE_ERR_INVALID_ARG;
   const VariantGrad vg = var.grad(V);
-  if (!h || !W || !labels || !loss || !lse || !dH || !dW || !ws)
-    return LCE_ERR_INVALID_ARG;
+  // dH and dW may each be NULL: that gradient is not computed
+  if (!h || !W || !labels || !loss || !lse || !ws) return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, V) || chunk_rows < 0) return LCE_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws) || !aligned16(dH) ||
@@ -1411,7 +1413,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
       block_off += nb;
     }
     // (3) exponentials -> softmax - onehot, in place
-    {
+    if (dH || dW) {
       ProfScope ps(LCE_K_GRAD_FROM_EXP, s);
       e = launch_grad_from_exp(E, w.ldg, tile_max, num_n, lse + c0,
                                labels + c0, cr, V, ignore_index, dev->num_sms,
@@ -1420,7 +1422,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
       if (e != cudaSuccess) return cuda_fail(e, "grad_from_exp");
     }
     // (4) dH_c = G_c W / N
-    {
+    if (dH) {
       GemmPlan pl;
       if ((st = plan_gemm({cr, H, V, false, true, E, w.ldg, Wb, H, false},
                           *dev, &pl)) != LCE_OK)
@@ -1440,7 +1442,7 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
       if (e != cudaSuccess) return cuda_fail(e, "gemm_dH");
     }
     // (5) dW (+)= G_c^T h_c / N
-    {
+    if (dW) {
       GemmPlan pl;
       if ((st = plan_gemm({V, H, cr, true, true, E, w.ldg, hc, H, false},
                           *dev, &pl)) != LCE_OK)
@@ -1472,19 +1474,21 @@ lce_status lce_forward_backward_ex(const void* h, const void* W, lce_dtype dt,
 lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
                                float* dW, int64_t V, const float* dloss,
                                void* stream) {
-  if (!dH || !dW || !dloss) return LCE_ERR_INVALID_ARG;
+  // either gradient may be NULL (not scaled)
+  if (!dloss) return LCE_ERR_INVALID_ARG;
   if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_UNSUPPORTED;
   if (!sizes_ok(L, H, V)) return LCE_ERR_INVALID_ARG;
   if (!aligned16(dH) || !aligned16(dW) ||
       (reinterpret_cast<uintptr_t>(dloss) & 3u))
     return LCE_ERR_INVALID_ARG;
+  if (!dH && !dW) return LCE_OK;  // nothing to scale
   DeviceInfo* dev = nullptr;
   lce_status st = device_info(&dev);
   if (st != LCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope ps(LCE_K_SCALE_GRADS, s);
-  cudaError_t e = launch_scale_grads(dH, dt == LCE_F32, L * H, dW, V * H,
-                                     dloss, s);
+  cudaError_t e = launch_scale_grads(dH, dt == LCE_F32, dH ? L * H : 0, dW,
+                                     dW ? V * H : 0, dloss, s);
   ps.done(0);
   return e == cudaSuccess ? LCE_OK : cuda_fail(e, "scale_grads");
 }

@@ -117,6 +117,9 @@ lce_status lce_forward(const void* h, const void* W, lce_dtype dt,
  *   chunk_rows rows per chunk (multiple of 128, or 0 for the default)
  *   dH         device, [L][H] of dt, overwritten
  *   dW         device, [V][H] float32, overwritten
+ *   Either of dH, dW may be NULL (not both): that gradient is not computed
+ *   and its contraction is skipped (a frozen head: dW NULL, about a third
+ *   of the backward's flops saved); the other is the same, bit for bit.
  * For each chunk of rows: one tensor-core kernel recomputes the chunk's
  * logits and writes bf16 (softmax - onehot) into the workspace, one computes
  * the chunk's dH rows, one adds the chunk's contribution into dW (fp32
@@ -143,6 +146,8 @@ lce_status lce_backward(const void* h, const void* W, lce_dtype dt,
  *   Arguments as lce_forward and lce_backward; loss, lse, dH and dW are all
  *   outputs, the gradients being those of the loss itself (dloss = 1).
  *   Scale them afterwards with lce_scale_gradients for another dloss.
+ *   dH and dW may each be NULL: that gradient's contraction is skipped
+ *   (both NULL: only the forward's outputs, from the fused logits pass).
  * The softmax is rounded to bf16 as exp(z - tile max) before being
  * rescaled, so G differs from lce_backward's by bf16 rounding only.
  */
@@ -155,8 +160,8 @@ lce_status lce_forward_backward(const void* h, const void* W, lce_dtype dt,
 
 /*
  * dH *= dloss[0] and dW *= dloss[0] in place (dH of dtype dt, [L][H]; dW
- * fp32 [V][H]; dloss a device float). Nothing is done when dloss[0] is
- * exactly 1. For gradients from lce_forward_backward under another upstream
+ * fp32 [V][H]; dloss a device float; either gradient may be NULL and is
+ * then left out). Nothing is done when dloss[0] is exactly 1. For gradients from lce_forward_backward under another upstream
  * gradient; bf16 dH is rounded again after the multiply.
  */
 lce_status lce_scale_gradients(void* dH, lce_dtype dt, int64_t L, int64_t H,
@@ -265,6 +270,7 @@ lce_status lce_combine_slices(const float* m, const float* s, const float* zy,
  *   dH_part  device [L][H] float32 out: G_s W_s; the sum over the slices is
  *            dH (the caller's all-reduce)
  *   dW       device [Vs][H] float32 out: this slice's rows of dW
+ *   either of dH_part, dW may be NULL (not both), as in lce_backward
  *   other arguments as lce_forward_slice and lce_backward
  */
 lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
@@ -290,7 +296,8 @@ lce_status lce_backward_slice(const void* h, const void* W, lce_dtype dt,
  * and a 151936 / 8 slice).
  *   ws  lce_slice_exp_workspace_size(L, H, Vs, dt) bytes, the same buffer
  *       for both calls and untouched in between; other arguments as
- *       lce_forward_slice and lce_backward_slice.
+ *       lce_forward_slice and lce_backward_slice (dH_part or dW may be
+ *       NULL, not both).
  */
 size_t lce_slice_exp_workspace_size(int64_t L, int64_t H, int64_t Vs,
                                     lce_dtype dt);

@@ -172,6 +172,18 @@ def test_bad_arguments_return_before_any_device_call(lib):
                                      null) == 1
     assert lib.lce_backward_slice_exp_ex(p, p, 0, p, p, 8, 8, 8, 0, 10, -100,
                                          smooth, p, p, p, p, 16, null) == 3
+    # optional gradients: the backward wants at least one of dH, dW; the
+    # scale call with neither has nothing to do
+    assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, 0, null, null, p,
+                            1 << 30, null) == 1
+    assert lib.lce_backward_slice(p, p, 0, p, p, 8, 8, 8, 0, 10, -100, p, 0,
+                                  null, null, p, 1 << 30, null) == 1
+    assert lib.lce_backward_slice_exp(p, p, 0, p, p, 8, 8, 8, 0, 10, -100, p,
+                                      null, null, p, 1 << 30, null) == 1
+    assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, 0, null, p, p,
+                            16, null) == 3   # dH skipped: the workspace next
+    assert lib.lce_scale_gradients(null, 0, 8, 8, null, 8, p, null) == 0
+    assert lib.lce_scale_gradients(null, 0, 8, 8, null, 8, null, null) == 1
     # the shard combine: null or misaligned pointers
     assert lib.lce_shard_sums(null, p, p, null) == 1
     assert lib.lce_shard_sums(p, p, ctypes.c_void_p(0x1004), null) == 1

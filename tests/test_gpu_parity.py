@@ -9,7 +9,7 @@ import oracle
 from chunked_lm_head_gemm_gb300.inputs import (WORKLOADS, Workload,
                                                make_inputs)
 from tests.gpu_util import (MODES, PAIRS, assert_parity, rel_fro,
-                            require_gpu, run_gpu)
+                            require_gpu, run_gpu, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -229,3 +229,79 @@ def test_multichunk_row_slice_of_head_shape(name, rows, mode, pair):
     vrows = _touched_vocab_rows(y, wl.V)
     f, b = _slice_oracle((name, rows), h, W, y, vrows)
     assert_parity(gpu, f, b, dW_rows=vrows)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_optional_gradients(mode):
+    """Skipping dW (a frozen head) or dH skips that contraction and leaves
+    the other gradient, the loss and lse with the full call's bits; with
+    neither, the fused call still gives the loss and lse, and the
+    recomputing backward refuses the call."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = Workload("optional", 640, 128, 4100, "bf16", 1.0, 0.05, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=9, device=dev)
+    d = torch.full((), 0.5, device=dev)
+
+    def run(cdh, cdw):
+        if mode == "fused":
+            loss, lse, dH, dW = lce.forward_backward(
+                h, W, y, chunk_rows=256, compute_dH=cdh, compute_dW=cdw)
+            lce.scale_gradients(dH, dW, d)
+        else:
+            loss, lse = lce.forward(h, W, y)
+            dH, dW = lce.backward(h, W, y, lse, d, chunk_rows=256,
+                                  compute_dH=cdh, compute_dW=cdw)
+        return loss, lse, dH, dW
+
+    full = run(True, True)
+    only_dH = run(True, False)
+    only_dW = run(False, True)
+    assert only_dH[3] is None and only_dW[2] is None
+    assert torch.equal(only_dH[2], full[2])
+    assert torch.equal(only_dW[3], full[3])
+    for part in (only_dH, only_dW):
+        assert torch.equal(part[0], full[0]) and torch.equal(part[1], full[1])
+    if mode == "fused":
+        loss, lse, dH, dW = lce.forward_backward(h, W, y, chunk_rows=256,
+                                                 compute_dH=False,
+                                                 compute_dW=False)
+        assert dH is None and dW is None
+        assert torch.equal(loss, full[0]) and torch.equal(lse, full[1])
+    else:
+        with pytest.raises(lce.LCEError):
+            lce.backward(h, W, y, full[1], d, compute_dH=False,
+                         compute_dW=False)
+    assert lce.get_error() == 0
+    f, b = _oracle(h, W, y, dloss=0.5)
+    gpu = dict(loss=full[0].item(), lse=to64(full[1]), dH=to64(only_dH[2]),
+               dW=to64(only_dW[3]), status=0)
+    assert_parity(gpu, f, b)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["recompute", "fused"])
+def test_autograd_frozen_head_or_input(fused):
+    """The autograd Function computes only the gradients autograd asks for:
+    a frozen head (W without grad) gives h.grad with the bits of the full
+    call's dH and no W.grad; a frozen input the converse."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = Workload("frozen", 300, 64, 900, "bf16", 1.0, 0.1, "uniform",
+                  ignore_frac=0.1)
+    h, W, y = make_inputs(wl, seed=10, device=dev)
+    one = torch.ones((), device=dev)
+    if fused:
+        _, _, dH, dW = lce.forward_backward(h, W, y)
+    else:
+        _, lse = lce.forward(h, W, y)
+        dH, dW = lce.backward(h, W, y, lse, one)
+    hh = h.clone().requires_grad_(True)
+    loss = lce.linear_cross_entropy(hh, W, y, fused=fused)
+    loss.backward()
+    assert torch.equal(hh.grad, dH)
+    WW = W.clone().requires_grad_(True)
+    loss = lce.linear_cross_entropy(h, WW, y, fused=fused)
+    loss.backward()
+    assert torch.equal(WW.grad, dW.to(W.dtype))
+    assert lce.get_error() == 0
