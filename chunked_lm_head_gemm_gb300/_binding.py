@@ -703,9 +703,13 @@ def mlp_forward(x, Wg, Wu, Wd, chunk_rows: int = 0, workspace=None,
 
 
 def mlp_backward(x, Wg, Wu, Wd, dy, chunk_rows: int = 0, workspace=None,
-                 dx_out=None, dWg_out=None, dWu_out=None, dWd_out=None):
+                 dx_out=None, dWg_out=None, dWu_out=None, dWd_out=None,
+                 compute_dx: bool = True, compute_dWgu: bool = True,
+                 compute_dWd: bool = True):
     """Returns (dx bf16 [L,H], dWg fp32 [I,H], dWu fp32 [I,H], dWd fp32
-    [H,I]) for upstream gradient dy, recomputing the chunk intermediates."""
+    [H,I]) for upstream gradient dy, recomputing the chunk intermediates.
+    compute_dx / compute_dWgu (dWg and dWu) / compute_dWd = False skips
+    that gradient's contraction (returned as None)."""
     lib = load()
     L, H, I = _check_mlp(x, Wg, Wu, Wd)
     if not (dy.is_cuda and dy.dtype == torch.bfloat16 and dy.is_contiguous()
@@ -715,17 +719,20 @@ def mlp_backward(x, Wg, Wu, Wd, dy, chunk_rows: int = 0, workspace=None,
     if workspace is None:
         workspace = torch.empty(mlp_workspace_size(L, H, I, chunk_rows),
                                 dtype=torch.uint8, device=dev)
-    dx = dx_out if dx_out is not None else torch.empty_like(x)
     f32 = dict(dtype=torch.float32, device=dev)
-    dWg = dWg_out if dWg_out is not None else torch.empty(I, H, **f32)
-    dWu = dWu_out if dWu_out is not None else torch.empty(I, H, **f32)
-    dWd = dWd_out if dWd_out is not None else torch.empty(H, I, **f32)
+    dx = dWg = dWu = dWd = None
+    if compute_dx:
+        dx = dx_out if dx_out is not None else torch.empty_like(x)
+    if compute_dWgu:
+        dWg = dWg_out if dWg_out is not None else torch.empty(I, H, **f32)
+        dWu = dWu_out if dWu_out is not None else torch.empty(I, H, **f32)
+    if compute_dWd:
+        dWd = dWd_out if dWd_out is not None else torch.empty(H, I, **f32)
     st = lib.lce_mlp_backward(x.data_ptr(), Wg.data_ptr(), Wu.data_ptr(),
                               Wd.data_ptr(), dy.data_ptr(), L, H, I,
-                              chunk_rows, dx.data_ptr(), dWg.data_ptr(),
-                              dWu.data_ptr(), dWd.data_ptr(),
-                              workspace.data_ptr(), workspace.numel(),
-                              _stream_ptr(dev))
+                              chunk_rows, _ptr(dx), _ptr(dWg), _ptr(dWu),
+                              _ptr(dWd), workspace.data_ptr(),
+                              workspace.numel(), _stream_ptr(dev))
     _check(st, "lce_mlp_backward")
     return dx, dWg, dWu, dWd
 
@@ -820,7 +827,8 @@ class SequenceTiledMLP(torch.autograd.Function):
     Function: forward keeps only its inputs (no L x I intermediate outlives
     a chunk); backward recomputes each chunk's gate/up activations in the
     library and returns dx (bf16) and the three weight gradients in the
-    weights' dtype. dy is made a contiguous bf16 tensor first."""
+    weights' dtype, computing only those autograd asks for. dy is made a
+    contiguous bf16 tensor first."""
 
     @staticmethod
     def forward(ctx, x, Wg, Wu, Wd, chunk_rows=0):
@@ -831,10 +839,19 @@ class SequenceTiledMLP(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         x, Wg, Wu, Wd = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        if not any(need[:4]):
+            return None, None, None, None, None
         dy = dy.to(torch.bfloat16).contiguous()
-        dx, dWg, dWu, dWd = mlp_backward(x, Wg, Wu, Wd, dy, ctx.chunk_rows)
-        return (dx, dWg.to(Wg.dtype), dWu.to(Wu.dtype), dWd.to(Wd.dtype),
-                None)
+        # only the gradients autograd asks for (frozen weights: dx alone)
+        dx, dWg, dWu, dWd = mlp_backward(x, Wg, Wu, Wd, dy, ctx.chunk_rows,
+                                         compute_dx=need[0],
+                                         compute_dWgu=need[1] or need[2],
+                                         compute_dWd=need[3])
+        cast = [t.to(w.dtype) if (t is not None and n) else None
+                for t, w, n in ((dWg, Wg, need[1]), (dWu, Wu, need[2]),
+                                (dWd, Wd, need[3]))]
+        return (dx, cast[0], cast[1], cast[2], None)
 
 
 def sequence_tiled_mlp(x, Wg, Wu, Wd, chunk_rows: int = 0):

@@ -1708,8 +1708,12 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
                             void* ws, size_t ws_bytes, void* stream) {
   lce_status st = mlp_check(x, Wg, Wu, Wd, L, H, I);
   if (st != LCE_OK) return st;
-  if (!dy || !dx || !dWg || !dWu || !dWd || !ws || chunk_rows < 0)
+  // dx, dWd and the pair (dWg, dWu) may each be NULL (not computed); dWg
+  // and dWu come from one contraction, so both or neither; not all
+  if (!dy || !ws || chunk_rows < 0 || (!dWg != !dWu) ||
+      (!dx && !dWg && !dWd))
     return LCE_ERR_INVALID_ARG;
+  const bool need_dgu = dx || dWg;  // dx and [dWg ; dWu] read [dg | du]
   if (!aligned16(dy) || !aligned16(dx) || !aligned16(dWg) ||
       !aligned16(dWu) || !aligned16(dWd) || !aligned16(ws))
     return LCE_ERR_INVALID_ARG;
@@ -1732,7 +1736,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
                           s)) != LCE_OK)
       return st;
     // (2) da_c = dy_c Wd -> dg_c, du_c into [dg | du]
-    {
+    if (need_dgu) {
       GemmOperands o{cr, I, H, false, true, dyc, H, Wd, I, false};
       GemmPlan pl;
       if ((st = plan_gemm(o, *dev, &pl)) != LCE_OK) return st;
@@ -1752,7 +1756,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
       if (e != cudaSuccess) return cuda_fail(e, "mlp_da");
     }
     // (3) dx_c = [dg | du] [Wg ; Wu]  (K = 2I, B from two maps along K)
-    {
+    if (dx) {
       GemmOperands o{cr, H, 2 * I, false, true, DGU, 2 * I, Wg, H, false};
       o.b_dual = 2;
       o.b2 = Wu;
@@ -1765,7 +1769,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
         return st;
     }
     // (4) dWd (+)= dy_c^T a_c
-    {
+    if (dWd) {
       StoreParams p{};
       p.out = dWd;
       p.ldo = I;
@@ -1776,7 +1780,7 @@ lce_status lce_mlp_backward(const void* x, const void* Wg, const void* Wu,
         return st;
     }
     // (5) [dWg ; dWu] (+)= [dg | du]^T x_c, rows >= I going to dWu
-    {
+    if (dWg) {
       StoreParams p{};
       p.out = dWg;
       p.out2 = dWu;

@@ -500,6 +500,9 @@ lce_status lce_forward_static(const void* h, const void* W,
  *   x   device bf16 [L][H];  Wg, Wu device bf16 [I][H];  Wd device bf16 [H][I]
  *   y   device bf16 [L][H] out;  dy device bf16 [L][H]
  *   dx  device bf16 [L][H] out;  dWg, dWu fp32 [I][H] out;  dWd fp32 [H][I] out
+ *   dx, dWd and the pair (dWg, dWu) may each be NULL, and that gradient's
+ *   contraction is skipped (frozen weights: dx alone); not all of them,
+ *   and dWg, dWu both or neither. The others keep their bits.
  *   H % 8 == 0, I % 64 == 0; chunk_rows 0 = the library's default.
  * The gate and up projections run as one tensor-core contraction (each
  * 256-row B tile is 128 rows of Wg and the same 128 rows of Wu) whose

@@ -183,6 +183,13 @@ def test_bad_arguments_return_before_any_device_call(lib):
     assert lib.lce_backward(p, p, 0, p, p, 8, 8, 8, -100, p, 0, null, p, p,
                             16, null) == 3   # dH skipped: the workspace next
     assert lib.lce_scale_gradients(null, 0, 8, 8, null, 8, p, null) == 0
+    # the MLP: dWg and dWu both or neither; not every gradient left out
+    assert lib.lce_mlp_backward(p, p, p, p, p, 8, 8, 64, 0, p, null, p, p, p,
+                                1 << 30, null) == 1
+    assert lib.lce_mlp_backward(p, p, p, p, p, 8, 8, 64, 0, null, null, null,
+                                null, p, 1 << 30, null) == 1
+    assert lib.lce_mlp_backward(p, p, p, p, p, 8, 8, 64, 0, p, null, null,
+                                null, p, 16, null) == 3  # dx alone: valid
     assert lib.lce_scale_gradients(null, 0, 8, 8, null, 8, null, null) == 1
     # the shard combine: null or misaligned pointers
     assert lib.lce_shard_sums(null, p, p, null) == 1

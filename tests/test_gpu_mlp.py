@@ -140,3 +140,34 @@ def test_mlp_autograd_function():
     got = dict(y=to64(y), dx=to64(grads[0]), dWg=to64(grads[1]),
                dWu=to64(grads[2]), dWd=to64(grads[3]))
     _compare(got, ref)
+
+
+def test_mlp_optional_gradients():
+    """Frozen weights (adapter fine-tuning): dx alone skips the three
+    weight-gradient contractions and keeps the full call's bits; the weight
+    gradients alone, and dWd alone, likewise; under autograd with the
+    weights frozen, x.grad is the full call's dx."""
+    dev = require_gpu()
+    import chunked_lm_head_gemm_gb300 as lce
+    wl = MlpWorkload("opt", 400, 128, 256, 1.0, 0.05)
+    x, Wg, Wu, Wd, dy = make_mlp_inputs(wl, seed=11, device=dev)
+    full = lce.mlp_backward(x, Wg, Wu, Wd, dy, 128)
+    only_dx = lce.mlp_backward(x, Wg, Wu, Wd, dy, 128, compute_dWgu=False,
+                               compute_dWd=False)
+    assert only_dx[1] is None and only_dx[3] is None
+    assert torch.equal(only_dx[0], full[0])
+    only_w = lce.mlp_backward(x, Wg, Wu, Wd, dy, 128, compute_dx=False)
+    assert only_w[0] is None
+    for a, b in zip(only_w[1:], full[1:]):
+        assert torch.equal(a, b)
+    only_wd = lce.mlp_backward(x, Wg, Wu, Wd, dy, 128, compute_dx=False,
+                               compute_dWgu=False)
+    assert torch.equal(only_wd[3], full[3])
+    with pytest.raises(lce.LCEError):
+        lce.mlp_backward(x, Wg, Wu, Wd, dy, 128, compute_dx=False,
+                         compute_dWgu=False, compute_dWd=False)
+    xx = x.clone().requires_grad_(True)
+    y = lce.sequence_tiled_mlp(xx, Wg, Wu, Wd, chunk_rows=128)
+    y.backward(dy)
+    assert torch.equal(xx.grad, full[0])
+    assert lce.get_error() == 0
