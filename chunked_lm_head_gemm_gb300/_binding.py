@@ -556,9 +556,11 @@ def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
                    dloss: torch.Tensor, v0: int, V_total: int,
                    ignore_index: int = IGNORE_INDEX, chunk_rows: int = 0,
                    workspace=None, label_smoothing: float = 0.0,
-                   z_loss: float = 0.0):
+                   z_loss: float = 0.0, compute_dH: bool = True,
+                   compute_dW: bool = True):
     """One vocabulary slice's backward from the merged lse: returns
-    (dH_part [L,H] float32, whose sum over slices is dH; dW_slice [Vs,H])."""
+    (dH_part [L,H] float32, whose sum over slices is dH; dW_slice [Vs,H]);
+    compute_dH / compute_dW = False skips that one (None)."""
     lib = load()
     _check_inputs(h, W_slice, labels)
     L, H = h.shape
@@ -569,15 +571,16 @@ def backward_slice(h: torch.Tensor, W_slice: torch.Tensor,
     dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
     if workspace is None:
         workspace = alloc_workspace(L, H, Vs, h.dtype, chunk_rows, dev)
-    dH = torch.empty(L, H, dtype=torch.float32, device=dev)
-    dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dH = torch.empty(L, H, **f32) if compute_dH else None
+    dW = torch.empty(Vs, H, **f32) if compute_dW else None
     st = lib.lce_backward_slice_ex(h.data_ptr(), W_slice.data_ptr(),
                                    _dtype_code(h), labels.data_ptr(),
                                    lse.data_ptr(), L, H, Vs, v0, V_total,
                                    ignore_index,
                                    _opts(label_smoothing, z_loss),
                                    dloss.data_ptr(), chunk_rows,
-                                   dH.data_ptr(), dW.data_ptr(),
+                                   _ptr(dH), _ptr(dW),
                                    workspace.data_ptr(), workspace.numel(),
                                    _stream_ptr(dev))
     _check(st, "lce_backward_slice")
@@ -615,9 +618,11 @@ def forward_slice_exp(h, W_slice, labels, v0: int, V_total: int, workspace,
 
 def backward_slice_exp(h, W_slice, labels, lse, dloss, v0: int, V_total: int,
                        workspace, ignore_index: int = IGNORE_INDEX,
-                       label_smoothing: float = 0.0, z_loss: float = 0.0):
+                       label_smoothing: float = 0.0, z_loss: float = 0.0,
+                       compute_dH: bool = True, compute_dW: bool = True):
     """The slice's backward from the exponentials forward_slice_exp kept:
-    returns (dH_part [L,H] float32, dW_slice [Vs,H] float32)."""
+    returns (dH_part [L,H] float32, dW_slice [Vs,H] float32), None for a
+    gradient not asked for."""
     lib = load()
     _check_inputs(h, W_slice, labels)
     L, H = h.shape
@@ -626,15 +631,16 @@ def backward_slice_exp(h, W_slice, labels, lse, dloss, v0: int, V_total: int,
     if lse.dtype != torch.float32 or lse.shape != (L,) or not lse.is_cuda:
         raise ValueError("lse must be a CUDA float32 [L] tensor")
     dloss = dloss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
-    dH = torch.empty(L, H, dtype=torch.float32, device=dev)
-    dW = torch.empty(Vs, H, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dH = torch.empty(L, H, **f32) if compute_dH else None
+    dW = torch.empty(Vs, H, **f32) if compute_dW else None
     st = lib.lce_backward_slice_exp_ex(h.data_ptr(), W_slice.data_ptr(),
                                        _dtype_code(h), labels.data_ptr(),
                                        lse.data_ptr(), L, H, Vs, v0, V_total,
                                        ignore_index,
                                        _opts(label_smoothing, z_loss),
-                                       dloss.data_ptr(), dH.data_ptr(),
-                                       dW.data_ptr(), workspace.data_ptr(),
+                                       dloss.data_ptr(), _ptr(dH), _ptr(dW),
+                                       workspace.data_ptr(),
                                        workspace.numel(),
                                        _stream_ptr(dev))
     _check(st, "lce_backward_slice_exp")

@@ -87,14 +87,19 @@ def backward(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
              lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
              group=None, ignore_index: int = B.IGNORE_INDEX,
              chunk_rows: int = 0, workspace=None,
-             label_smoothing: float = 0.0, z_loss: float = 0.0):
+             label_smoothing: float = 0.0, z_loss: float = 0.0,
+             compute_dH: bool = True, compute_dW: bool = True):
     """Returns (dH [L,H] float32, summed over the group; dW of this slice
-    [Vs,H] float32)."""
+    [Vs,H] float32), None for a gradient not asked for (every process must
+    ask for dH alike: its sum is a collective)."""
     dH_part, dW = B.backward_slice(h, W_slice, labels, lse, dloss, v0,
                                    V_total, ignore_index, chunk_rows,
                                    workspace, label_smoothing=label_smoothing,
-                                   z_loss=z_loss)
-    return sum_partials(dH_part, group), dW
+                                   z_loss=z_loss, compute_dH=compute_dH,
+                                   compute_dW=compute_dW)
+    if dH_part is not None:
+        dH_part = sum_partials(dH_part, group)
+    return dH_part, dW
 
 
 def exp_workspace(h: torch.Tensor, W_slice: torch.Tensor) -> torch.Tensor:
@@ -121,13 +126,17 @@ def backward_exp(h: torch.Tensor, W_slice: torch.Tensor, labels: torch.Tensor,
                  lse: torch.Tensor, dloss: torch.Tensor, v0: int, V_total: int,
                  workspace: torch.Tensor, group=None,
                  ignore_index: int = B.IGNORE_INDEX,
-                 label_smoothing: float = 0.0, z_loss: float = 0.0):
+                 label_smoothing: float = 0.0, z_loss: float = 0.0,
+                 compute_dH: bool = True, compute_dW: bool = True):
     """backward from the exponentials forward_exp kept (same workspace)."""
     dH_part, dW = B.backward_slice_exp(h, W_slice, labels, lse, dloss, v0,
                                        V_total, workspace, ignore_index,
                                        label_smoothing=label_smoothing,
-                                       z_loss=z_loss)
-    return sum_partials(dH_part, group), dW
+                                       z_loss=z_loss, compute_dH=compute_dH,
+                                       compute_dW=compute_dW)
+    if dH_part is not None:
+        dH_part = sum_partials(dH_part, group)
+    return dH_part, dW
 
 
 class VocabParallelCrossEntropy(torch.autograd.Function):
@@ -163,17 +172,23 @@ class VocabParallelCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dloss):
         h, W_slice, labels, lse = ctx.saved_tensors
+        want = dict(compute_dH=ctx.needs_input_grad[0],
+                    compute_dW=ctx.needs_input_grad[1])
+        if not any(want.values()):
+            ctx.ws = None
+            return (None,) * 10
         if ctx.keep_exp:
             dH, dW = backward_exp(h, W_slice, labels, lse, dloss, ctx.v0,
                                   ctx.V_total, ctx.ws, ctx.group,
-                                  ctx.ignore_index, **ctx.variant)
+                                  ctx.ignore_index, **ctx.variant, **want)
             ctx.ws = None
         else:
             dH, dW = backward(h, W_slice, labels, lse, dloss, ctx.v0,
                               ctx.V_total, ctx.group, ctx.ignore_index,
-                              **ctx.variant)
-        return (dH.to(ctx.h_dtype), dW.to(ctx.w_dtype), None, None, None,
-                None, None, None, None, None)
+                              **ctx.variant, **want)
+        return (dH.to(ctx.h_dtype) if dH is not None else None,
+                dW.to(ctx.w_dtype) if dW is not None else None, None, None,
+                None, None, None, None, None, None)
 
 
 def vocab_parallel_cross_entropy(h, W_slice, labels, v0: int, V_total: int,

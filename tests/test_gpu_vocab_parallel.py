@@ -307,3 +307,35 @@ def test_autograd_function_one_slice_with_variant(keep):
     assert abs(loss.item() - loss1.item()) <= 1e-6 * abs(loss1.item())
     assert rel_fro(to64(hl.grad), to64(dH1)) <= 8e-3
     assert rel_fro(to64(Wl.grad), to64(dW1)) <= 8e-3
+
+
+@pytest.mark.parametrize("keep", [False, True], ids=["recompute", "keep_exp"])
+def test_slice_optional_gradients(keep):
+    """A frozen head slice (W_slice without grad) computes only dH, with
+    the bits of the full call's dH; a frozen input only the slice's dW."""
+    h, W, y = _inputs("opt_slice", 320, 64, 1500)
+    d = torch.full((), 1.0, device=h.device)
+    Ws = W[:1000].contiguous()
+    if keep:
+        ws = vp.exp_workspace(h, Ws)
+        _, lse = vp.forward_exp(h, Ws, y, 0, 1500, ws)
+        full = vp.backward_exp(h, Ws, y, lse, d, 0, 1500, ws)
+        vp.forward_exp(h, Ws, y, 0, 1500, ws)
+        only_dH = vp.backward_exp(h, Ws, y, lse, d, 0, 1500, ws,
+                                  compute_dW=False)
+        vp.forward_exp(h, Ws, y, 0, 1500, ws)
+        only_dW = vp.backward_exp(h, Ws, y, lse, d, 0, 1500, ws,
+                                  compute_dH=False)
+    else:
+        _, lse = vp.forward(h, Ws, y, 0, 1500)
+        full = vp.backward(h, Ws, y, lse, d, 0, 1500)
+        only_dH = vp.backward(h, Ws, y, lse, d, 0, 1500, compute_dW=False)
+        only_dW = vp.backward(h, Ws, y, lse, d, 0, 1500, compute_dH=False)
+    assert only_dH[1] is None and only_dW[0] is None
+    assert torch.equal(only_dH[0], full[0])
+    assert torch.equal(only_dW[1], full[1])
+    hh = h.clone().requires_grad_(True)
+    loss = vp.vocab_parallel_cross_entropy(hh, Ws, y, 0, 1500, keep_exp=keep)
+    loss.backward()
+    assert torch.equal(hh.grad, full[0].to(h.dtype))
+    assert lce.get_error() == 0
